@@ -1,0 +1,239 @@
+"""The oracle: a plain, slow, obviously-correct CPU statement of paged decode attention.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, ``__graft_entry__.smoke()`` and bench.py's
+cpu_baseline / reference leg may import this package.  It shares no code with the CUDA
+library in ``paged_kv_cache_159_gb300`` and never imports it.
+
+Pieces and the passage each follows (page title, section):
+
+* ``kv_bytes`` -- bytes = 2 * layers * kv_heads * head_dim * elem_bytes * tokens * seqs.
+  "KV Cache 与推理优化" (note.yj-dis.top), section "KV Cache 有多大：一张显存账单";
+  "一个请求为什么越生成越占内存?" (learning-field-guides), section "按 K 与 V 的维度推导容量";
+  "理解 KV Cache" (steinslab.io), §1.4.
+* ``blocks_needed`` / ``block_capacity`` / ``empty_slots`` -- a sequence of n positions
+  takes ceil(n / bs) fixed-size blocks; "一个请求为什么越生成越占内存?", section
+  "分页改变分配方式，不改变独立 token 的表示" (18 positions -> 2 blocks, 14 empty).
+* ``slot_of`` / ``slot_mapping`` -- "理解 KV Cache" (steinslab.io), §3.3 and the §3.4 example.
+* ``BlockAllocator`` / ``build_block_tables`` -- block lifecycle (allocate from a free
+  pool, use, return), "理解 KV Cache" §3.5; block tables mapping logical to physical
+  blocks and shared prefix blocks referenced by many tables, "KV Cache 与推理优化",
+  section "PagedAttention：把 KV Cache 当虚拟内存管".
+* ``kv_append`` / ``paged_decode`` / FP8 codec -- C code in ``pkv_oracle.c`` (fp64).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+BF16 = 0
+FP8E4M3 = 1
+
+_lib = None
+
+
+def lib():
+    """Load (building first if needed) the C part of the oracle."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        L.oracle_e4m3_decode.restype = ctypes.c_double
+        L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_quantize.restype = ctypes.c_uint8
+        L.oracle_e4m3_quantize.argtypes = [ctypes.c_float, ctypes.c_float]
+        L.oracle_kv_append.restype = ctypes.c_int
+        L.oracle_kv_append.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+            ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_paged_decode.restype = ctypes.c_int
+        L.oracle_paged_decode.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+            ctypes.c_float, ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+            ctypes.c_void_p]
+        L.oracle_max_threads.restype = ctypes.c_int
+        L.oracle_max_threads.argtypes = []
+        _lib = L
+    return _lib
+
+
+def max_threads() -> int:
+    return int(lib().oracle_max_threads())
+
+
+# ------------------------------------------------------------------------------------
+# Capacity arithmetic (plain integers).
+# ------------------------------------------------------------------------------------
+def kv_bytes(layers: int, kv_heads: int, head_dim: int, elem_bytes: int,
+             tokens: int = 1, seqs: int = 1) -> int:
+    """K and V bytes: 2 (K and V) x layers x kv_heads x head_dim x elem_bytes x T x N."""
+    return 2 * layers * kv_heads * head_dim * elem_bytes * tokens * seqs
+
+
+def blocks_needed(positions: int, block_size: int) -> int:
+    """Whole blocks a sequence of ``positions`` cached tokens occupies (ceil)."""
+    if positions < 0 or block_size < 1:
+        raise ValueError("positions >= 0 and block_size >= 1 required")
+    return (positions + block_size - 1) // block_size
+
+
+def block_capacity(positions: int, block_size: int) -> int:
+    """Token positions the allocated blocks can hold."""
+    return blocks_needed(positions, block_size) * block_size
+
+
+def empty_slots(positions: int, block_size: int) -> int:
+    """Unused positions in the last block (internal fragmentation, < one block)."""
+    return block_capacity(positions, block_size) - positions
+
+
+# ------------------------------------------------------------------------------------
+# Slot addressing ("理解 KV Cache" §3.3): two-level lookup.
+# ------------------------------------------------------------------------------------
+def slot_of(block_table, i: int, block_size: int):
+    """Return (logical_block, offset, physical_block, slot) for token position i."""
+    logical = i // block_size
+    offset = i % block_size
+    physical = int(block_table[logical])
+    return logical, offset, physical, physical * block_size + offset
+
+
+def slot_mapping(block_tables, seq_lens, block_size: int = 16) -> np.ndarray:
+    """Slot of each sequence's newest token, at position seq_len - 1 (int64 [B])."""
+    out = np.empty(len(seq_lens), dtype=np.int64)
+    for b, L in enumerate(seq_lens):
+        out[b] = slot_of(block_tables[b], int(L) - 1, block_size)[3]
+    return out
+
+
+# ------------------------------------------------------------------------------------
+# Block lifecycle ("理解 KV Cache" §3.5): a free pool handed out in a fixed order,
+# reference counts for blocks that several tables share.
+# ------------------------------------------------------------------------------------
+class BlockAllocator:
+    def __init__(self, num_blocks: int, free_order=None):
+        order = list(range(num_blocks)) if free_order is None else [int(x) for x in free_order]
+        if sorted(order) != list(range(num_blocks)):
+            raise ValueError("free_order must be a permutation of 0..num_blocks-1")
+        self.num_blocks = num_blocks
+        self.free = list(order)          # front of the list is handed out first
+        self.refcount = [0] * num_blocks
+
+    def alloc(self, n: int):
+        if n > len(self.free):
+            raise MemoryError("pool exhausted")
+        ids, self.free = self.free[:n], self.free[n:]
+        for i in ids:
+            self.refcount[i] = 1
+        return ids
+
+    def share(self, ids):
+        for i in ids:
+            if self.refcount[i] < 1:
+                raise ValueError("cannot share a free block")
+            self.refcount[i] += 1
+
+    def release(self, ids):
+        for i in ids:
+            if self.refcount[i] < 1:
+                raise ValueError("double free")
+            self.refcount[i] -= 1
+            if self.refcount[i] == 0:
+                self.free.append(i)
+
+
+def build_block_tables(allocator: BlockAllocator, seq_lens, max_blocks: int,
+                       block_size: int = 16, prefix_ids=()) -> np.ndarray:
+    """One table row per sequence: its first min(len(prefix_ids), nblk) entries are the
+    shared prefix blocks (one more reference each), the rest fresh blocks from the free
+    pool in order; unused entries are -1.  int32 [B, max_blocks]."""
+    prefix_ids = [int(x) for x in prefix_ids]
+    tables = np.full((len(seq_lens), max_blocks), -1, dtype=np.int32)
+    for b, L in enumerate(seq_lens):
+        nblk = blocks_needed(int(L), block_size)
+        if nblk > max_blocks:
+            raise ValueError("sequence longer than its block table")
+        shared = prefix_ids[:nblk]
+        allocator.share(shared)
+        fresh = allocator.alloc(nblk - len(shared))
+        tables[b, :nblk] = shared + fresh
+    return tables
+
+
+def poison_unused(cache: np.ndarray, block_tables, seq_lens, block_size: int, fill_bits: int):
+    """Overwrite every cache position that no sequence may read -- tail slots of each
+    sequence's last block and blocks no table references -- with ``fill_bits`` (a bf16
+    NaN pattern in the tests).  ``cache`` is [num_blocks, Hkv, bs, D] of uint16/uint8."""
+    num_blocks = cache.shape[0]
+    live = np.zeros((num_blocks, block_size), dtype=bool)
+    for b, L in enumerate(seq_lens):
+        for i in range(int(L)):
+            _, off, phys, _ = slot_of(block_tables[b], i, block_size)
+            live[phys, off] = True
+    mask = ~live                                           # [NB, bs]
+    cache[np.broadcast_to(mask[:, None, :, None], cache.shape)] = fill_bits
+    return cache
+
+
+# ------------------------------------------------------------------------------------
+# FP8 E4M3 codec and the fp64 kernels (C).
+# ------------------------------------------------------------------------------------
+def e4m3_decode(code: int) -> float:
+    return float(lib().oracle_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(lib().oracle_e4m3_encode(float(x)))
+
+
+def e4m3_quantize(x: float, scale: float) -> int:
+    return int(lib().oracle_e4m3_quantize(float(x), float(scale)))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def kv_append(k_bits, v_bits, slots, key_cache, value_cache, block_size=16,
+              kv_dtype=BF16, k_scale=1.0, v_scale=1.0) -> int:
+    """Scatter K/V rows (bf16 bit patterns, uint16 [T, Hkv, D]) into the caches in place."""
+    k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    slots = np.ascontiguousarray(slots, dtype=np.int64)
+    assert key_cache.flags.c_contiguous and value_cache.flags.c_contiguous
+    T, Hkv, D = k_bits.shape
+    return int(lib().oracle_kv_append(
+        _ptr(k_bits), _ptr(v_bits), _ptr(slots), T, Hkv, D, block_size, key_cache.shape[0],
+        kv_dtype, k_scale, v_scale, _ptr(key_cache), _ptr(value_cache)))
+
+
+def paged_decode(q_bits, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                 num_kv_heads: int, block_size: int = 16, kv_dtype=BF16, k_scale=1.0,
+                 v_scale=1.0, pairs=None, num_threads: int = 1):
+    """fp64 paged decode attention.  q_bits: uint16 [B, Hq, D] (bf16 patterns).
+    Returns (status, out float64 [B, Hq, D]); with ``pairs`` only those (b, hq) rows of
+    ``out`` are computed (the rest stay zero)."""
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    assert key_cache.flags.c_contiguous and value_cache.flags.c_contiguous
+    B, Hq, D = q_bits.shape
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    if pairs is not None:
+        pairs = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+        pptr, npairs = _ptr(pairs), pairs.shape[0]
+    else:
+        pptr, npairs = None, 0
+    st = lib().oracle_paged_decode(
+        _ptr(q_bits), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), _ptr(seq_lens),
+        B, Hq, num_kv_heads, D, block_tables.shape[1], block_size, key_cache.shape[0],
+        kv_dtype, k_scale, v_scale, scale, pptr, npairs, num_threads, _ptr(out))
+    return int(st), out
