@@ -1,0 +1,195 @@
+/*
+ * pkv.h -- C ABI of the GB300 paged KV-cache decode-attention library (libpkv.so).
+ *
+ * Plain C: host integers and pointers only.  "device pointer" means memory the caller
+ * allocated on the CUDA device the pool is attached to; "host pointer" means ordinary
+ * process memory.  Every function returns a pkv_status (0 = PKV_OK) unless noted.
+ * Kernels run asynchronously on the caller's stream (a cudaStream_t passed as void*,
+ * NULL = the legacy default stream); argument errors are reported before anything is
+ * launched, and violations found on the device (a block id or slot outside the pool, a
+ * sequence length outside its table, a pipeline wait that gave up) set bits in the pool's
+ * device error word, read with pkv_get_device_error().
+ *
+ * Sources (page title, section), cited per entry point below:
+ *   [Slot]    "理解 KV Cache：Attention、P/D 分离与 vLLM 的页式显存管理" (steinslab.io),
+ *             §3.3 slot addressing and the §3.4 example.
+ *   [Layout]  same page, §3.2: a block holds block_size tokens of K and V per KV head,
+ *             head-first ([num_kv_heads, block_size, head_dim]).
+ *   [Life]    same page, §3.5: blocks are allocated from a free pool, used, and returned.
+ *   [Decode]  same page, §1.2-§1.3 and §2.2: the new token's query attends over every
+ *             cached position of its sequence (causal mask), computed as two fused GEMVs.
+ *   [Attn]    "传统 Attention 的 KV Cache 问题" (pyllm.pages.dev), §1.1: scaled softmax
+ *             attention sum_j softmax_j(q.K_j / sqrt(d_k)) V_j.
+ *   [Paged]   "KV Cache 与推理优化" (note.yj-dis.top), section "PagedAttention：把 KV Cache
+ *             当虚拟内存管": 16-token blocks, one block table per request mapping logical to
+ *             physical blocks, shared prefix blocks, the kernel gathering K/V via the table.
+ *   [GQA]     same page, section on MHA/GQA/MQA: query heads share KV heads in contiguous
+ *             groups of g = Hq / Hkv.
+ *   [Quant]   same page, section "KV 量化": K/V stored in FP8 (1 byte) with higher-precision
+ *             arithmetic.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = 1,   /* bad argument; nothing was launched */
+    PKV_ERR_OOM = 2,       /* the pool has fewer free blocks than requested */
+    PKV_ERR_DEVICE = 3,    /* the device error word is non-zero (see PKV_DEVERR_*) */
+    PKV_ERR_TIMEOUT = 4,   /* a kernel's bounded pipeline wait gave up */
+    PKV_ERR_CUDA = 5       /* a CUDA runtime call failed (launch, copy, allocation) */
+} pkv_status;
+
+/* Bits of the device error word. */
+#define PKV_DEVERR_SLOT     0x1u   /* kv_append: slot >= num_blocks * block_size (row skipped) */
+#define PKV_DEVERR_BLOCK_ID 0x2u   /* decode: a needed table entry outside [0, num_blocks) */
+#define PKV_DEVERR_SEQ_LEN  0x4u   /* decode: seq_len outside [1, max_blocks * block_size] */
+#define PKV_DEVERR_TIMEOUT  0x8u   /* a pipeline wait exceeded its bound (about 1 s) */
+
+typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8E4M3 = 1 } pkv_kv_dtype;
+
+/* Shape and element type of one layer's paged K/V pool [Layout]: two caller-owned device
+ * tensors key_cache and value_cache, each [num_blocks, num_kv_heads, block_size, head_dim],
+ * contiguous, 16-byte aligned.  block_size must be 16 [Paged]; head_dim 64 or 128.
+ * FP8 pools store OCP E4M3 codes of x / scale with one scale per tensor [Quant]; k_scale
+ * and v_scale must be positive and finite (ignored for bf16). */
+typedef struct {
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t kv_dtype;      /* pkv_kv_dtype */
+    float k_scale;
+    float v_scale;
+} pkv_pool_desc;
+
+typedef struct pkv_pool pkv_pool;   /* host allocator state + the device error word */
+
+/* Create a pool descriptor and its host block allocator [Life].  free_order (host,
+ * optional) is a permutation of 0..num_blocks-1 giving the order in which free blocks are
+ * handed out; NULL means ascending ids.  Touches no GPU.  *out receives the pool, owned by
+ * the caller until pkv_pool_destroy.  INVALID on a bad descriptor or permutation. */
+int pkv_pool_create(const pkv_pool_desc *desc, const int32_t *free_order, pkv_pool **out);
+
+/* Free the pool, its allocator and (if attached) its device error word. */
+int pkv_pool_destroy(pkv_pool *pool);
+
+/* Copy the pool's descriptor to *out. */
+int pkv_pool_get_desc(const pkv_pool *pool, pkv_pool_desc *out);
+
+/* Number of blocks currently free. */
+int pkv_pool_num_free(const pkv_pool *pool, int32_t *out);
+
+/* Reference count of one block (0 = free). */
+int pkv_pool_refcount(const pkv_pool *pool, int32_t block_id, int32_t *out);
+
+/* Take n blocks from the front of the free list [Life]; ids_out (host, n entries)
+ * receives them, each with reference count 1.  OOM (nothing taken) if fewer than n free. */
+int pkv_pool_alloc(pkv_pool *pool, int32_t n, int32_t *ids_out);
+
+/* Add one reference to each listed block, which must be allocated: a shared prefix block
+ * referenced by several block tables [Paged].  INVALID (nothing changed) otherwise. */
+int pkv_pool_share(pkv_pool *pool, const int32_t *ids, int32_t n);
+
+/* Drop one reference from each listed block; blocks reaching zero return to the back of
+ * the free list [Life].  INVALID (nothing changed) on a free or out-of-range id. */
+int pkv_pool_free(pkv_pool *pool, const int32_t *ids, int32_t n);
+
+/* Build block tables for a batch [Paged][Life]: row b (tables_out is host int32
+ * [batch, max_blocks], row-major) gets ceil(seq_lens[b] / block_size) entries -- first the
+ * shared prefix ids (prefix_ids, host, num_prefix entries, already allocated; one more
+ * reference each, as many as the row needs), then fresh blocks from the free list in
+ * order -- and -1 in unused entries.  seq_lens counts the token appended this step.
+ * INVALID if a length is < 1 or needs more than max_blocks entries; OOM if the pool runs
+ * dry (then every block taken by this call is returned and tables_out is unspecified). */
+int pkv_build_block_tables(pkv_pool *pool, const int32_t *seq_lens, int32_t batch,
+                           int32_t max_blocks, const int32_t *prefix_ids, int32_t num_prefix,
+                           int32_t *tables_out);
+
+/* Slot of each sequence's newest token, at position seq_lens[b]-1 [Slot]:
+ * slot = tables[b][(L-1) / block_size] * block_size + (L-1) % block_size.  Host arrays:
+ * tables int32 [batch, max_blocks], seq_lens int32 [batch], slots_out int64 [batch].
+ * INVALID on a length outside [1, max_blocks*block_size] or a negative table entry. */
+int pkv_slot_mapping(const int32_t *tables, const int32_t *seq_lens, int32_t batch,
+                     int32_t max_blocks, int32_t block_size, int64_t *slots_out);
+
+/* Bind the pool to a CUDA device: allocates its 4-byte device error word (cudaMalloc) on
+ * that device.  Required once before pkv_kv_append / pkv_paged_attention_decode. */
+int pkv_pool_attach_device(pkv_pool *pool, int device);
+
+/* Append K/V rows into their slots [Slot][Decode]: for each token t and KV head h with
+ * slot = slot_mapping[t] >= 0, key_cache[slot/16][h][slot%16][:] = k[t][h][:] (bf16 bit
+ * copy; FP8 pools store E4M3(fl32(k * fl32(1/k_scale))), round-to-nearest-even, saturated
+ * to +-448), likewise V.  Device pointers: k, v bf16 [num_tokens, Hkv, D]; slot_mapping
+ * int64 [num_tokens] (negative = padding, skipped); caches as in pkv_pool_desc.  A slot
+ * beyond the pool sets PKV_DEVERR_SLOT and its row is skipped.  Slots must be distinct. */
+int pkv_kv_append(pkv_pool *pool, const void *k, const void *v, const int64_t *slot_mapping,
+                  int32_t num_tokens, void *key_cache, void *value_cache, void *stream);
+
+/* Tuning knobs for pkv_paged_attention_decode_ex; zero fields mean "choose". */
+typedef struct {
+    int32_t partition_blocks; /* logical blocks per split-KV partition (0 = auto) */
+    int32_t variant;          /* 0 = auto, 1 = CUDA-core dot products, 2 = tensor-core mma */
+    int32_t warps_per_cta;    /* 0 = auto; 1, 2, 4 or 8 */
+    int32_t stages;           /* 0 = auto; per-warp shared-memory pipeline depth 1..4 */
+} pkv_decode_opts;
+
+/* Device workspace needed by the split-KV path for this shape (0 when no sequence can be
+ * split).  Must be called with the same opts as the decode call. */
+size_t pkv_decode_workspace_bytes(const pkv_pool *pool, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_blocks, const pkv_decode_opts *opts);
+
+/* Paged decode attention, one query token per sequence [Decode][Attn][GQA][Paged]:
+ *   out[b][hq][:] = sum_{j < L_b} softmax_j(scale * q[b][hq] . K_j) V_j,
+ *   K_j, V_j = cache[block_tables[b][j / 16]][hq / (Hq/Hkv)][j % 16][:],  L_b = seq_lens[b].
+ * Device pointers: q bf16 [batch, num_q_heads, D]; caches as in pkv_pool_desc;
+ * block_tables int32 [batch, max_blocks]; seq_lens int32 [batch]; out bf16
+ * [batch, num_q_heads, D] (fp32 accumulation, rounded to nearest even); workspace of at
+ * least pkv_decode_workspace_bytes() bytes (may be NULL when that is 0), 256-byte aligned.
+ * Positions j >= L_b are never used, whatever they hold.  Long sequences are split into
+ * partitions whose partial softmax states are merged by a second kernel on the same
+ * stream; the summation order depends only on logical positions, so any physical
+ * placement of the blocks gives bit-identical output.  Requires num_q_heads a multiple of
+ * Hkv with group <= 16, an attached pool, max_blocks >= 1.  FP8 pools compute q.K with
+ * q rounded to fp16 (|q| must stay below 65504). */
+int pkv_paged_attention_decode(pkv_pool *pool, const void *q, const void *key_cache,
+                               const void *value_cache, const int32_t *block_tables,
+                               const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                               int32_t max_blocks, float scale, void *out, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/* Same, with explicit tuning knobs (opts may be NULL). */
+int pkv_paged_attention_decode_ex(pkv_pool *pool, const void *q, const void *key_cache,
+                                  const void *value_cache, const int32_t *block_tables,
+                                  const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_blocks, float scale, void *out, void *workspace,
+                                  size_t workspace_bytes, const pkv_decode_opts *opts,
+                                  void *stream);
+
+/* Synchronise the stream, read the pool's device error word into *bits_out and clear it.
+ * Returns PKV_OK if it was zero, PKV_ERR_TIMEOUT if the timeout bit was set, else
+ * PKV_ERR_DEVICE. */
+int pkv_get_device_error(pkv_pool *pool, void *stream, uint32_t *bits_out);
+
+/* Device-to-device copy of `bytes` (a multiple of 16; both pointers 16-byte aligned) by a
+ * plain streaming kernel: the bandwidth denominator measured in the same process. */
+int pkv_probe_copy(void *dst, const void *src, size_t bytes, void *stream);
+
+/* Number of SMs of a device (used by the partition planner). */
+int pkv_device_sm_count(int device, int32_t *out);
+
+/* Static description of a status code (never NULL). */
+const char *pkv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

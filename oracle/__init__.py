@@ -168,16 +168,34 @@ def build_block_tables(allocator: BlockAllocator, seq_lens, max_blocks: int,
     return tables
 
 
+def live_positions(block_tables, seq_lens, num_blocks: int, block_size: int = 16) -> np.ndarray:
+    """bool [num_blocks, block_size]: True where some sequence's position maps (slot_of)."""
+    live = np.zeros((num_blocks, block_size), dtype=bool)
+    for b, L in enumerate(seq_lens):
+        L = int(L)
+        nblk = blocks_needed(L, block_size)
+        phys = np.asarray(block_tables[b][:nblk], dtype=np.int64)
+        live[phys[:-1], :] = True                          # full blocks
+        last = L - (nblk - 1) * block_size                 # positions in the last block
+        live[phys[-1], :last] = True
+    return live
+
+
+def all_slots(block_tables, seq_lens, block_size: int = 16) -> np.ndarray:
+    """int64 slots of every position 0..L-1 of every sequence, sequence-major."""
+    out = []
+    for b, L in enumerate(seq_lens):
+        i = np.arange(int(L), dtype=np.int64)
+        phys = np.asarray(block_tables[b], dtype=np.int64)[i // block_size]
+        out.append(phys * block_size + i % block_size)
+    return np.concatenate(out) if out else np.zeros(0, np.int64)
+
+
 def poison_unused(cache: np.ndarray, block_tables, seq_lens, block_size: int, fill_bits: int):
     """Overwrite every cache position that no sequence may read -- tail slots of each
     sequence's last block and blocks no table references -- with ``fill_bits`` (a bf16
     NaN pattern in the tests).  ``cache`` is [num_blocks, Hkv, bs, D] of uint16/uint8."""
-    num_blocks = cache.shape[0]
-    live = np.zeros((num_blocks, block_size), dtype=bool)
-    for b, L in enumerate(seq_lens):
-        for i in range(int(L)):
-            _, off, phys, _ = slot_of(block_tables[b], i, block_size)
-            live[phys, off] = True
+    live = live_positions(block_tables, seq_lens, cache.shape[0], block_size)
     mask = ~live                                           # [NB, bs]
     cache[np.broadcast_to(mask[:, None, :, None], cache.shape)] = fill_bits
     return cache

@@ -1,0 +1,271 @@
+"""GB300 paged KV-cache decode attention: Python binding of libpkv.so (include/pkv.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels and
+its C++ host allocator.  If the shared library is missing, importing the kernels raises:
+there is no fallback.  Build it with ``python -m paged_kv_cache_159_gb300.build``.
+
+Names follow the C ABI without the ``pkv_`` prefix:
+
+* ``Pool(desc, free_order=None)`` -- pool_create / destroy / alloc / share / free /
+  build_block_tables / attach_device / get_device_error.
+* ``slot_mapping(tables, seq_lens)`` -- slot of each sequence's newest token (host).
+* ``kv_append(pool, k, v, slot_mapping, key_cache, value_cache)``.
+* ``paged_attention_decode(pool, q, key_cache, value_cache, block_tables, seq_lens, scale,
+  out, workspace=None, opts=None)``.
+* ``decode_workspace_bytes``, ``probe_copy``, ``device_sm_count``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libpkv.so")
+
+OK, ERR_INVALID, ERR_OOM, ERR_DEVICE, ERR_TIMEOUT, ERR_CUDA = range(6)
+DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+KV_BF16, KV_FP8E4M3 = 0, 1
+BLOCK_SIZE = 16
+
+EXPORTED = (
+    "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_get_desc", "pkv_pool_num_free",
+    "pkv_pool_refcount", "pkv_pool_alloc", "pkv_pool_share", "pkv_pool_free",
+    "pkv_build_block_tables", "pkv_slot_mapping", "pkv_pool_attach_device", "pkv_kv_append",
+    "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
+    "pkv_paged_attention_decode_ex", "pkv_get_device_error", "pkv_probe_copy",
+    "pkv_device_sm_count", "pkv_status_string",
+)
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (what, status_string(status), status))
+
+
+class pool_desc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
+
+
+class decode_opts(ctypes.Structure):
+    _fields_ = [("partition_blocks", ctypes.c_int32), ("variant", ctypes.c_int32),
+                ("warps_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+
+
+def lib():
+    """The loaded libpkv.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libpkv.so not built (%s); run python -m "
+                              "paged_kv_cache_159_gb300.build" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "pkv_pool_create": (ctypes.c_int, [ctypes.POINTER(pool_desc), _P, ctypes.POINTER(_P)]),
+            "pkv_pool_destroy": (ctypes.c_int, [_P]),
+            "pkv_pool_get_desc": (ctypes.c_int, [_P, ctypes.POINTER(pool_desc)]),
+            "pkv_pool_num_free": (ctypes.c_int, [_P, ctypes.POINTER(_I32)]),
+            "pkv_pool_refcount": (ctypes.c_int, [_P, _I32, ctypes.POINTER(_I32)]),
+            "pkv_pool_alloc": (ctypes.c_int, [_P, _I32, _P]),
+            "pkv_pool_share": (ctypes.c_int, [_P, _P, _I32]),
+            "pkv_pool_free": (ctypes.c_int, [_P, _P, _I32]),
+            "pkv_build_block_tables": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _I32, _P]),
+            "pkv_slot_mapping": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P]),
+            "pkv_pool_attach_device": (ctypes.c_int, [_P, ctypes.c_int]),
+            "pkv_kv_append": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P]),
+            "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32, _I32, ctypes.POINTER(decode_opts)]),
+            "pkv_paged_attention_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
+                                                          ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
+            "pkv_paged_attention_decode_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
+                                                             ctypes.c_float, _P, _P, ctypes.c_size_t,
+                                                             ctypes.POINTER(decode_opts), _P]),
+            "pkv_get_device_error": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+            "pkv_probe_copy": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
+            "pkv_device_sm_count": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(_I32)]),
+            "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().pkv_status_string(int(status)).decode()
+    except ImportError:
+        return "status %d" % status
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise PkvError(status, what)
+
+
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dev_ptr(t, what: str):
+    """Device address of a contiguous CUDA tensor (or None)."""
+    if t is None:
+        return None
+    if not getattr(t, "is_cuda", False):
+        raise ValueError("%s must be a CUDA tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+class Pool:
+    """A paged K/V pool descriptor with its host block allocator (pkv_pool_*)."""
+
+    def __init__(self, num_blocks, num_kv_heads, head_dim, kv_dtype=KV_BF16, k_scale=1.0,
+                 v_scale=1.0, free_order=None, block_size=BLOCK_SIZE):
+        self.desc = pool_desc(int(num_blocks), int(block_size), int(num_kv_heads),
+                              int(head_dim), int(kv_dtype), float(k_scale), float(v_scale))
+        h = ctypes.c_void_p()
+        order = None
+        if free_order is not None:
+            order = np.ascontiguousarray(free_order, dtype=np.int32)
+            if order.shape != (int(num_blocks),):
+                raise ValueError("free_order must have num_blocks entries")
+        _check(lib().pkv_pool_create(ctypes.byref(self.desc),
+                                     _np_ptr(order) if order is not None else None,
+                                     ctypes.byref(h)), "pool_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            lib().pkv_pool_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        n = _I32()
+        _check(lib().pkv_pool_num_free(self._h, ctypes.byref(n)), "pool_num_free")
+        return n.value
+
+    def refcount(self, block_id: int) -> int:
+        n = _I32()
+        _check(lib().pkv_pool_refcount(self._h, int(block_id), ctypes.byref(n)), "pool_refcount")
+        return n.value
+
+    def alloc(self, n: int) -> np.ndarray:
+        ids = np.empty(int(n), dtype=np.int32)
+        _check(lib().pkv_pool_alloc(self._h, int(n), _np_ptr(ids)), "pool_alloc")
+        return ids
+
+    def share(self, ids):
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        _check(lib().pkv_pool_share(self._h, _np_ptr(ids), ids.size), "pool_share")
+
+    def free(self, ids):
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        _check(lib().pkv_pool_free(self._h, _np_ptr(ids), ids.size), "pool_free")
+
+    def build_block_tables(self, seq_lens, max_blocks: int, prefix_ids=None) -> np.ndarray:
+        seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        prefix = np.ascontiguousarray(prefix_ids if prefix_ids is not None else [], dtype=np.int32)
+        out = np.empty((seq_lens.size, int(max_blocks)), dtype=np.int32)
+        _check(lib().pkv_build_block_tables(self._h, _np_ptr(seq_lens), seq_lens.size, int(max_blocks),
+                                            _np_ptr(prefix) if prefix.size else None, prefix.size,
+                                            _np_ptr(out)), "build_block_tables")
+        return out
+
+    def attach_device(self, device: int = 0):
+        _check(lib().pkv_pool_attach_device(self._h, int(device)), "pool_attach_device")
+
+    def get_device_error(self, stream=None):
+        """(status, bits): synchronises the stream, reads and clears the error word."""
+        bits = ctypes.c_uint32()
+        st = lib().pkv_get_device_error(self._h, _stream_ptr(stream), ctypes.byref(bits))
+        return st, bits.value
+
+
+def slot_mapping(tables, seq_lens, block_size: int = BLOCK_SIZE) -> np.ndarray:
+    tables = np.ascontiguousarray(tables, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    out = np.empty(seq_lens.size, dtype=np.int64)
+    _check(lib().pkv_slot_mapping(_np_ptr(tables), _np_ptr(seq_lens), seq_lens.size,
+                                  tables.shape[1], int(block_size), _np_ptr(out)), "slot_mapping")
+    return out
+
+
+def kv_append(pool: Pool, k, v, slots, key_cache, value_cache, stream=None):
+    """k, v: bf16 CUDA [T, Hkv, D]; slots: int64 CUDA [T]; caches: CUDA pool tensors."""
+    _check(lib().pkv_kv_append(pool.handle, _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                               _dev_ptr(slots, "slot_mapping"), int(slots.numel()),
+                               _dev_ptr(key_cache, "key_cache"), _dev_ptr(value_cache, "value_cache"),
+                               _stream_ptr(stream)), "kv_append")
+
+
+def _opts(opts):
+    if opts is None:
+        return None
+    if isinstance(opts, decode_opts):
+        return opts
+    return decode_opts(int(opts.get("partition_blocks", 0)), int(opts.get("variant", 0)),
+                       int(opts.get("warps_per_cta", 0)), int(opts.get("stages", 0)))
+
+
+def decode_workspace_bytes(pool: Pool, batch: int, num_q_heads: int, max_blocks: int,
+                           opts=None) -> int:
+    o = _opts(opts)
+    return int(lib().pkv_decode_workspace_bytes(pool.handle, int(batch), int(num_q_heads),
+                                                int(max_blocks), ctypes.byref(o) if o else None))
+
+
+def paged_attention_decode(pool: Pool, q, key_cache, value_cache, block_tables, seq_lens,
+                           scale: float, out, workspace=None, opts=None, stream=None):
+    """q/out: bf16 CUDA [B, Hq, D]; block_tables int32 CUDA [B, MB]; seq_lens int32 CUDA [B];
+    workspace: CUDA uint8 tensor of >= decode_workspace_bytes() bytes (or None)."""
+    B, Hq, _ = q.shape
+    o = _opts(opts)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pkv_paged_attention_decode_ex(
+        pool.handle, _dev_ptr(q, "q"), _dev_ptr(key_cache, "key_cache"),
+        _dev_ptr(value_cache, "value_cache"), _dev_ptr(block_tables, "block_tables"),
+        _dev_ptr(seq_lens, "seq_lens"), int(B), int(Hq), int(block_tables.shape[1]),
+        float(scale), _dev_ptr(out, "out"), _dev_ptr(workspace, "workspace"), int(ws_bytes),
+        ctypes.byref(o) if o else None, _stream_ptr(stream)), "paged_attention_decode")
+
+
+def probe_copy(dst, src, stream=None):
+    nbytes = src.numel() * src.element_size()
+    _check(lib().pkv_probe_copy(_dev_ptr(dst, "dst"), _dev_ptr(src, "src"), int(nbytes),
+                                _stream_ptr(stream)), "probe_copy")
+
+
+def device_sm_count(device: int = 0) -> int:
+    n = _I32()
+    _check(lib().pkv_device_sm_count(int(device), ctypes.byref(n)), "device_sm_count")
+    return n.value

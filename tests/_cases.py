@@ -1,0 +1,144 @@
+"""Build GPU parity cases: seeded inputs (workloads), block tables and slots from the
+oracle's allocator, unread positions poisoned with NaN, and the oracle's own results."""
+import dataclasses
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+import paged_kv_cache_159_gb300 as pkv
+
+NAN16 = workloads.BF16_NAN_BITS
+FP8_NAN = 0x7F
+
+
+def tol_check(gpu: np.ndarray, ref: np.ndarray, atol=1e-2, rtol=1e-2):
+    """Elementwise |gpu - ref| <= atol + rtol*|ref| (the stated decode tolerance).
+    Returns (max_abs_err, max_rel_err over |ref| > 1e-3)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    assert np.isfinite(gpu).all(), "non-finite output"
+    err = np.abs(gpu - ref)
+    bad = err > atol + rtol * np.abs(ref)
+    assert not bad.any(), "%d elements out of tolerance; worst abs %.3g" % (bad.sum(), err.max())
+    big = np.abs(ref) > 1e-3
+    rel = (err[big] / np.abs(ref[big])).max() if big.any() else 0.0
+    return float(err.max()), float(rel)
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+@dataclasses.dataclass
+class Case:
+    w: workloads.Workload
+    seq_lens: np.ndarray
+    tables: np.ndarray
+    slots: np.ndarray            # int64 [B] newest-token slots (append workloads)
+    pool: "pkv.Pool"
+    key_cache: torch.Tensor      # device pool (bf16 or uint8 codes)
+    value_cache: torch.Tensor
+    q: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    k_scale: float
+    v_scale: float
+    kv_dtype: int
+    # oracle-side pools (host), before any append
+    key_host: np.ndarray
+    value_host: np.ndarray
+
+
+def build(name: str, device="cuda", seq_lens=None, overrides=None, free_order=None) -> Case:
+    w = workloads.WORKLOADS[name]
+    if overrides:
+        w = dataclasses.replace(w, **overrides)
+    d = workloads.draw(w, device, seq_lens)
+    order = d.free_order if free_order is None else np.asarray(free_order, np.int32)
+    alloc = oracle.BlockAllocator(d.num_blocks, order)
+    prefix = alloc.alloc(w.prefix_blocks) if w.prefix_blocks else []
+    tables = oracle.build_block_tables(alloc, d.seq_lens, d.max_blocks, 16, prefix)
+    slots = oracle.slot_mapping(tables, d.seq_lens)
+    live = torch.from_numpy(oracle.live_positions(tables, d.seq_lens, d.num_blocks)).to(device)
+    dead = ~live                                               # [NB, 16]
+    kc, vc = d.key_cache, d.value_cache
+    nan = torch.tensor(NAN16, dtype=torch.int16, device=device).view(torch.bfloat16)
+    kc[dead[:, None, :, None].expand_as(kc)] = nan
+    vc[dead[:, None, :, None].expand_as(vc)] = nan
+    slots_dev = torch.from_numpy(slots).to(device)
+    if w.append:                                               # the new token's slot starts as NaN
+        blk, off = slots_dev // 16, slots_dev % 16
+        kc[blk, :, off, :] = nan
+        vc[blk, :, off, :] = nan
+    k_scale = v_scale = 1.0
+    kv_dtype = pkv.KV_BF16
+    if w.kv_dtype == "fp8":
+        # The FP8 pool is written through kv_append from the bf16 history of every live
+        # position; the per-tensor scales are amax / 448 in fp32.
+        kv_dtype = pkv.KV_FP8E4M3
+        all_slots = torch.from_numpy(oracle.all_slots(tables, d.seq_lens)).to(device)
+        blk, off = all_slots // 16, all_slots % 16
+        k_src = kc[blk, :, off, :].contiguous()                # [T, Hkv, D]
+        v_src = vc[blk, :, off, :].contiguous()
+        k_scale = float(np.float32(k_src.float().abs().max().item()) / np.float32(448.0))
+        v_scale = float(np.float32(v_src.float().abs().max().item()) / np.float32(448.0))
+        pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim, kv_dtype, k_scale, v_scale, order)
+        pool.attach_device(torch.cuda.current_device())
+        k8 = torch.full(kc.shape, FP8_NAN, dtype=torch.uint8, device=device)
+        v8 = torch.full(vc.shape, FP8_NAN, dtype=torch.uint8, device=device)
+        # host copies of the source rows for the oracle's own encode
+        key_host = np.full(kc.shape, FP8_NAN, dtype=np.uint8)
+        value_host = np.full(vc.shape, FP8_NAN, dtype=np.uint8)
+        ks_host, vs_host = workloads.bf16_bits(k_src), workloads.bf16_bits(v_src)
+        sl_host = all_slots.cpu().numpy()
+        assert oracle.kv_append(ks_host, vs_host, sl_host, key_host, value_host, 16,
+                                oracle.FP8E4M3, k_scale, v_scale) == 0
+        pkv.kv_append(pool, k_src, v_src, all_slots, k8, v8)
+        torch.cuda.synchronize()
+        kc, vc = k8, v8
+    else:
+        pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim, free_order=order)
+        pool.attach_device(torch.cuda.current_device())
+        key_host = workloads.bf16_bits(kc)
+        value_host = workloads.bf16_bits(vc)
+    return Case(w, d.seq_lens, tables, slots, pool, kc, vc, d.q, d.k_new, d.v_new, k_scale,
+                v_scale, kv_dtype, key_host, value_host)
+
+
+def oracle_append(c: Case):
+    """The oracle's kv_append on its own host pools (in place)."""
+    assert c.kv_dtype == pkv.KV_BF16
+    st = oracle.kv_append(workloads.bf16_bits(c.k_new), workloads.bf16_bits(c.v_new), c.slots,
+                          c.key_host, c.value_host)
+    assert st == 0
+
+
+def oracle_decode(c: Case, pairs=None, threads=None):
+    st, out = oracle.paged_decode(
+        workloads.bf16_bits(c.q), c.key_host, c.value_host, c.tables, c.seq_lens, c.w.scale,
+        c.w.num_kv_heads, 16, oracle.FP8E4M3 if c.kv_dtype == pkv.KV_FP8E4M3 else oracle.BF16,
+        c.k_scale, c.v_scale, pairs=pairs, num_threads=threads or oracle.max_threads())
+    assert st == 0
+    return out
+
+
+def device_tables(c: Case, device="cuda"):
+    return (torch.from_numpy(c.tables).to(device), torch.from_numpy(c.seq_lens).to(device),
+            torch.from_numpy(c.slots).to(device))
+
+
+def gpu_step(c: Case, opts=None, append=True):
+    """kv_append (if the workload appends) then decode; returns the bf16 output."""
+    bt, sl, slots = device_tables(c)
+    if append and c.w.append:
+        pkv.kv_append(c.pool, c.k_new, c.v_new, slots, c.key_cache, c.value_cache)
+    B, Hq, D = c.q.shape
+    out = torch.empty_like(c.q)
+    nbytes = pkv.decode_workspace_bytes(c.pool, B, Hq, bt.shape[1], opts)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=c.q.device) if nbytes else None
+    pkv.paged_attention_decode(c.pool, c.q, c.key_cache, c.value_cache, bt, sl, c.w.scale, out,
+                               ws, opts)
+    st, bits = c.pool.get_device_error()
+    assert st == pkv.OK and bits == 0, (st, bits)
+    return out

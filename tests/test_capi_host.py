@@ -1,0 +1,137 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every symbol include/pkv.h
+declares, and its host allocator / block tables / slot mapping equal the oracle's bit for
+bit.  No kernel is launched here."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pkv = pytest.importorskip("paged_kv_cache_159_gb300")
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(pkv.LIB_PATH):
+        from paged_kv_cache_159_gb300 import build
+        build.build()
+    return pkv.lib()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "pkv.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert len(declared) >= 18
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(pkv.EXPORTED)
+
+
+def test_status_strings(lib):
+    assert pkv.status_string(0) == "ok"
+    assert "invalid" in pkv.status_string(1)
+    assert pkv.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("name", list(workloads.WORKLOADS))
+def test_block_tables_and_slots_equal_the_oracle(lib, name):
+    w = workloads.WORKLOADS[name]
+    L = workloads.draw_seq_lens(w)
+    nb = workloads.pool_blocks(w, L)
+    mb = workloads.max_blocks(w, L)
+    order = workloads.draw_free_order(w, nb)
+
+    a = oracle.BlockAllocator(nb, order)
+    prefix = a.alloc(w.prefix_blocks) if w.prefix_blocks else []
+    t_orc = oracle.build_block_tables(a, L, mb, 16, prefix)
+
+    p = pkv.Pool(nb, w.num_kv_heads, w.head_dim, free_order=order)
+    prefix_p = p.alloc(w.prefix_blocks) if w.prefix_blocks else None
+    if w.prefix_blocks:
+        assert list(prefix_p) == list(prefix)
+    t_pkv = p.build_block_tables(L, mb, prefix_p)
+    assert np.array_equal(t_orc, t_pkv)
+    assert p.num_free() == len(a.free)
+    assert np.array_equal(pkv.slot_mapping(t_pkv, L), oracle.slot_mapping(t_orc, L))
+    for blk in {int(x) for x in t_orc.ravel() if x >= 0}:
+        assert p.refcount(blk) == a.refcount[blk]
+    # return everything: the free lists stay in lock-step
+    for row in t_orc:
+        ids = [int(x) for x in row if x >= 0]
+        a.release(ids)
+        p.free(ids)
+    if w.prefix_blocks:
+        a.release(prefix)
+        p.free(prefix_p)
+    assert p.num_free() == nb == len(a.free)
+    assert np.array_equal(p.alloc(nb), np.array(a.alloc(nb), dtype=np.int32))
+
+
+def test_slot_mapping_page_example_at_block_size_4(lib):
+    # steinslab.io §3.4: table [7, 3, 12], block_size 4, token 6 -> slot 14
+    slots = pkv.slot_mapping(np.array([[7, 3, 12]], np.int32), np.array([7], np.int32), block_size=4)
+    assert slots.tolist() == [14]
+
+
+def test_allocator_errors(lib):
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.Pool(0, 8, 128)
+    assert e.value.status == pkv.ERR_INVALID
+    for bad in (dict(head_dim=96), dict(block_size=32), dict(kv_dtype=7),
+                dict(kv_dtype=pkv.KV_FP8E4M3, k_scale=0.0)):
+        kw = dict(num_blocks=4, num_kv_heads=2, head_dim=64)
+        kw.update(bad)
+        with pytest.raises(pkv.PkvError):
+            pkv.Pool(**kw)
+    with pytest.raises(pkv.PkvError):
+        pkv.Pool(4, 2, 64, free_order=[0, 1, 1, 2])
+    p = pkv.Pool(4, 2, 64, free_order=[3, 2, 1, 0])
+    with pytest.raises(pkv.PkvError) as e:
+        p.alloc(5)
+    assert e.value.status == pkv.ERR_OOM and p.num_free() == 4
+    ids = p.alloc(2)
+    assert ids.tolist() == [3, 2]
+    with pytest.raises(pkv.PkvError):
+        p.free([3, 3])                      # second reference does not exist
+    assert p.refcount(3) == 1               # nothing changed by the failed call
+    with pytest.raises(pkv.PkvError):
+        p.share([1])                        # free block
+    with pytest.raises(pkv.PkvError):
+        p.build_block_tables([0], 2)         # empty sequence
+    with pytest.raises(pkv.PkvError):
+        p.build_block_tables([33], 2)        # needs 3 entries
+    with pytest.raises(pkv.PkvError) as e:
+        p.build_block_tables([16, 16, 16], 1)
+    assert e.value.status == pkv.ERR_OOM
+    assert p.num_free() == 2                # the failed call returned what it took
+    assert p.alloc(2).tolist() == [1, 0]
+    with pytest.raises(pkv.PkvError):
+        pkv.slot_mapping(np.array([[5, -1]], np.int32), np.array([20], np.int32))
+
+
+def test_decode_workspace_bytes_follows_the_partition_plan(lib):
+    p = pkv.Pool(64, 8, 128)
+    assert pkv.decode_workspace_bytes(p, 64, 32, 128, {"partition_blocks": 128}) == 0
+    ws = pkv.decode_workspace_bytes(p, 4, 64, 2048, {"partition_blocks": 128})
+    rows = 4 * 64 * 16
+    assert ws >= rows * 128 * 4 + rows * 2 * 4
+    assert pkv.decode_workspace_bytes(p, 4, 60, 2048, None) == 0     # Hq % Hkv != 0
+
+
+def test_device_calls_need_an_attached_pool(lib):
+    p = pkv.Pool(8, 2, 64)
+    st = lib.pkv_kv_append(p.handle, None, None, None, 1, None, None, None)
+    assert st == pkv.ERR_INVALID
+    st = lib.pkv_paged_attention_decode(p.handle, None, None, None, None, None, 1, 8, 1, 0.125,
+                                        None, None, 0, None)
+    assert st == pkv.ERR_INVALID
