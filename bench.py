@@ -1,0 +1,468 @@
+"""Benchmark: one paged decode step (kv_append of each sequence's new token, then paged
+GQA decode attention) on the Llama-3-8B layer shape, through libpkv's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is K/V-cache bytes read per step divided by the
+device time of a step, summed over ranks (replicas: every rank runs its own copy of the
+workload, nothing is exchanged).  Each timed step is bracketed by CUDA events on the launch
+stream; the L2 cache is flushed between steps (outside the events) by reading a buffer twice
+its size (a read, so that no write-back of the flush lands in the next step).
+`e2e` repeats the measurement through the Python/C-ABI calls with pinned host inputs copied
+in and the output copied back every step.  `--impl reference` times the fp64 CPU oracle on
+a bounded sample of the same workload (one sequence per step).
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode-attn KV GB/s (% of HBM peak) and query-tokens/s, Llama-3-8B layer shape"
+DEFAULT_WORKLOAD = "llama3_8b"
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ("decode_kernels.cuh", "paged_decode.cu", "pkv_device.cuh")
+
+
+# ------------------------------------------------------------------ helpers
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def _hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_159_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    current decode sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_%s.md" % workload)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    s = re.search(r"decode_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != decode_source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def reduce_max_over_ranks(values, device):
+    """Elementwise max of per-rank timings (the slowest rank sets the step time)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def aggregate_value(world, kv_bytes_per_step, steps, slowest_total_s):
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time (weak scaling)."""
+    return world * kv_bytes_per_step * steps / slowest_total_s / 1e9
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local_rank):
+    import torch
+    import paged_kv_cache_159_gb300 as pkv
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workloads.WORKLOADS[args.workload]
+    d = workloads.draw(w, dev)
+    B, Hq, D = d.q.shape
+    Hkv = w.num_kv_heads
+    elem = 1 if w.kv_dtype == "fp8" else 2
+
+    # pool, block tables and slots from the library's host allocator
+    k_scale = v_scale = 1.0
+    kc, vc = d.key_cache, d.value_cache
+    if w.kv_dtype == "fp8":
+        k_scale = float(np.float32(kc.float().abs().max().item()) / np.float32(448.0))
+        v_scale = float(np.float32(vc.float().abs().max().item()) / np.float32(448.0))
+    pool = pkv.Pool(d.num_blocks, Hkv, D, pkv.KV_FP8E4M3 if w.kv_dtype == "fp8" else pkv.KV_BF16,
+                    k_scale, v_scale, d.free_order)
+    pool.attach_device(local_rank)
+    prefix = pool.alloc(w.prefix_blocks) if w.prefix_blocks else None
+    tables = pool.build_block_tables(d.seq_lens, d.max_blocks, prefix)
+    slots = pkv.slot_mapping(tables, d.seq_lens)
+    if w.kv_dtype == "fp8":                      # encode the history through kv_append
+        alls = torch.from_numpy(pkv.slot_mapping_all(tables, d.seq_lens)).to(dev)
+        k8 = torch.zeros(kc.shape, dtype=torch.uint8, device=dev)
+        v8 = torch.zeros_like(k8)
+        for i in range(0, alls.numel(), 1 << 16):
+            s = alls[i:i + (1 << 16)]
+            pkv.kv_append(pool, kc[s // 16, :, s % 16, :].contiguous(),
+                          vc[s // 16, :, s % 16, :].contiguous(), s, k8, v8)
+        kc, vc = k8, v8
+        del d.key_cache, d.value_cache
+    bt = torch.from_numpy(tables).to(dev)
+    sl = torch.from_numpy(d.seq_lens).to(dev)
+    sm = torch.from_numpy(slots).to(dev)
+    out = torch.empty_like(d.q)
+    ws_bytes = pkv.decode_workspace_bytes(pool, B, Hq, d.max_blocks)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    launches_per_step = (1 if w.append else 0) + 1
+    # algorithmic bytes (no credit for tail-slot over-read; shared prefix blocks counted
+    # once per reader here, i.e. logical bytes)
+    kv_read = int(d.seq_lens.astype(np.int64).sum()) * Hkv * D * elem * 2
+    decode_bytes = kv_read + 2 * B * Hq * D * 2 + B * d.max_blocks * 4 + B * 4
+    append_bytes = (B * 8 + 2 * B * Hkv * D * (2 + elem)) if w.append else 0
+    step_bytes = decode_bytes + append_bytes
+
+    # same-process bandwidth denominator: the library's copy probe over 2 x 1 GiB
+    src = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        pkv.probe_copy(dst, src, stream=stream)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    probe = []
+    with torch.cuda.stream(stream):
+        for _ in range(10):
+            ev[0].record(stream)
+            pkv.probe_copy(dst, src, stream=stream)
+            ev[1].record(stream)
+            ev[1].synchronize()
+            probe.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+    copy_gbs = 2 * src.numel() / min(probe) / 1e9
+    del src, dst
+
+    # L2 flush between steps: a read of a buffer twice the L2 size.  Reading leaves only clean
+    # lines behind, so no write-back of the flush lands inside the next timed step.
+    flush_buf = torch.ones(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4,
+                           dtype=torch.int32, device=dev)
+    flush_out = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        torch.sum(flush_buf, dim=0, out=flush_out)
+
+    K, W = args.steps, args.warmup
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+
+    def timed_step(i):
+        flush_l2()                                # L2 flush (read), outside the timed interval
+        starts[i].record(stream)
+        if w.append:
+            pkv.kv_append(pool, d.k_new, d.v_new, sm, kc, vc, stream=stream)
+        mids[i].record(stream)
+        pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws, stream=stream)
+        ends[i].record(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            timed_step(i % K)
+    stream.synchronize()
+    st, bits = pool.get_device_error(stream)
+    if st != pkv.OK:
+        raise RuntimeError("device error in warm-up: %d bits %#x" % (st, bits))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                timed_step(i)
+        stream.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_s = [starts[i].elapsed_time(ends[i]) * 1e-3 for i in range(K)]
+    dec_s = [mids[i].elapsed_time(ends[i]) * 1e-3 for i in range(K)]
+    total = float(sum(step_s))
+    dec_mean = float(sum(dec_s) / K)
+    st, bits = pool.get_device_error(stream)
+    if st != pkv.OK:
+        raise RuntimeError("device error in the timed region: %d bits %#x" % (st, bits))
+
+    # ---- end to end through the API: pinned host inputs in, output back, every step
+    host = {}
+    pin = lambda t: t.detach().cpu().pin_memory()
+    host["q"], host["k"], host["v"] = pin(d.q), pin(d.k_new), pin(d.v_new)
+    host["sl"] = torch.from_numpy(d.seq_lens.copy()).pin_memory()
+    host["out"] = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    tables_host = tables
+    h2d = (host["q"].numel() * 2 + (host["k"].numel() * 2 * 2 if w.append else 0)
+           + tables_host.nbytes + host["sl"].numel() * 4 + (B * 8 if w.append else 0))
+    d2h = host["out"].numel() * 2
+    e2e_steps = max(5, min(K, 200))
+    bt_h = torch.from_numpy(tables_host).pin_memory()
+    sm_h = torch.empty(B, dtype=torch.int64).pin_memory()
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    e2e_t = []
+    for i in range(e2e_steps + 3):
+        flush_l2()
+        torch.cuda.synchronize()
+        ee[0].record()
+        slots_np = pkv.slot_mapping(tables_host, d.seq_lens)            # host allocator side
+        sm_h[:] = torch.from_numpy(slots_np)
+        d.q.copy_(host["q"], non_blocking=True)
+        bt.copy_(bt_h, non_blocking=True)
+        sl.copy_(host["sl"], non_blocking=True)
+        if w.append:
+            d.k_new.copy_(host["k"], non_blocking=True)
+            d.v_new.copy_(host["v"], non_blocking=True)
+            sm.copy_(sm_h, non_blocking=True)
+            pkv.kv_append(pool, d.k_new, d.v_new, sm, kc, vc)
+        pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws)
+        host["out"].copy_(out, non_blocking=True)
+        ee[1].record()
+        ee[1].synchronize()
+        if i >= 3:
+            e2e_t.append(ee[0].elapsed_time(ee[1]) * 1e-3)
+    e2e_step = float(statistics.median(e2e_t))
+
+    # ---- reduce over ranks (max time), aggregate bytes over ranks
+    if world > 1:
+        total, dec_mean, e2e_step = reduce_max_over_ranks([total, dec_mean, e2e_step], dev)
+    peak, peak_src = _hbm_peak()
+    ms_per_step = total / K * 1e3
+    value = aggregate_value(world, kv_read, K, total)
+    achieved = decode_bytes / dec_mean / 1e9
+    traffic = _profiled_traffic(args.workload)
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8e4m3-kv/bf16-q" if w.kv_dtype == "fp8" else "bf16", "data": "synthetic",
+        "config": {
+            "workload": "%s: batch %d, q heads %d / kv heads %d, head_dim %d, block 16, "
+                        "seq_lens %s, kv %s" % (w.name, B, Hq, Hkv, D,
+                                                 "all %d" % d.seq_lens[0] if w.lengths == "fixed"
+                                                 else "%s (sum %d)" % (w.lengths, int(d.seq_lens.sum())),
+                                                 w.kv_dtype),
+            "step": ("kv_append + " if w.append else "") + "paged_attention_decode",
+            "l2": "flushed between steps (read of a 2x L2 buffer); inputs also exceed L2",
+            "parallelism": "replicas",
+            "timing": "CUDA events around each step on the launch stream; flush outside them",
+        },
+        "pct_of_hbm_peak": round(100.0 * (kv_read * K / total / 1e9) / peak, 2),
+        "query_tokens_per_s": round(world * B * K / total, 1),
+        "step_bytes": step_bytes,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "paged_attention_decode (decode_mma_kernel)",
+                     "bytes_per_launch": decode_bytes, "peak_source": peak_src + " hbm_gbs",
+                     "same_run_copy_gbs": round(copy_gbs, 1)},
+        "e2e": {"value": round(world * kv_read / e2e_step / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_step * 1e3, 4)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, sample_seqs=args.cpu_sample_seqs)
+    return res
+
+
+# ------------------------------------------------------------------ the oracle on host cores
+def _oracle_case(w, nseq):
+    """A bounded sample of the workload for the oracle: the first `nseq` sequences."""
+    import torch
+    import oracle
+    L = workloads.draw_seq_lens(w)[:nseq]
+    sub = workloads.Workload(**{**w.__dict__, "batch": nseq, "lengths": "list",
+                                "len_list": tuple(int(x) for x in L), "pool": "exact",
+                                "prefix_blocks": 0})
+    d = workloads.draw(sub, "cpu")
+    a = oracle.BlockAllocator(d.num_blocks, d.free_order)
+    tables = oracle.build_block_tables(a, d.seq_lens, d.max_blocks)
+    kb, vb = workloads.bf16_bits(d.key_cache), workloads.bf16_bits(d.value_cache)
+    return sub, d, tables, kb, vb
+
+
+def cpu_baseline(w, sample_seqs=64, threads=None, reps=3):
+    import oracle
+    threads = threads or os.cpu_count() or 1
+    sample_seqs = min(sample_seqs, w.batch)
+    sub, d, tables, kb, vb = _oracle_case(w, sample_seqs)
+    q = workloads.bf16_bits(d.q)
+    kn, vn = workloads.bf16_bits(d.k_new), workloads.bf16_bits(d.v_new)
+    slots = oracle.slot_mapping(tables, d.seq_lens)
+    t = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        if w.append:
+            oracle.kv_append(kn, vn, slots, kb, vb)
+        st, _ = oracle.paged_decode(q, kb, vb, tables, d.seq_lens, w.scale, w.num_kv_heads,
+                                    num_threads=threads)
+        t.append(time.perf_counter() - t0)
+    sec = min(t)
+    kv_read = int(d.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    return {"value": round(kv_read / sec / 1e9, 4), "unit": "GB/s", "cores": int(threads),
+            "kind": "oracle",
+            "sample": "%d of %d sequences (all %d query heads), kv_append + fp64 decode, best of %d: %.3f s"
+                      % (sample_seqs, w.batch, w.num_q_heads, reps, sec),
+            "query_tokens_per_s": round(sample_seqs / sec, 2)}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is one sequence of the workload (all its
+    query heads, kv_append + decode) in fp64 on the host cores."""
+    import oracle
+    w = workloads.WORKLOADS[args.workload]
+    threads = os.cpu_count() or 1
+    nseq = min(w.batch, 8)
+    sub, d, tables, kb, vb = _oracle_case(w, nseq)
+    q = workloads.bf16_bits(d.q)
+    kn, vn = workloads.bf16_bits(d.k_new), workloads.bf16_bits(d.v_new)
+    slots = oracle.slot_mapping(tables, d.seq_lens)
+    per_seq_bytes = [int(L) * w.num_kv_heads * w.head_dim * 2 * 2 for L in d.seq_lens]
+
+    def one(i):
+        b = i % nseq
+        pairs = np.array([[b, h] for h in range(w.num_q_heads)], dtype=np.int32)
+        if w.append:
+            oracle.kv_append(kn[b:b + 1], vn[b:b + 1], slots[b:b + 1], kb, vb)
+        st, _ = oracle.paged_decode(q, kb, vb, tables, d.seq_lens, w.scale, w.num_kv_heads,
+                                    pairs=pairs, num_threads=threads)
+        return per_seq_bytes[b]
+
+    for i in range(args.warmup):
+        one(i)
+    nbytes = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        nbytes += one(i)
+    total = time.perf_counter() - t0
+    value = nbytes / total / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "parallelism": "host threads",
+                   "sample": "one sequence per step (all query heads, kv_append + decode)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": "one of the first %d sequences per step, %d steps" % (nseq, args.steps)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "query_tokens_per_s": round(args.steps / total, 3),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-seqs", type=int, default=64)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local_rank = _dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        res = run_ours(args, world, rank, local_rank)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -120,6 +120,12 @@ int pkv_build_block_tables(pkv_pool *pool, const int32_t *seq_lens, int32_t batc
 int pkv_slot_mapping(const int32_t *tables, const int32_t *seq_lens, int32_t batch,
                      int32_t max_blocks, int32_t block_size, int64_t *slots_out);
 
+/* Slots of every position 0 .. seq_lens[b]-1 of every sequence [Slot], sequence-major
+ * (slots_out has sum(seq_lens) int64 entries): the slot mapping of a whole-prompt append.
+ * Host arrays as in pkv_slot_mapping; same errors. */
+int pkv_slot_mapping_all(const int32_t *tables, const int32_t *seq_lens, int32_t batch,
+                         int32_t max_blocks, int32_t block_size, int64_t *slots_out);
+
 /* Bind the pool to a CUDA device: allocates its 4-byte device error word (cudaMalloc) on
  * that device.  Required once before pkv_kv_append / pkv_paged_attention_decode. */
 int pkv_pool_attach_device(pkv_pool *pool, int device);
@@ -135,14 +141,14 @@ int pkv_kv_append(pkv_pool *pool, const void *k, const void *v, const int64_t *s
 
 /* Tuning knobs for pkv_paged_attention_decode_ex; zero fields mean "choose". */
 typedef struct {
-    int32_t partition_blocks; /* logical blocks per split-KV partition (0 = auto) */
+    int32_t grid_ctas;        /* CTAs of the persistent grid (0 = SM count x CTAs per SM) */
     int32_t variant;          /* 0 = auto, 1 = CUDA-core dot products, 2 = tensor-core mma */
-    int32_t warps_per_cta;    /* 0 = auto; 1, 2, 4 or 8 */
-    int32_t stages;           /* 0 = auto; per-warp shared-memory pipeline depth 1..4 */
+    int32_t warps_per_cta;    /* 0 = auto (4); 4 or 8 */
+    int32_t stages;           /* 0 = auto (2); per-warp shared-memory pipeline depth 2..4 */
 } pkv_decode_opts;
 
-/* Device workspace needed by the split-KV path for this shape (0 when no sequence can be
- * split).  Must be called with the same opts as the decode call. */
+/* Device workspace bytes the decode needs for this shape and these opts (0 if the shape or
+ * opts are invalid).  Queries the current device. */
 size_t pkv_decode_workspace_bytes(const pkv_pool *pool, int32_t batch, int32_t num_q_heads,
                                   int32_t max_blocks, const pkv_decode_opts *opts);
 
@@ -152,13 +158,19 @@ size_t pkv_decode_workspace_bytes(const pkv_pool *pool, int32_t batch, int32_t n
  * Device pointers: q bf16 [batch, num_q_heads, D]; caches as in pkv_pool_desc;
  * block_tables int32 [batch, max_blocks]; seq_lens int32 [batch]; out bf16
  * [batch, num_q_heads, D] (fp32 accumulation, rounded to nearest even); workspace of at
- * least pkv_decode_workspace_bytes() bytes (may be NULL when that is 0), 256-byte aligned.
- * Positions j >= L_b are never used, whatever they hold.  Long sequences are split into
- * partitions whose partial softmax states are merged by a second kernel on the same
- * stream; the summation order depends only on logical positions, so any physical
- * placement of the blocks gives bit-identical output.  Requires num_q_heads a multiple of
- * Hkv with group <= 16, an attached pool, max_blocks >= 1.  FP8 pools compute q.K with
- * q rounded to fp16 (|q| must stay below 65504). */
+ * least pkv_decode_workspace_bytes() bytes, 256-byte aligned, ZERO-FILLED before its first
+ * use: it holds per-(sequence, KV head) counters that every call leaves at zero again
+ * (re-zero it after a call that reported a device error), plus partial softmax states.
+ * Calls sharing a workspace must not overlap on the GPU.
+ * Positions j >= L_b are never used, whatever they hold.  The work -- every sequence's
+ * blocks for every KV head -- is split evenly over a one-wave persistent grid; a
+ * (sequence, head) cut by that split is finished by whichever of its CTAs ends last.  All
+ * split points and merge orders depend only on seq_lens, the grid and logical positions,
+ * so any physical placement of the blocks gives bit-identical output.  Requires
+ * 1 <= batch <= 4096, num_q_heads a multiple of Hkv with group <= 16, an attached pool,
+ * max_blocks >= 1, batch * max_blocks * Hkv < 2^31.  FP8 pools compute q.K with q rounded
+ * to fp16 (|q| must stay below 65504).  An invalid seq_len sets PKV_DEVERR_SEQ_LEN and
+ * zeroes that sequence's output. */
 int pkv_paged_attention_decode(pkv_pool *pool, const void *q, const void *key_cache,
                                const void *value_cache, const int32_t *block_tables,
                                const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,

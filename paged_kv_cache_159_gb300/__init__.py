@@ -8,7 +8,8 @@ Names follow the C ABI without the ``pkv_`` prefix:
 
 * ``Pool(desc, free_order=None)`` -- pool_create / destroy / alloc / share / free /
   build_block_tables / attach_device / get_device_error.
-* ``slot_mapping(tables, seq_lens)`` -- slot of each sequence's newest token (host).
+* ``slot_mapping(tables, seq_lens)`` -- slot of each sequence's newest token (host);
+  ``slot_mapping_all`` -- slots of every position (a whole-prompt append).
 * ``kv_append(pool, k, v, slot_mapping, key_cache, value_cache)``.
 * ``paged_attention_decode(pool, q, key_cache, value_cache, block_tables, seq_lens, scale,
   out, workspace=None, opts=None)``.
@@ -32,7 +33,8 @@ BLOCK_SIZE = 16
 EXPORTED = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_get_desc", "pkv_pool_num_free",
     "pkv_pool_refcount", "pkv_pool_alloc", "pkv_pool_share", "pkv_pool_free",
-    "pkv_build_block_tables", "pkv_slot_mapping", "pkv_pool_attach_device", "pkv_kv_append",
+    "pkv_build_block_tables", "pkv_slot_mapping", "pkv_slot_mapping_all",
+    "pkv_pool_attach_device", "pkv_kv_append",
     "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
     "pkv_paged_attention_decode_ex", "pkv_get_device_error", "pkv_probe_copy",
     "pkv_device_sm_count", "pkv_status_string",
@@ -53,7 +55,7 @@ class pool_desc(ctypes.Structure):
 
 
 class decode_opts(ctypes.Structure):
-    _fields_ = [("partition_blocks", ctypes.c_int32), ("variant", ctypes.c_int32),
+    _fields_ = [("grid_ctas", ctypes.c_int32), ("variant", ctypes.c_int32),
                 ("warps_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32)]
 
 
@@ -81,6 +83,7 @@ def lib():
             "pkv_pool_free": (ctypes.c_int, [_P, _P, _I32]),
             "pkv_build_block_tables": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _I32, _P]),
             "pkv_slot_mapping": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P]),
+            "pkv_slot_mapping_all": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P]),
             "pkv_pool_attach_device": (ctypes.c_int, [_P, ctypes.c_int]),
             "pkv_kv_append": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P]),
             "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32, _I32, ctypes.POINTER(decode_opts)]),
@@ -220,6 +223,17 @@ def slot_mapping(tables, seq_lens, block_size: int = BLOCK_SIZE) -> np.ndarray:
     return out
 
 
+def slot_mapping_all(tables, seq_lens, block_size: int = BLOCK_SIZE) -> np.ndarray:
+    """Slots of every position of every sequence, sequence-major (int64 [sum(seq_lens)])."""
+    tables = np.ascontiguousarray(tables, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    out = np.empty(int(seq_lens.astype(np.int64).sum()), dtype=np.int64)
+    _check(lib().pkv_slot_mapping_all(_np_ptr(tables), _np_ptr(seq_lens), seq_lens.size,
+                                      tables.shape[1], int(block_size), _np_ptr(out)),
+           "slot_mapping_all")
+    return out
+
+
 def kv_append(pool: Pool, k, v, slots, key_cache, value_cache, stream=None):
     """k, v: bf16 CUDA [T, Hkv, D]; slots: int64 CUDA [T]; caches: CUDA pool tensors."""
     _check(lib().pkv_kv_append(pool.handle, _dev_ptr(k, "k"), _dev_ptr(v, "v"),
@@ -233,7 +247,7 @@ def _opts(opts):
         return None
     if isinstance(opts, decode_opts):
         return opts
-    return decode_opts(int(opts.get("partition_blocks", 0)), int(opts.get("variant", 0)),
+    return decode_opts(int(opts.get("grid_ctas", 0)), int(opts.get("variant", 0)),
                        int(opts.get("warps_per_cta", 0)), int(opts.get("stages", 0)))
 
 
@@ -247,7 +261,8 @@ def decode_workspace_bytes(pool: Pool, batch: int, num_q_heads: int, max_blocks:
 def paged_attention_decode(pool: Pool, q, key_cache, value_cache, block_tables, seq_lens,
                            scale: float, out, workspace=None, opts=None, stream=None):
     """q/out: bf16 CUDA [B, Hq, D]; block_tables int32 CUDA [B, MB]; seq_lens int32 CUDA [B];
-    workspace: CUDA uint8 tensor of >= decode_workspace_bytes() bytes (or None)."""
+    workspace: zero-initialised CUDA uint8 tensor of >= decode_workspace_bytes() bytes (calls
+    leave it zeroed)."""
     B, Hq, _ = q.shape
     o = _opts(opts)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

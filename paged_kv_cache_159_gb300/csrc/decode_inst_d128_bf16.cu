@@ -1,5 +1,5 @@
 // decode_inst_d128_bf16.cu -- compiles the decode kernels for head_dim 128 with a bf16 pool.
 #include "decode_kernels.cuh"
 
-template cudaError_t pkv::decode::dispatch_nw_ns<128, false>(const pkv::decode::Plan &, int, int, cudaStream_t,
-                                                        const pkv::decode::DecodeParams &);
+template cudaError_t pkv::decode::dispatch_nw_ns<128, false>(const pkv::decode::Plan &, int, bool, int *, cudaStream_t,
+                                                        const pkv::decode::DecodeParams *);

@@ -1,5 +1,4 @@
-// paged_decode.cu -- single-query (decode) GQA attention over the paged KV pool, plus the
-// split-KV combine kernel.
+// decode_kernels.cuh -- single-query (decode) GQA attention over the paged KV pool.
 //
 // What is computed (the pages' definitions):
 //   * "传统 Attention 的 KV Cache 问题" (pyllm.pages.dev) §1.1: out = sum_j softmax_j(q.K_j /
@@ -15,14 +14,28 @@
 //     heads hq = h*g .. h*g+g-1 share KV head h.
 //
 // GB300 design:
-//   * One CTA per (sequence, KV head, partition of logical blocks).  All g query heads of
-//     the group are computed from one read of each K/V tile, so every K/V byte crosses HBM
-//     once per step.
+//   * Work unit = (sequence b, KV head h); its work is ceil(L_b/16) blocks.  All g query heads
+//     of the group are computed from one read of each K/V tile, so every K/V byte crosses
+//     HBM once per step.
+//   * Persistent, balanced schedule ("stream-K"): the units' blocks are laid end to end
+//     (b-major, then h, then logical block) into W block-tasks and CTA c of a one-wave grid
+//     of G CTAs takes tasks [W*c/G, W*(c+1)/G).  Every CTA streams the same number of bytes
+//     whatever the batch shape.  W is computed by every CTA from seq_lens (a block-wide scan
+//     in shared memory), so the host needs no lengths.
+//   * A CTA's range splits into segments at unit boundaries.  A unit that lies wholly in
+//     one CTA is finished there.  A unit cut by CTA boundaries leaves a partial softmax
+//     state (max, sum, unnormalised output) per CTA in the workspace; each such CTA then
+//     bumps the unit's counter, and the one that completes the count merges the partials in
+//     CTA order and writes the output (no CTA ever waits for another), then resets the
+//     counter to zero.
 //   * Each (block, head) tile of K or V is contiguous (16 x head_dim elements: 4 KiB bf16 at
 //     head_dim 128), so it is staged by one 1-D bulk (TMA) copy into shared memory.  Every
 //     warp owns a ring of `NS` stages (K and V tile each) with one mbarrier per stage and
-//     streams the blocks j = first + warp, first + warp + NW, ...; no CTA-wide barrier sits in
-//     the loop.  Waits are bounded (about 1 s) and report PKV_DEVERR_TIMEOUT.
+//     streams the tasks first + warp, first + warp + NW, ...; the copy for a task is issued
+//     NS tasks ahead of its use, across segment boundaries.  Physical block ids are fetched
+//     32 tasks ahead into registers.  The g query rows of each segment's unit are staged
+//     by a bulk copy one segment ahead.  Waits are bounded (about 1 s) and report
+//     PKV_DEVERR_TIMEOUT.
 //   * Two ways to do the small g x D x 16 contractions, selectable for measurement:
 //       - variant 1 (CUDA cores): each lane owns D/32 columns, dot products are finished with
 //         warp-shuffle butterflies;
@@ -35,10 +48,8 @@
 //     denominator share the same reference) and skips almost every accumulator rescale.
 //   * Positions past seq_len in the last block are masked by select (scores -> -inf, V rows
 //     -> 0), so whatever the tail slots hold (NaN included) never reaches the output.
-//   * Partitions: a sequence longer than one partition writes (max, sum, unnormalised
-//     output) per partition to the workspace and `combine_kernel` merges them; the merge
-//     order and every partition boundary depend only on logical positions, so any physical
-//     placement of the blocks gives bit-identical results.
+//   * Every split point and every merge order depends only on seq_lens, the grid size and
+//     logical positions, so any physical placement of the blocks gives bit-identical output.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -53,9 +64,10 @@ namespace pkv {
 namespace decode {
 
 constexpr int BS = 16;                    // tokens per block
-constexpr int PB_MAX = 1024;              // table entries one CTA may stage
+constexpr int MAX_BATCH = 4096;           // sequences per call (prefix scan in shared memory)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_TAU = 8.0f;       // raise the running max only beyond 2^8
+constexpr int ACC_PAD = 8;                // floats of padding per merge-area row
 
 struct DecodeParams {
     const uint16_t *q;            // bf16 [B, Hq, D]
@@ -64,12 +76,33 @@ struct DecodeParams {
     const int32_t *block_tables;  // [B, MB]
     const int32_t *seq_lens;      // [B]
     uint16_t *out;                // bf16 [B, Hq, D]
-    float *part_o;                // [B, Hq, P, D]   unnormalised partial outputs
-    float *part_ml;               // [B, Hq, P, 2]   (running max in log2 units, sum)
+    int32_t *counters;            // [B * Hkv] arrival counts of split units (kept at zero)
+    float *part_o;                // [G][2][group][D]   unnormalised partial outputs
+    float *part_ml;               // [G][2][group][2]   (running max in log2 units, sum)
     uint32_t *err;
-    int B, Hq, Hkv, group, MB, P, PB, num_blocks;
+    int B, Hq, Hkv, group, MB, num_blocks;
     float score_scale;            // scale * k_scale * log2(e)
     float out_scale;              // v_scale (1 for bf16 pools)
+};
+
+__host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+// Shared-memory plan of one CTA (host and device agree on it).
+struct Layout {
+    int stage, q, ml, acc, prefix, phys, bar, flag, total;
+    __host__ __device__ Layout(int NW, int NS, int tile, int D, int group, int B)
+    {
+        int o = 0;
+        stage = o;  o += NW * NS * 2 * tile;                      // K and V tiles per stage
+        q = o;      o += 2 * align_up(group * D * 2, 128);       // two segments' q rows
+        ml = o;     o += NW * 16 * 2 * 4;                        // per-warp (max, sum) rows
+        acc = o;    o += align_up(NW * group * (D + ACC_PAD) * 4, 128);
+        prefix = o; o += align_up((B + 1) * 4, 16);              // task prefix over sequences
+        phys = o;   o += align_up(NW * NS * 4, 16);              // tile index per stage
+        bar = o;    o += (NW * NS + 2) * 8;                      // stage + q barriers
+        flag = o;   o += 64;                                    // scan scratch / merge flag
+        total = o;
+    }
 };
 
 __device__ __forceinline__ float warp_allreduce_sum(float x)
@@ -79,45 +112,25 @@ __device__ __forceinline__ float warp_allreduce_sum(float x)
     return x;
 }
 
-// ------------------------------------------------------------------------------------
-// Shared-memory plan of one CTA:
-//   [stage area: NW * NS * 2 * TILE bytes, reused as the merge area after the loop]
-//   [table: PB_MAX int32] [barriers: NW * NS * 8 bytes]
-// ------------------------------------------------------------------------------------
-template <int D, bool FP8, int NW, int NS>
-struct Smem {
-    static constexpr int ELEM = FP8 ? 1 : 2;
-    static constexpr int ROW = D * ELEM;                  // bytes of one token row
-    static constexpr int TILE = BS * ROW;                 // one (block, head) tile of K or V
-    static constexpr int STAGE = 2 * TILE;
-    static constexpr int STAGE_AREA = NW * NS * STAGE;
-    static constexpr int MERGE_AREA = NW * (16 * D * 4 + 2 * 16 * 4);
-    static constexpr int AREA = STAGE_AREA > MERGE_AREA ? STAGE_AREA : MERGE_AREA;
-    static constexpr int TABLE_OFF = AREA;
-    static constexpr int BAR_OFF = TABLE_OFF + PB_MAX * 4;
-    static constexpr int BYTES = BAR_OFF + NW * NS * 8;
-};
-
-// Issue the copies of this warp's i-th block into stage s (lane 0 only).
-template <int D, bool FP8, int NW, int NS>
-__device__ __forceinline__ void issue_block(const DecodeParams &p, int h, uint8_t *smem,
-                                            const int32_t *tbl, int warp, int i)
+// Largest b in [0, B) with prefix[b] <= r (prefix[B] > r assumed).
+__device__ __forceinline__ int find_seq(const int32_t *prefix, int B, int r)
 {
-    using S = Smem<D, FP8, NW, NS>;
-    const int s = i % NS;
-    const int local = warp + NW * i;                    // index within the partition
-    const int phys = tbl[local];
-    uint8_t *stage = smem + (warp * NS + s) * S::STAGE;
-    const uint32_t bar = dev::smem_u32(smem + S::BAR_OFF + (warp * NS + s) * 8);
-    if (phys >= 0) {
-        const size_t off = ((size_t)phys * p.Hkv + h) * S::TILE;
-        dev::mbar_arrive_expect_tx(bar, 2 * S::TILE);
-        dev::bulk_g2s(dev::smem_u32(stage), p.key_cache + off, S::TILE, bar);
-        dev::bulk_g2s(dev::smem_u32(stage + S::TILE), p.value_cache + off, S::TILE, bar);
-    } else {
-        dev::mbar_arrive(bar);                          // nothing to copy; block is masked
+    int lo = 0, hi = B;                       // invariant: prefix[lo] <= r < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= r) lo = mid;
+        else hi = mid;
     }
+    return lo;
 }
+
+// CTA that owns task r under the even split of W tasks over G CTAs.
+__device__ __forceinline__ int cta_of(long long r, long long W, int G)
+{
+    return (int)(((r + 1) * G - 1) / W);
+}
+
+__device__ __forceinline__ long long task_start(int c, long long W, int G) { return W * c / G; }
 
 // ------------------------------------------------------------------------------------
 // Tensor-core compute (variant 2).  Lane l: gid = l/4 (mma row group), tid = l%4.
@@ -141,11 +154,14 @@ struct MmaCompute {
 
     // Column d of O held by n-tile nt, mma column n.
     __device__ static int dmap(int nt, int n) { return (n + 8 * (nt / EV)) * EV + nt % EV; }
+    // Where column d sits in a merge-area row (fragment order: nt*8 + n).
+    __device__ static int slot_of_d(int d) { return ((d / (8 * EV)) * EV + d % EV) * 8 + (d / EV) % 8; }
 
-    __device__ void init(const DecodeParams &p, int b, int h, int lane)
+    // Load the q fragments of rows 0..group-1 (bf16 [group][D] in shared memory) and reset
+    // the softmax state.
+    __device__ void start(const uint16_t *qs, int group, int lane)
     {
         const int gid = lane >> 2, tid = lane & 3;
-        const uint16_t *qb = p.q + ((size_t)b * p.Hq + (size_t)h * p.group) * D;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             const int d0 = (4 * (ks / SUBS) + tid) * EK + (ks % SUBS) * 4;
@@ -153,11 +169,11 @@ struct MmaCompute {
             for (int r = 0; r < 2; ++r) {
                 const int row = gid + 8 * r;
                 uint32_t lo = 0, hi = 0;
-                if (row < p.group && (r == 0 || G16)) {
-                    const uint32_t *src = reinterpret_cast<const uint32_t *>(qb + (size_t)row * D + d0);
-                    lo = __ldg(src);
-                    hi = __ldg(src + 1);
-                    if (FP8) {
+                if (row < group && (r == 0 || G16)) {
+                    const uint32_t *src = reinterpret_cast<const uint32_t *>(qs + row * D + d0);
+                    lo = src[0];
+                    hi = src[1];
+                    if constexpr (FP8) {
                         lo = dev::pack_f16x2(dev::bf16_lo(lo), dev::bf16_hi(lo));
                         hi = dev::pack_f16x2(dev::bf16_lo(hi), dev::bf16_hi(hi));
                     }
@@ -302,8 +318,8 @@ struct MmaCompute {
         }
     }
 
-    // Write this warp's (m, l, acc) for rows < group into the merge area.
-    __device__ void dump(float *ms, float *ls, float *accs, int group, int lane)
+    // Write this warp's (max, sum) rows and accumulators into the merge area.
+    __device__ void dump(float *ml, float *accs, int group, int lane)
     {
         const int gid = lane >> 2, tid = lane & 3;
 #pragma unroll
@@ -316,14 +332,13 @@ struct MmaCompute {
             const int row = gid + 8 * r;
             if (row < group) {
                 if (tid == 0) {
-                    ms[row] = m[r];
-                    ls[row] = l[r];
+                    ml[row * 2] = m[r];
+                    ml[row * 2 + 1] = l[r];
                 }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    accs[row * D + dmap(nt, 2 * tid)] = acc[nt][2 * r];
-                    accs[row * D + dmap(nt, 2 * tid + 1)] = acc[nt][2 * r + 1];
-                }
+                for (int nt = 0; nt < NT; ++nt)
+                    *reinterpret_cast<float2 *>(accs + row * (D + ACC_PAD) + nt * 8 + 2 * tid) =
+                        make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]);
             }
         }
     }
@@ -342,20 +357,20 @@ struct SimtCompute {
     float qf[GP][EPL];
     float acc[GP][EPL];
     float m[GP], l[GP];
-    int group;
+    float sscale;
 
-    __device__ void init(const DecodeParams &p, int b, int h, int lane, float score_scale)
+    __device__ static int slot_of_d(int d) { return d; }
+
+    __device__ void start(const uint16_t *qs, int group, int lane)
     {
-        group = p.group;
-        const uint16_t *qb = p.q + ((size_t)b * p.Hq + (size_t)h * p.group) * D;
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
 #pragma unroll
             for (int e = 0; e < EPL; ++e) {
                 float x = 0.f;
-                if (g < p.group) x = __uint_as_float((uint32_t)__ldg(qb + (size_t)g * D + lane * EPL + e) << 16);
+                if (g < group) x = __uint_as_float((uint32_t)qs[g * D + lane * EPL + e] << 16);
                 if (FP8) x = __half2float(__float2half_rn(x));   // same q rounding as variant 2
-                qf[g][e] = x * score_scale;
+                qf[g][e] = x * sscale;
                 acc[g][e] = 0.f;
             }
             m[g] = -INFINITY;
@@ -365,7 +380,7 @@ struct SimtCompute {
 
     __device__ __forceinline__ void load_row(const uint8_t *row, int lane, float (&x)[EPL])
     {
-        if (FP8) {
+        if constexpr (FP8) {
             const uint8_t *src = row + lane * EPL;
 #pragma unroll
             for (int e = 0; e < EPL; e += 2) {
@@ -438,162 +453,285 @@ struct SimtCompute {
         }
     }
 
-    __device__ void dump(float *ms, float *ls, float *accs, int grp, int lane)
+    __device__ void dump(float *ml, float *accs, int group, int lane)
     {
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-            if (g < grp) {
+            if (g < group) {
                 if (lane == 0) {
-                    ms[g] = m[g];
-                    ls[g] = l[g];
+                    ml[g * 2] = m[g];
+                    ml[g * 2 + 1] = l[g];
                 }
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) accs[g * D + lane * EPL + e] = acc[g][e];
+                for (int e = 0; e < EPL; ++e) accs[g * (D + ACC_PAD) + lane * EPL + e] = acc[g][e];
             }
         }
     }
 };
 
 // ------------------------------------------------------------------------------------
-// The decode kernel: pipeline + compute + in-CTA merge + output / partial write.
+// The decode kernel body.
 // ------------------------------------------------------------------------------------
 template <int D, bool FP8, int NW, int NS, class Compute>
 __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
 {
-    using S = Smem<D, FP8, NW, NS>;
+    constexpr int ELEM = FP8 ? 1 : 2;
+    constexpr int TILE = BS * D * ELEM;
+    constexpr int NTHR = NW * 32;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Layout lay(NW, NS, TILE, D, p.group, p.B);
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + lay.prefix);
+    int32_t *stage_tile = reinterpret_cast<int32_t *>(smem + lay.phys);
+    int *flag = reinterpret_cast<int *>(smem + lay.flag);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int Hkv = p.Hkv, group = p.group;
 
-    int item = blockIdx.x;
-    const int h = item % p.Hkv;
-    item /= p.Hkv;
-    const int b = item % p.B;
-    const int part = item / p.B;
-
-    const int L = __ldg(p.seq_lens + b);
-    if (L < 1 || L > p.MB * BS) {                    // uniform over the CTA
-        if (threadIdx.x == 0) dev::flag_error(p.err, PKV_DEVERR_SEQ_LEN);
-        if (part == 0) {
-            for (int e = threadIdx.x; e < p.group * D; e += NW * 32)
-                p.out[((size_t)b * p.Hq + (size_t)h * p.group) * D + e] = 0;
+    // ---- 1. tasks per sequence (Hkv * ceil(L/16); 0 for an invalid length) and their
+    //         exclusive prefix, by a block-wide scan; CTA 0 zeroes invalid sequences' rows.
+    {
+        const int per = (p.B + NTHR - 1) / NTHR;
+        const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
+        int run = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int L = __ldg(p.seq_lens + b);
+            const bool ok = L >= 1 && L <= p.MB * BS;
+            if (!ok && c == 0) {
+                dev::flag_error(p.err, PKV_DEVERR_SEQ_LEN);
+                for (int e = 0; e < p.Hq * D; ++e) p.out[(size_t)b * p.Hq * D + e] = 0;
+            }
+            run += ok ? Hkv * ((L + BS - 1) / BS) : 0;
         }
-        return;
-    }
-    const int nblk = (L + BS - 1) / BS;
-    const int nparts = (nblk + p.PB - 1) / p.PB;
-    const int blk0 = part * p.PB;
-    if (blk0 >= nblk) return;                        // uniform: nothing in this partition
-    const int blk1 = min(nblk, blk0 + p.PB);
-    const int nloc = blk1 - blk0;
-
-    // Stage this partition's table entries (validated) in shared memory.
-    int32_t *tbl = reinterpret_cast<int32_t *>(smem + S::TABLE_OFF);
-    const int32_t *row = p.block_tables + (size_t)b * p.MB + blk0;
-    for (int i = threadIdx.x; i < nloc; i += NW * 32) {
-        int32_t id = __ldg(row + i);
-        if (id < 0 || id >= p.num_blocks) {
-            dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-            id = -1;
+        int incl = run;                                   // inclusive scan over the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(dev::FULL, incl, o);
+            if (lane >= o) incl += v;
         }
-        tbl[i] = id;
+        int *wsum = flag;                                  // NW <= 8 warp totals
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += wsum[w];
+        int acc = base + incl - run;                       // exclusive prefix of b0
+        for (int b = b0; b < b1; ++b) {
+            prefix[b] = acc;
+            const int L = __ldg(p.seq_lens + b);
+            const bool ok = L >= 1 && L <= p.MB * BS;
+            acc += ok ? Hkv * ((L + BS - 1) / BS) : 0;
+        }
+        if (tid == NTHR - 1) prefix[p.B] = base + incl;
+        __syncthreads();
     }
-    if (lane == 0) {
-        for (int s = 0; s < NS; ++s)
-            dev::mbar_init(dev::smem_u32(smem + S::BAR_OFF + (warp * NS + s) * 8), 1);
-        dev::fence_barrier_init();
+    const long long W = prefix[p.B];
+    // With fewer tasks than CTAs only the first W CTAs work, one task each; every working
+    // CTA then owns at least one task, so the CTAs that cut a unit are exactly c0..c1.
+    const int G = (int)(W < (long long)gridDim.x ? W : (long long)gridDim.x);
+    if (c >= G) return;                                    // uniform over the CTA
+    const long long s = task_start(c, W, G), e = task_start(c + 1, W, G);
+
+    // ---- 2. barriers
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar);
+    const uint32_t qbar0 = dev::smem_u32(bars + NW * NS);
+    if (lane == 0)
+        for (int st = 0; st < NS; ++st) dev::mbar_init(dev::smem_u32(bars + warp * NS + st), 1);
+    if (tid == 0) {
+        dev::mbar_init(qbar0, 1);
+        dev::mbar_init(qbar0 + 8, 1);
     }
+    dev::fence_barrier_init();
     __syncthreads();
 
-    const int n_mine = (nloc - warp + NW - 1) / NW;  // blocks warp, warp+NW, ... (may be 0)
-    cmp.init(p, b, h, lane, p.score_scale);
+    // Unit geometry of task r: sequence, head, first task of the unit, blocks in it.
+    struct Unit { int b, h, L, nb; long long U0; };
+    auto unit_of = [&](long long r) {
+        Unit u;
+        u.b = find_seq(prefix, p.B, (int)r);
+        const int tasks = prefix[u.b + 1] - prefix[u.b];
+        u.nb = tasks / Hkv;
+        u.h = (int)(r - prefix[u.b]) / u.nb;
+        u.U0 = prefix[u.b] + (long long)u.h * u.nb;
+        u.L = __ldg(p.seq_lens + u.b);
+        return u;
+    };
+    const int qbytes = group * D * 2;
+    const int qslot_bytes = align_up(qbytes, 128);
+    auto issue_q = [&](const Unit &u, int k) {            // thread 0 only
+        const uint32_t bar = qbar0 + 8 * (k & 1);
+        dev::fence_proxy_async_smem();
+        dev::mbar_arrive_expect_tx(bar, qbytes);
+        dev::bulk_g2s(dev::smem_u32(smem + lay.q + (k & 1) * qslot_bytes),
+                      p.q + ((size_t)u.b * p.Hq + (size_t)u.h * group) * D, qbytes, bar);
+    };
 
-    if (lane == 0)
-        for (int i = 0; i < NS && i < n_mine; ++i) issue_block<D, FP8, NW, NS>(p, h, smem, tbl, warp, i);
-    __syncwarp();
+    // ---- 3. per-warp producer: tasks r_i = s + warp + NW*i, copies issued NS ahead
+    const int n_mine = (int)max(0LL, (e - s - warp + NW - 1) / NW);
+    // tile index (phys * Hkv + h, or -1 if the table entry is invalid) of warp task i, for a
+    // chunk of 32 tasks: lane j holds task chunk*32 + j
+    auto load_tiles = [&](int chunk) {
+        const int i = chunk * 32 + lane;
+        int t = -1;
+        if (i < n_mine) {
+            const long long r = s + warp + (long long)NW * i;
+            const Unit u = unit_of(r);
+            const int blk = (int)(r - u.U0);
+            const int id = __ldg(p.block_tables + (size_t)u.b * p.MB + blk);
+            if (id >= 0 && id < p.num_blocks) t = id * Hkv + u.h;
+            else dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+        }
+        return t;
+    };
+    int tcur = load_tiles(0), tnext = load_tiles(1);
+    auto issue = [&](int i) {                              // warp-collective
+        if ((i & 31) == 0 && i > 0) {
+            tcur = tnext;
+            tnext = load_tiles((i >> 5) + 1);
+        }
+        const int t = __shfl_sync(dev::FULL, tcur, i & 31);
+        if (lane == 0) {
+            const int st = i % NS;
+            const uint32_t bar = dev::smem_u32(bars + warp * NS + st);
+            uint8_t *stage = smem + lay.stage + (warp * NS + st) * 2 * TILE;
+            stage_tile[warp * NS + st] = t;
+            if (t >= 0) {
+                const size_t off = (size_t)t * TILE;
+                dev::fence_proxy_async_smem();
+                dev::mbar_arrive_expect_tx(bar, 2 * TILE);
+                dev::bulk_g2s(dev::smem_u32(stage), p.key_cache + off, TILE, bar);
+                dev::bulk_g2s(dev::smem_u32(stage + TILE), p.value_cache + off, TILE, bar);
+            } else {
+                dev::mbar_arrive(bar);                    // nothing to copy; block is masked
+            }
+        }
+    };
+    int ip = 0;
+    for (; ip < NS && ip < n_mine; ++ip) issue(ip);
+    if (tid == 0) issue_q(unit_of(s), 0);
 
-    int i = 0;
-    for (; i < n_mine; ++i) {
-        const int s = i % NS;
-        const uint32_t bar = dev::smem_u32(smem + S::BAR_OFF + (warp * NS + s) * 8);
-        const bool ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(bar, (uint32_t)((i / NS) & 1)));
-        if (!ok) break;
-        const int local = warp + NW * i;
-        const int j = blk0 + local;
-        const int ntok = tbl[local] >= 0 ? min(BS, L - j * BS) : 0;
-        if (ntok > 0) {
-            const uint8_t *stage = smem + (warp * NS + s) * S::STAGE;
-            cmp.block(stage, stage + S::TILE, ntok, p.score_scale, lane);
+    // ---- 4. segments
+    float *ml_all = reinterpret_cast<float *>(smem + lay.ml);
+    float *acc_all = reinterpret_cast<float *>(smem + lay.acc);
+    const int rowstride = D + ACC_PAD;
+    bool aborted = false;
+    int ic = 0;
+    int k = 0;
+    for (long long seg_lo = s; seg_lo < e; ++k) {
+        const Unit u = unit_of(seg_lo);
+        const long long U1 = u.U0 + u.nb;
+        const long long seg_hi = U1 < e ? U1 : e;
+        if (tid == 0 && seg_hi < e) issue_q(unit_of(seg_hi), k + 1);
+        const bool qok = __all_sync(dev::FULL, dev::mbar_wait_bounded(qbar0 + 8 * (k & 1), (uint32_t)((k >> 1) & 1)));
+        aborted |= !qok;
+        cmp.start(reinterpret_cast<const uint16_t *>(smem + lay.q + (k & 1) * qslot_bytes), group, lane);
+        while (!aborted && ic < n_mine && s + warp + (long long)NW * ic < seg_hi) {
+            const int st = ic % NS;
+            const uint32_t bar = dev::smem_u32(bars + warp * NS + st);
+            if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(bar, (uint32_t)((ic / NS) & 1)))) {
+                aborted = true;
+                break;
+            }
+            const long long r = s + warp + (long long)NW * ic;
+            const int blk = (int)(r - u.U0);
+            const int ntok = stage_tile[warp * NS + st] >= 0 ? min(BS, u.L - blk * BS) : 0;
+            if (ntok > 0) {
+                const uint8_t *stage = smem + lay.stage + (warp * NS + st) * 2 * TILE;
+                cmp.block(stage, stage + TILE, ntok, p.score_scale, lane);
+            }
+            __syncwarp();
+            if (ip < n_mine) issue(ip++);
+            ++ic;
         }
-        __syncwarp();
-        if (lane == 0 && i + NS < n_mine) {
-            dev::fence_proxy_async_smem();
-            issue_block<D, FP8, NW, NS>(p, h, smem, tbl, warp, i + NS);
+        // merge the warps' states for this segment
+        cmp.dump(ml_all + warp * 32, acc_all + warp * group * rowstride, group, lane);
+        __syncthreads();
+        const bool whole = seg_lo == u.U0 && seg_hi == U1;
+        const int slot = k == 0 ? 0 : 1;
+        const size_t prow = ((size_t)c * 2 + slot) * group;        // partial rows of this CTA
+        for (int x = tid; x < group * D; x += NTHR) {
+            const int row = x / D, d = x - row * D;
+            const int sd = Compute::slot_of_d(d);
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) M = fmaxf(M, ml_all[w * 32 + row * 2]);
+            float num = 0.f, den = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    const float mw = ml_all[w * 32 + row * 2];
+                    const float wt = mw == -INFINITY ? 0.f : dev::fast_exp2(mw - M);
+                    num += wt * acc_all[(w * group + row) * rowstride + sd];
+                    den += wt * ml_all[w * 32 + row * 2 + 1];
+                }
+            }
+            if (whole) {
+                const float o = den > 0.f ? num / den * p.out_scale : 0.f;
+                const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+                p.out[((size_t)u.b * p.Hq + (size_t)u.h * group + row) * D + d] =
+                    *reinterpret_cast<const uint16_t *>(&ob);
+            } else {
+                p.part_o[(prow + row) * D + d] = num * p.out_scale;
+                if (d == 0) {
+                    p.part_ml[(prow + row) * 2] = M;
+                    p.part_ml[(prow + row) * 2 + 1] = den;
+                }
+            }
         }
+        if (!whole) {
+            // hand-off: the last CTA of this unit to arrive merges every CTA's partial
+            __threadfence();
+            __syncthreads();
+            const int c0 = cta_of(u.U0, W, G), c1 = cta_of(U1 - 1, W, G);
+            if (tid == 0) {
+                const int old = atomicAdd(p.counters + (size_t)u.b * Hkv + u.h, 1);
+                flag[0] = old == c1 - c0;
+            }
+            __syncthreads();
+            if (flag[0]) {
+                __threadfence();
+                const bool c0_shared = task_start(c0, W, G) < u.U0;   // unit is c0's 2nd+ segment
+                for (int x = tid; x < group * D; x += NTHR) {
+                    const int row = x / D, d = x - row * D;
+                    float M = -INFINITY;
+                    for (int cc = c0; cc <= c1; ++cc) {
+                        const int sl = (cc == c0 && c0_shared) ? 1 : 0;
+                        M = fmaxf(M, __ldcg(p.part_ml + (((size_t)cc * 2 + sl) * group + row) * 2));
+                    }
+                    float num = 0.f, den = 0.f;
+                    if (M != -INFINITY) {
+                        for (int cc = c0; cc <= c1; ++cc) {
+                            const int sl = (cc == c0 && c0_shared) ? 1 : 0;
+                            const size_t pr = ((size_t)cc * 2 + sl) * group + row;
+                            const float mc = __ldcg(p.part_ml + pr * 2);
+                            const float wt = mc == -INFINITY ? 0.f : dev::fast_exp2(mc - M);
+                            num += wt * __ldcg(p.part_o + pr * D + d);
+                            den += wt * __ldcg(p.part_ml + pr * 2 + 1);
+                        }
+                    }
+                    const float o = den > 0.f ? num / den : 0.f;
+                    const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+                    p.out[((size_t)u.b * p.Hq + (size_t)u.h * group + row) * D + d] =
+                        *reinterpret_cast<const uint16_t *>(&ob);
+                }
+                if (tid == 0) atomicExch(p.counters + (size_t)u.b * Hkv + u.h, 0);
+            }
+        }
+        __syncthreads();                                  // merge area and q slot reusable
+        seg_lo = seg_hi;
     }
-    if (i < n_mine) {
+    if (aborted) {
         // A wait gave up: report it, then give the copies still in flight one more bounded
         // wait so that none lands after this CTA has left.
         if (lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
-        const int last = min(n_mine, i + NS);
-        for (int k = i; k < last; ++k) {
-            const uint32_t bar = dev::smem_u32(smem + S::BAR_OFF + (warp * NS + (k % NS)) * 8);
-            (void)dev::mbar_wait_bounded(bar, (uint32_t)((k / NS) & 1));
-        }
-    }
-    __syncthreads();                                 // every warp done with its stages
-
-    // ---- merge the warps' partial softmax states (fixed warp order)
-    float *ms = reinterpret_cast<float *>(smem);     // [NW][16]
-    float *ls = ms + NW * 16;                        // [NW][16]
-    float *accs = ls + NW * 16;                      // [NW][16][D]
-    cmp.dump(ms + warp * 16, ls + warp * 16, accs + (size_t)warp * 16 * D, p.group, lane);
-    __syncthreads();
-
-    const int hq0 = h * p.group;
-    for (int e = threadIdx.x; e < p.group * D; e += NW * 32) {
-        const int r = e / D, d = e - r * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, ms[w * 16 + r]);
-        float num = 0.f, den = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float mw = ms[w * 16 + r];
-                const float wt = mw == -INFINITY ? 0.f : dev::fast_exp2(mw - M);
-                num += wt * accs[((size_t)w * 16 + r) * D + d];
-                den += wt * ls[w * 16 + r];
-            }
-        }
-        const size_t bh = (size_t)b * p.Hq + hq0 + r;
-        if (nparts == 1) {
-            const float o = den > 0.f ? num / den * p.out_scale : 0.f;
-            const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-            p.out[bh * D + d] = *reinterpret_cast<const uint16_t *>(&ob);
-        } else {
-            p.part_o[(bh * p.P + part) * D + d] = num * p.out_scale;
-            if (d == 0) {
-                p.part_ml[(bh * p.P + part) * 2 + 0] = M;
-                p.part_ml[(bh * p.P + part) * 2 + 1] = den;
-            }
-        }
+        for (int i = ic; i < ip; ++i)
+            (void)dev::mbar_wait_bounded(dev::smem_u32(bars + warp * NS + i % NS), (uint32_t)((i / NS) & 1));
     }
 }
 
-// MmaCompute::init takes no score_scale (it is applied to S); adapt decode_body's call.
-template <int D, bool FP8, bool G16>
-struct MmaAdapter : MmaCompute<D, FP8, G16> {
-    __device__ void init(const DecodeParams &p, int b, int h, int lane, float)
-    {
-        MmaCompute<D, FP8, G16>::init(p, b, h, lane);
-    }
-};
-
-// At most 128 registers per thread: 16 warps (512 threads) can be resident per SM.
+// Register budget for 8 resident warps per SM (the shared-memory ring allows no more).
 template <int D, bool FP8, int NW, int NS, bool G16>
-__global__ void __launch_bounds__(NW * 32, 16 / NW) decode_mma_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(NW * 32, 8 / NW) decode_mma_kernel(const DecodeParams p)
 {
-    MmaAdapter<D, FP8, G16> cmp;
+    MmaCompute<D, FP8, G16> cmp;
     decode_body<D, FP8, NW, NS>(p, cmp);
 }
 
@@ -601,6 +739,7 @@ template <int D, bool FP8, int NW, int NS, int GP>
 __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const DecodeParams p)
 {
     SimtCompute<D, FP8, GP> cmp;
+    cmp.sscale = p.score_scale;
     decode_body<D, FP8, NW, NS>(p, cmp);
 }
 
@@ -608,70 +747,78 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const DecodeParams
 // Launch plan and per-instantiation launchers.
 // ------------------------------------------------------------------------------------
 struct Plan {
-    int variant, nw, ns, pb, parts;
-    size_t ws_o, ws_ml;                              // workspace byte offsets
-    size_t ws_bytes;
+    int variant, nw, ns;
+    int grid;                 // CTAs (one wave)
+    size_t smem;              // dynamic shared memory per CTA
+    size_t ws_counters, ws_o, ws_ml, ws_bytes;
 };
 
 template <class K>
-cudaError_t launch_with_smem(K kernel, int grid, int threads, size_t smem, cudaStream_t s,
-                             const DecodeParams &p)
+cudaError_t prepare(K kernel, size_t smem, int threads, int *per_sm)
 {
-    // cudaFuncSetAttribute is cheap but not free; remember per (kernel, device).
+    // cudaFuncSetAttribute is cheap but not free; remember per (kernel, device, size).
     static std::mutex mu;
     static const void *seen_fn[256];
     static int seen_dev[256];
+    static size_t seen_smem[256];
     static int nseen = 0;
     int dev = 0;
     cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> g(mu);
     bool known = false;
-    {
-        std::lock_guard<std::mutex> g(mu);
-        for (int i = 0; i < nseen; ++i)
-            if (seen_fn[i] == (const void *)kernel && seen_dev[i] == dev) known = true;
-        if (!known) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            if (nseen < 256) {
-                seen_fn[nseen] = (const void *)kernel;
-                seen_dev[nseen] = dev;
-                ++nseen;
-            }
+    for (int i = 0; i < nseen; ++i)
+        if (seen_fn[i] == (const void *)kernel && seen_dev[i] == dev && seen_smem[i] >= smem) known = true;
+    if (!known) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (nseen < 256) {
+            seen_fn[nseen] = (const void *)kernel;
+            seen_dev[nseen] = dev;
+            seen_smem[nseen] = smem;
+            ++nseen;
         }
     }
-    kernel<<<grid, threads, smem, s>>>(p);
-    return cudaGetLastError();
+    if (per_sm) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kernel, threads, smem);
+    return cudaSuccess;
 }
 
+// Either report CTAs per SM (launch == false) or launch.
 template <int D, bool FP8, int NW, int NS>
-cudaError_t launch_decode(const Plan &pl, int group, int grid, cudaStream_t s, const DecodeParams &p)
+cudaError_t run_decode(const Plan &pl, int group, bool launch, int *per_sm, cudaStream_t s,
+                       const DecodeParams *p)
 {
-    using S = Smem<D, FP8, NW, NS>;
     const int threads = NW * 32;
+    auto go = [&](auto kernel) -> cudaError_t {
+        cudaError_t e = prepare(kernel, pl.smem, threads, launch ? nullptr : per_sm);
+        if (e != cudaSuccess || !launch) return e;
+        kernel<<<pl.grid, threads, pl.smem, s>>>(*p);
+        return cudaGetLastError();
+    };
     if (pl.variant == 2) {
-        if (group > 8)
-            return launch_with_smem(decode_mma_kernel<D, FP8, NW, NS, true>, grid, threads, S::BYTES, s, p);
-        return launch_with_smem(decode_mma_kernel<D, FP8, NW, NS, false>, grid, threads, S::BYTES, s, p);
+        if (group > 8) return go(decode_mma_kernel<D, FP8, NW, NS, true>);
+        return go(decode_mma_kernel<D, FP8, NW, NS, false>);
     }
     if constexpr (NW == 4 && NS == 2) {
-        if (group <= 1) return launch_with_smem(decode_simt_kernel<D, FP8, NW, NS, 1>, grid, threads, S::BYTES, s, p);
-        if (group <= 2) return launch_with_smem(decode_simt_kernel<D, FP8, NW, NS, 2>, grid, threads, S::BYTES, s, p);
-        if (group <= 4) return launch_with_smem(decode_simt_kernel<D, FP8, NW, NS, 4>, grid, threads, S::BYTES, s, p);
-        return launch_with_smem(decode_simt_kernel<D, FP8, NW, NS, 8>, grid, threads, S::BYTES, s, p);
+        if (group <= 1) return go(decode_simt_kernel<D, FP8, NW, NS, 1>);
+        if (group <= 2) return go(decode_simt_kernel<D, FP8, NW, NS, 2>);
+        if (group <= 4) return go(decode_simt_kernel<D, FP8, NW, NS, 4>);
+        return go(decode_simt_kernel<D, FP8, NW, NS, 8>);
     }
     return cudaErrorInvalidConfiguration;
 }
 
 // (warps per CTA, stages per warp) pairs that are compiled.  The CUDA-core variant exists
-// for comparison only and is compiled for the default pair.
+// for comparison only and is compiled for one pair.
 template <int D, bool FP8>
-cudaError_t dispatch_nw_ns(const Plan &pl, int group, int grid, cudaStream_t s, const DecodeParams &p)
+cudaError_t dispatch_nw_ns(const Plan &pl, int group, bool launch, int *per_sm, cudaStream_t s,
+                           const DecodeParams *p)
 {
     if (pl.variant == 1 && !(pl.nw == 4 && pl.ns == 2)) return cudaErrorInvalidConfiguration;
-    if (pl.nw == 4 && pl.ns == 2) return launch_decode<D, FP8, 4, 2>(pl, group, grid, s, p);
-    if (pl.nw == 4 && pl.ns == 3) return launch_decode<D, FP8, 4, 3>(pl, group, grid, s, p);
-    if (pl.nw == 8 && pl.ns == 2) return launch_decode<D, FP8, 8, 2>(pl, group, grid, s, p);
-    if (pl.nw == 2 && pl.ns == 4) return launch_decode<D, FP8, 2, 4>(pl, group, grid, s, p);
+    if (pl.nw == 4 && pl.ns == 2) return run_decode<D, FP8, 4, 2>(pl, group, launch, per_sm, s, p);
+    if (pl.nw == 4 && pl.ns == 3) return run_decode<D, FP8, 4, 3>(pl, group, launch, per_sm, s, p);
+    if (pl.nw == 4 && pl.ns == 4) return run_decode<D, FP8, 4, 4>(pl, group, launch, per_sm, s, p);
+    if (pl.nw == 8 && pl.ns == 2) return run_decode<D, FP8, 8, 2>(pl, group, launch, per_sm, s, p);
+    if (pl.nw == 8 && pl.ns == 3) return run_decode<D, FP8, 8, 3>(pl, group, launch, per_sm, s, p);
     return cudaErrorInvalidConfiguration;
 }
 

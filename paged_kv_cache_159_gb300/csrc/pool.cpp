@@ -225,6 +225,27 @@ int pkv_slot_mapping(const int32_t *tables, const int32_t *seq_lens, int32_t bat
     return PKV_OK;
 }
 
+int pkv_slot_mapping_all(const int32_t *tables, const int32_t *seq_lens, int32_t batch,
+                         int32_t max_blocks, int32_t block_size, int64_t *slots_out)
+{
+    if (batch < 0 || max_blocks < 1 || block_size < 1) return PKV_ERR_INVALID;
+    if (batch > 0 && (!tables || !seq_lens || !slots_out)) return PKV_ERR_INVALID;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t L = seq_lens[b];
+        if (L < 1 || L > (int64_t)max_blocks * block_size) return PKV_ERR_INVALID;
+        const int32_t *row = tables + (int64_t)b * max_blocks;
+        for (int64_t j = 0; j < (L + block_size - 1) / block_size; ++j)
+            if (row[j] < 0) return PKV_ERR_INVALID;
+    }
+    int64_t k = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int32_t *row = tables + (int64_t)b * max_blocks;
+        for (int64_t pos = 0; pos < seq_lens[b]; ++pos)
+            slots_out[k++] = (int64_t)row[pos / block_size] * block_size + pos % block_size;
+    }
+    return PKV_OK;
+}
+
 int pkv_pool_attach_device(pkv_pool *pool, int device)
 {
     if (!pool || device < 0) return PKV_ERR_INVALID;

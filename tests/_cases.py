@@ -136,9 +136,12 @@ def gpu_step(c: Case, opts=None, append=True):
     B, Hq, D = c.q.shape
     out = torch.empty_like(c.q)
     nbytes = pkv.decode_workspace_bytes(c.pool, B, Hq, bt.shape[1], opts)
-    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=c.q.device) if nbytes else None
+    assert nbytes > 0
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=c.q.device)
     pkv.paged_attention_decode(c.pool, c.q, c.key_cache, c.value_cache, bt, sl, c.w.scale, out,
                                ws, opts)
     st, bits = c.pool.get_device_error()
     assert st == pkv.OK and bits == 0, (st, bits)
+    counters = ws[:B * c.w.num_kv_heads * 4].view(torch.int32)
+    assert int(torch.count_nonzero(counters)) == 0, "split counters not returned to zero"
     return out

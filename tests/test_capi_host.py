@@ -63,6 +63,7 @@ def test_block_tables_and_slots_equal_the_oracle(lib, name):
     assert np.array_equal(t_orc, t_pkv)
     assert p.num_free() == len(a.free)
     assert np.array_equal(pkv.slot_mapping(t_pkv, L), oracle.slot_mapping(t_orc, L))
+    assert np.array_equal(pkv.slot_mapping_all(t_pkv, L), oracle.all_slots(t_orc, L))
     for blk in {int(x) for x in t_orc.ravel() if x >= 0}:
         assert p.refcount(blk) == a.refcount[blk]
     # return everything: the free lists stay in lock-step
@@ -119,13 +120,15 @@ def test_allocator_errors(lib):
         pkv.slot_mapping(np.array([[5, -1]], np.int32), np.array([20], np.int32))
 
 
-def test_decode_workspace_bytes_follows_the_partition_plan(lib):
+def test_decode_workspace_bytes_follows_the_plan(lib):
+    # with the grid fixed, no device query is needed: counters + two partials per CTA
     p = pkv.Pool(64, 8, 128)
-    assert pkv.decode_workspace_bytes(p, 64, 32, 128, {"partition_blocks": 128}) == 0
-    ws = pkv.decode_workspace_bytes(p, 4, 64, 2048, {"partition_blocks": 128})
-    rows = 4 * 64 * 16
-    assert ws >= rows * 128 * 4 + rows * 2 * 4
-    assert pkv.decode_workspace_bytes(p, 4, 60, 2048, None) == 0     # Hq % Hkv != 0
+    ws = pkv.decode_workspace_bytes(p, 64, 32, 128, {"grid_ctas": 300})
+    rows = 300 * 2 * 4
+    assert ws >= 64 * 8 * 4 + rows * 128 * 4 + rows * 2 * 4
+    assert pkv.decode_workspace_bytes(p, 4, 60, 2048, {"grid_ctas": 8}) == 0      # Hq % Hkv != 0
+    assert pkv.decode_workspace_bytes(p, 4, 8 * 17, 2048, {"grid_ctas": 8}) == 0  # group > 16
+    assert pkv.decode_workspace_bytes(p, 5000, 32, 8, {"grid_ctas": 8}) == 0      # batch > 4096
 
 
 def test_device_calls_need_an_attached_pool(lib):

@@ -104,7 +104,7 @@ def _custom(lens, Hq, Hkv, D, kv, seed=7):
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "%s-g%d-D%d-%s" % (len(s[0]), s[1] // s[2], s[3], s[4]))
-def test_shapes_both_variants_and_partitions(shape):
+def test_shapes_both_variants_and_grids(shape):
     lens, Hq, Hkv, D, kv = shape
     c = _custom(lens, Hq, Hkv, D, kv)
     bt, sl, slots = C.device_tables(c)
@@ -113,21 +113,22 @@ def test_shapes_both_variants_and_partitions(shape):
         _append_bit_exact(c)
     ref = C.oracle_decode(c)
     variants = [2] + ([1] if Hq // Hkv <= 8 else [])
-    single = None
     for variant in variants:
-        for pb in (0, 1, 3, 16, 1000):
-            out = C.gpu_step(c, dict(variant=variant, partition_blocks=pb), append=False)
+        # grid 1: every unit whole in one CTA; small grids: units cut across CTAs
+        for grid in (0, 1, 2, 3, 7, 64, 1000):
+            out = C.gpu_step(c, dict(variant=variant, grid_ctas=grid), append=False)
             C.tol_check(C.bf16_to_f64(out), ref)
-            if variant == 2 and pb == 1000:
-                single = out
-    for nw, ns in ((4, 3), (8, 2), (2, 4)):
-        out = C.gpu_step(c, dict(variant=2, warps_per_cta=nw, stages=ns), append=False)
-        C.tol_check(C.bf16_to_f64(out), ref)
-    # a sequence that fits one partition gives the same bits whatever the partition size
-    fits = [b for b, L in enumerate(lens) if L <= 16 * 16]
-    out16 = C.gpu_step(c, dict(variant=2, partition_blocks=16), append=False)
-    for b in fits:
-        assert torch.equal(out16[b], single[b])
+    for nw, ns in ((4, 2), (4, 4), (8, 2), (8, 3)):
+        for grid in (0, 5):
+            opts = dict(variant=2, warps_per_cta=nw, stages=ns, grid_ctas=grid)
+            if pkv.decode_workspace_bytes(c.pool, len(lens), Hq, bt.shape[1], opts) == 0:
+                continue                        # this ring does not fit in shared memory
+            out = C.gpu_step(c, opts, append=False)
+            C.tol_check(C.bf16_to_f64(out), ref)
+    # the same call twice gives the same bits
+    a = C.gpu_step(c, dict(grid_ctas=7), append=False)
+    b = C.gpu_step(c, dict(grid_ctas=7), append=False)
+    assert torch.equal(a, b)
 
 
 def test_physical_placement_does_not_change_a_single_bit():
@@ -146,7 +147,7 @@ def test_physical_placement_does_not_change_a_single_bit():
         c.key_cache[pt] = kc0
         c.value_cache[pt] = vc0
         c.tables = np.where(t0 >= 0, perm[np.maximum(t0, 0)], -1).astype(np.int32)
-        for opts in (None, dict(partition_blocks=3), dict(variant=1), dict(warps_per_cta=8)):
+        for opts in (None, dict(grid_ctas=3), dict(grid_ctas=11), dict(variant=1), dict(warps_per_cta=8)):
             by_opts.setdefault(repr(opts), []).append(C.gpu_step(c, opts, append=False))
     for o, lst in by_opts.items():
         assert np.isfinite(lst[0].float().cpu().numpy()).all()
@@ -182,15 +183,17 @@ def test_device_errors_are_flagged_not_trapped():
     c = _custom((18, 33), 8, 2, 64, "bf16")
     bt, sl, slots = C.device_tables(c)
     out = torch.empty_like(c.q)
+    ws = torch.zeros(pkv.decode_workspace_bytes(c.pool, 2, 8, 3), dtype=torch.uint8, device="cuda")
     bad = bt.clone()
     bad[1, 2] = c.pool.desc.num_blocks + 5
-    pkv.paged_attention_decode(c.pool, c.q, c.key_cache, c.value_cache, bad, sl, 0.125, out)
+    pkv.paged_attention_decode(c.pool, c.q, c.key_cache, c.value_cache, bad, sl, 0.125, out, ws)
     st, bits = c.pool.get_device_error()
     assert st == pkv.ERR_DEVICE and bits & pkv.DEVERR_BLOCK_ID
     for L in (0, 3 * 16 + 1):
         sl2 = sl.clone()
         sl2[0] = L
-        pkv.paged_attention_decode(c.pool, c.q, c.key_cache, c.value_cache, bt, sl2, 0.125, out)
+        ws.zero_()
+        pkv.paged_attention_decode(c.pool, c.q, c.key_cache, c.value_cache, bt, sl2, 0.125, out, ws)
         st, bits = c.pool.get_device_error()
         assert st == pkv.ERR_DEVICE and bits == pkv.DEVERR_SEQ_LEN
         assert torch.count_nonzero(out[0]) == 0
@@ -214,20 +217,25 @@ def test_host_side_argument_errors():
     c = _custom((18, 33), 8, 2, 64, "bf16")
     bt, sl, slots = C.device_tables(c)
     out = torch.empty_like(c.q)
+    ws0 = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
     with pytest.raises(pkv.PkvError):                        # misaligned q
         q2 = torch.empty(c.q.numel() + 1, dtype=torch.bfloat16, device="cuda")[1:].view_as(c.q)
-        pkv.paged_attention_decode(c.pool, q2, c.key_cache, c.value_cache, bt, sl, 0.125, out)
+        pkv.paged_attention_decode(c.pool, q2, c.key_cache, c.value_cache, bt, sl, 0.125, out, ws0)
     with pytest.raises(pkv.PkvError):                        # Hq not a multiple of Hkv
         q3 = torch.zeros(2, 7, 64, dtype=torch.bfloat16, device="cuda")
         pkv.paged_attention_decode(c.pool, q3, c.key_cache, c.value_cache, bt, sl, 0.125,
-                                   torch.empty_like(q3))
-    with pytest.raises(pkv.PkvError):                        # split plan without workspace
+                                   torch.empty_like(q3), ws0)
+    with pytest.raises(pkv.PkvError):                        # no workspace
         pkv.paged_attention_decode(c.pool, c.q, c.key_cache, c.value_cache, bt, sl, 0.125, out,
-                                   None, dict(partition_blocks=1))
+                                   None)
+    ws = torch.zeros(pkv.decode_workspace_bytes(c.pool, 2, 8, 3), dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PkvError):                        # workspace too small
+        pkv.paged_attention_decode(c.pool, c.q, c.key_cache, c.value_cache, bt, sl, 0.125, out,
+                                   ws[:256])
     with pytest.raises(pkv.PkvError):                        # CUDA-core variant is group <= 8
         q4 = torch.zeros(2, 32, 64, dtype=torch.bfloat16, device="cuda")
         pkv.paged_attention_decode(c.pool, q4, c.key_cache, c.value_cache, bt, sl, 0.125,
-                                   torch.empty_like(q4), None, dict(variant=1))
+                                   torch.empty_like(q4), ws0, dict(variant=1))
     assert pool_ok(c)
 
 
