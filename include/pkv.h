@@ -185,6 +185,28 @@ int pkv_paged_attention_decode_ex(pkv_pool *pool, const void *q, const void *key
                                   size_t workspace_bytes, const pkv_decode_opts *opts,
                                   void *stream);
 
+/* Bytes of the fixed device scratch behind pkv_paged_attention_decode_noalloc. */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Paged decode attention that allocates nothing and takes no workspace.  The pages describe
+ * no such call; it exists for hosts that cannot allocate device memory while they run (a
+ * memory manager that owns every device byte, or a latency-bound loop that cannot afford an
+ * allocation's synchronisation, cost or failure).  Same arguments, result and errors as
+ * pkv_paged_attention_decode without the workspace: the scratch is a fixed array of
+ * PKV_NOALLOC_SCRATCH_BYTES compiled into the library, held by every GPU that loads it
+ * until the process exits.  Returns PKV_ERR_INVALID, launching nothing, if the shape needs
+ * more scratch than that (pkv_decode_workspace_bytes() tells how much it needs).  The
+ * first call on a device looks up the array's device address (once per device, with that
+ * device current); make that first call before any stream capture.  Every call clears the
+ * array's counters with an asynchronous memset on `stream`, then runs the same kernel as
+ * pkv_paged_attention_decode.  All calls on a device share the array, so calls that
+ * overlap on the GPU race and must not be issued.  The pool must be attached beforehand
+ * (pkv_pool_attach_device allocates its 4-byte error word once). */
+int pkv_paged_attention_decode_noalloc(pkv_pool *pool, const void *q, const void *key_cache,
+                                       const void *value_cache, const int32_t *block_tables,
+                                       const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                       int32_t max_blocks, float scale, void *out, void *stream);
+
 /* Synchronise the stream, read the pool's device error word into *bits_out and clear it.
  * Returns PKV_OK if it was zero, PKV_ERR_TIMEOUT if the timeout bit was set, else
  * PKV_ERR_DEVICE. */

@@ -36,7 +36,8 @@ EXPORTED = (
     "pkv_build_block_tables", "pkv_slot_mapping", "pkv_slot_mapping_all",
     "pkv_pool_attach_device", "pkv_kv_append",
     "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
-    "pkv_paged_attention_decode_ex", "pkv_get_device_error", "pkv_probe_copy",
+    "pkv_paged_attention_decode_ex", "pkv_paged_attention_decode_noalloc",
+    "pkv_get_device_error", "pkv_probe_copy",
     "pkv_device_sm_count", "pkv_status_string",
 )
 
@@ -92,6 +93,8 @@ def lib():
             "pkv_paged_attention_decode_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
                                                              ctypes.c_float, _P, _P, ctypes.c_size_t,
                                                              ctypes.POINTER(decode_opts), _P]),
+            "pkv_paged_attention_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32,
+                                                                  _I32, ctypes.c_float, _P, _P]),
             "pkv_get_device_error": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
             "pkv_probe_copy": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
             "pkv_device_sm_count": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(_I32)]),
@@ -272,6 +275,19 @@ def paged_attention_decode(pool: Pool, q, key_cache, value_cache, block_tables, 
         _dev_ptr(seq_lens, "seq_lens"), int(B), int(Hq), int(block_tables.shape[1]),
         float(scale), _dev_ptr(out, "out"), _dev_ptr(workspace, "workspace"), int(ws_bytes),
         ctypes.byref(o) if o else None, _stream_ptr(stream)), "paged_attention_decode")
+
+
+def paged_attention_decode_noalloc(pool: Pool, q, key_cache, value_cache, block_tables,
+                                   seq_lens, scale: float, out, stream=None):
+    """Decode without a workspace, for callers that cannot allocate device memory at run
+    time: the scratch is a fixed array inside the library (pkv.h documents its limit and
+    that overlapping calls race on it)."""
+    B, Hq, _ = q.shape
+    _check(lib().pkv_paged_attention_decode_noalloc(
+        pool.handle, _dev_ptr(q, "q"), _dev_ptr(key_cache, "key_cache"),
+        _dev_ptr(value_cache, "value_cache"), _dev_ptr(block_tables, "block_tables"),
+        _dev_ptr(seq_lens, "seq_lens"), int(B), int(Hq), int(block_tables.shape[1]),
+        float(scale), _dev_ptr(out, "out"), _stream_ptr(stream)), "paged_attention_decode_noalloc")
 
 
 def probe_copy(dst, src, stream=None):
