@@ -182,17 +182,21 @@ def run_ours(args, world, rank, local_rank):
     sl = torch.from_numpy(d.seq_lens).to(dev)
     sm = torch.from_numpy(slots).to(dev)
     out = torch.empty_like(d.q)
-    ws_bytes = pkv.decode_workspace_bytes(pool, B, Hq, d.max_blocks)
+    decode_opts = json.loads(args.opts) if args.opts else None
+    ws_bytes = pkv.decode_workspace_bytes(pool, B, Hq, d.max_blocks, decode_opts)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    launches_per_step = (1 if w.append else 0) + 1
+    launches_per_step = (1 if w.append and args.separate_append else 0) + 1
     # algorithmic bytes (no credit for tail-slot over-read; shared prefix blocks counted
     # once per reader here, i.e. logical bytes)
     kv_read = int(d.seq_lens.astype(np.int64).sum()) * Hkv * D * elem * 2
     decode_bytes = kv_read + 2 * B * Hq * D * 2 + B * d.max_blocks * 4 + B * 4
-    append_bytes = (B * 8 + 2 * B * Hkv * D * (2 + elem)) if w.append else 0
+    append_bytes = (2 * B * Hkv * D * (2 + elem) + (B * 8 if args.separate_append else 0)) if w.append else 0
     step_bytes = decode_bytes + append_bytes
+    # bytes of the timed decode launch: with decode_step it also reads k_new/v_new and writes
+    # the new rows
+    launch_bytes = decode_bytes + (2 * B * Hkv * D * (2 + elem) if w.append and not args.separate_append else 0)
 
     # same-process bandwidth denominator: the library's copy probe over 2 x 1 GiB
     src = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
@@ -229,10 +233,15 @@ def run_ours(args, world, rank, local_rank):
     def timed_step(i):
         flush_l2()                                # L2 flush (read), outside the timed interval
         starts[i].record(stream)
-        if w.append:
+        if w.append and args.separate_append:
             pkv.kv_append(pool, d.k_new, d.v_new, sm, kc, vc, stream=stream)
         mids[i].record(stream)
-        pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws, stream=stream)
+        if w.append and not args.separate_append:  # append + decode in one launch
+            pkv.decode_step(pool, d.q, d.k_new, d.v_new, kc, vc, bt, sl, w.scale, out, ws,
+                            opts=decode_opts, stream=stream)
+        else:
+            pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws, opts=decode_opts,
+                                       stream=stream)
         ends[i].record(stream)
 
     with torch.cuda.stream(stream):
@@ -272,7 +281,8 @@ def run_ours(args, world, rank, local_rank):
     host["out"] = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     tables_host = tables
     h2d = (host["q"].numel() * 2 + (host["k"].numel() * 2 * 2 if w.append else 0)
-           + tables_host.nbytes + host["sl"].numel() * 4 + (B * 8 if w.append else 0))
+           + tables_host.nbytes + host["sl"].numel() * 4
+           + (B * 8 if w.append and args.separate_append else 0))
     d2h = host["out"].numel() * 2
     e2e_steps = max(5, min(K, 200))
     bt_h = torch.from_numpy(tables_host).pin_memory()
@@ -283,17 +293,24 @@ def run_ours(args, world, rank, local_rank):
         flush_l2()
         torch.cuda.synchronize()
         ee[0].record()
-        slots_np = pkv.slot_mapping(tables_host, d.seq_lens)            # host allocator side
-        sm_h[:] = torch.from_numpy(slots_np)
+        if args.separate_append:
+            slots_np = pkv.slot_mapping(tables_host, d.seq_lens)        # host allocator side
+            sm_h[:] = torch.from_numpy(slots_np)
         d.q.copy_(host["q"], non_blocking=True)
         bt.copy_(bt_h, non_blocking=True)
         sl.copy_(host["sl"], non_blocking=True)
         if w.append:
             d.k_new.copy_(host["k"], non_blocking=True)
             d.v_new.copy_(host["v"], non_blocking=True)
-            sm.copy_(sm_h, non_blocking=True)
-            pkv.kv_append(pool, d.k_new, d.v_new, sm, kc, vc)
-        pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws)
+            if args.separate_append:
+                sm.copy_(sm_h, non_blocking=True)
+                pkv.kv_append(pool, d.k_new, d.v_new, sm, kc, vc)
+                pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws, opts=decode_opts)
+            else:
+                pkv.decode_step(pool, d.q, d.k_new, d.v_new, kc, vc, bt, sl, w.scale, out, ws,
+                                opts=decode_opts)
+        else:
+            pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws, opts=decode_opts)
         host["out"].copy_(out, non_blocking=True)
         ee[1].record()
         ee[1].synchronize()
@@ -307,7 +324,7 @@ def run_ours(args, world, rank, local_rank):
     peak, peak_src = _hbm_peak()
     ms_per_step = total / K * 1e3
     value = aggregate_value(world, kv_read, K, total)
-    achieved = decode_bytes / dec_mean / 1e9
+    achieved = launch_bytes / dec_mean / 1e9
     traffic = _profiled_traffic(args.workload)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -320,7 +337,10 @@ def run_ours(args, world, rank, local_rank):
                                                  "all %d" % d.seq_lens[0] if w.lengths == "fixed"
                                                  else "%s (sum %d)" % (w.lengths, int(d.seq_lens.sum())),
                                                  w.kv_dtype),
-            "step": ("kv_append + " if w.append else "") + "paged_attention_decode",
+            "step": ("kv_append + paged_attention_decode" if args.separate_append else
+                     "decode_step (append at L-1 + paged decode, one launch)") if w.append
+                    else "paged_attention_decode",
+            "decode_opts": decode_opts,
             "l2": "flushed between steps (read of a 2x L2 buffer); inputs also exceed L2",
             "parallelism": "replicas",
             "timing": "CUDA events around each step on the launch stream; flush outside them",
@@ -330,8 +350,9 @@ def run_ours(args, world, rank, local_rank):
         "step_bytes": step_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "paged_attention_decode (decode_mma_kernel)",
-                     "bytes_per_launch": decode_bytes, "peak_source": peak_src + " hbm_gbs",
+                     "kernel": "decode_mma_kernel (%s)" % ("decode_step" if w.append and not args.separate_append
+                                                           else "paged_attention_decode"),
+                     "bytes_per_launch": launch_bytes, "peak_source": peak_src + " hbm_gbs",
                      "same_run_copy_gbs": round(copy_gbs, 1)},
         "e2e": {"value": round(world * kv_read / e2e_step / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -441,6 +462,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=64)
+    ap.add_argument("--separate-append", action="store_true",
+                    help="time kv_append and decode as two launches instead of decode_step")
+    ap.add_argument("--opts", default="", help='decode knobs as JSON, e.g. {"warps_per_cta": 8}')
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -144,7 +144,7 @@ typedef struct {
     int32_t grid_ctas;        /* CTAs of the persistent grid (0 = SM count x CTAs per SM) */
     int32_t variant;          /* 0 = auto, 1 = CUDA-core dot products, 2 = tensor-core mma */
     int32_t warps_per_cta;    /* 0 = auto (4); 4 or 8 */
-    int32_t stages;           /* 0 = auto (2); per-warp shared-memory pipeline depth 2..4 */
+    int32_t stages;           /* 0 = auto (16 KiB of tiles: 2 bf16 / 4 FP8 at D 128); 2..4 */
 } pkv_decode_opts;
 
 /* Device workspace bytes the decode needs for this shape and these opts (0 if the shape or
@@ -184,6 +184,21 @@ int pkv_paged_attention_decode_ex(pkv_pool *pool, const void *q, const void *key
                                   int32_t max_blocks, float scale, void *out, void *workspace,
                                   size_t workspace_bytes, const pkv_decode_opts *opts,
                                   void *stream);
+
+/* One whole decode step in one launch [Decode][Slot][Attn]: the new token of every sequence,
+ * at position L_b - 1, has its K and V rows (k_new, v_new: device bf16 [batch, Hkv, D])
+ * written into slot table[b][(L_b-1)/16]*16 + (L_b-1)%16 of the caches -- exactly what
+ * pkv_slot_mapping + pkv_kv_append store (FP8 pools encode them the same way) -- and then
+ * every sequence attends over positions 0 .. L_b-1 as in pkv_paged_attention_decode.  Each
+ * row is written by the CTA that streams that block, just before it loads the block, so
+ * no other launch and no slot mapping is needed.  The block holding the new token must not
+ * be shared with another sequence (copy it first).  Other arguments, workspace rules and
+ * errors as pkv_paged_attention_decode_ex. */
+int pkv_decode_step(pkv_pool *pool, const void *q, const void *k_new, const void *v_new,
+                    void *key_cache, void *value_cache, const int32_t *block_tables,
+                    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
+                    float scale, void *out, void *workspace, size_t workspace_bytes,
+                    const pkv_decode_opts *opts, void *stream);
 
 /* Bytes of the fixed device scratch behind pkv_paged_attention_decode_noalloc. */
 #define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)

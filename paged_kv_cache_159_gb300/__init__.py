@@ -13,6 +13,7 @@ Names follow the C ABI without the ``pkv_`` prefix:
 * ``kv_append(pool, k, v, slot_mapping, key_cache, value_cache)``.
 * ``paged_attention_decode(pool, q, key_cache, value_cache, block_tables, seq_lens, scale,
   out, workspace=None, opts=None)``.
+* ``decode_step(...)`` -- append each new token at position L-1 and decode, one launch.
 * ``decode_workspace_bytes``, ``probe_copy``, ``device_sm_count``.
 """
 from __future__ import annotations
@@ -36,7 +37,7 @@ EXPORTED = (
     "pkv_build_block_tables", "pkv_slot_mapping", "pkv_slot_mapping_all",
     "pkv_pool_attach_device", "pkv_kv_append",
     "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
-    "pkv_paged_attention_decode_ex", "pkv_paged_attention_decode_noalloc",
+    "pkv_paged_attention_decode_ex", "pkv_decode_step", "pkv_paged_attention_decode_noalloc",
     "pkv_get_device_error", "pkv_probe_copy",
     "pkv_device_sm_count", "pkv_status_string",
 )
@@ -93,6 +94,9 @@ def lib():
             "pkv_paged_attention_decode_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
                                                              ctypes.c_float, _P, _P, ctypes.c_size_t,
                                                              ctypes.POINTER(decode_opts), _P]),
+            "pkv_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
+                                               ctypes.c_float, _P, _P, ctypes.c_size_t,
+                                               ctypes.POINTER(decode_opts), _P]),
             "pkv_paged_attention_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32,
                                                                   _I32, ctypes.c_float, _P, _P]),
             "pkv_get_device_error": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -275,6 +279,22 @@ def paged_attention_decode(pool: Pool, q, key_cache, value_cache, block_tables, 
         _dev_ptr(seq_lens, "seq_lens"), int(B), int(Hq), int(block_tables.shape[1]),
         float(scale), _dev_ptr(out, "out"), _dev_ptr(workspace, "workspace"), int(ws_bytes),
         ctypes.byref(o) if o else None, _stream_ptr(stream)), "paged_attention_decode")
+
+
+def decode_step(pool: Pool, q, k_new, v_new, key_cache, value_cache, block_tables, seq_lens,
+                scale: float, out, workspace, opts=None, stream=None):
+    """Append every sequence's new K/V (bf16 CUDA [B, Hkv, D]) at position L-1 and decode,
+    in one launch (pkv_decode_step)."""
+    B, Hq, _ = q.shape
+    o = _opts(opts)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pkv_decode_step(
+        pool.handle, _dev_ptr(q, "q"), _dev_ptr(k_new, "k_new"), _dev_ptr(v_new, "v_new"),
+        _dev_ptr(key_cache, "key_cache"), _dev_ptr(value_cache, "value_cache"),
+        _dev_ptr(block_tables, "block_tables"), _dev_ptr(seq_lens, "seq_lens"), int(B), int(Hq),
+        int(block_tables.shape[1]), float(scale), _dev_ptr(out, "out"),
+        _dev_ptr(workspace, "workspace"), int(ws_bytes), ctypes.byref(o) if o else None,
+        _stream_ptr(stream)), "decode_step")
 
 
 def paged_attention_decode_noalloc(pool: Pool, q, key_cache, value_cache, block_tables,

@@ -80,16 +80,19 @@ struct DecodeParams {
     float *part_o;                // [G][2][group][D]   unnormalised partial outputs
     float *part_ml;               // [G][2][group][2]   (running max in log2 units, sum)
     uint32_t *err;
+    const uint16_t *k_new;        // bf16 [B, Hkv, D]: appended at position L-1 (or null)
+    const uint16_t *v_new;
     int B, Hq, Hkv, group, MB, num_blocks;
     float score_scale;            // scale * k_scale * log2(e)
     float out_scale;              // v_scale (1 for bf16 pools)
+    float inv_k_scale, inv_v_scale;   // fl32(1/scale) for FP8 appends
 };
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 // Shared-memory plan of one CTA (host and device agree on it).
 struct Layout {
-    int stage, q, ml, acc, prefix, phys, bar, flag, total;
+    int stage, q, ml, acc, prefix, lens, phys, bar, flag, total;
     __host__ __device__ Layout(int NW, int NS, int tile, int D, int group, int B)
     {
         int o = 0;
@@ -98,6 +101,7 @@ struct Layout {
         ml = o;     o += NW * 16 * 2 * 4;                        // per-warp (max, sum) rows
         acc = o;    o += align_up(NW * group * (D + ACC_PAD) * 4, 128);
         prefix = o; o += align_up((B + 1) * 4, 16);              // task prefix over sequences
+        lens = o;   o += align_up(B * 4, 16);                    // seq_lens
         phys = o;   o += align_up(NW * NS * 4, 16);              // tile index per stage
         bar = o;    o += (NW * NS + 2) * 8;                      // stage + q barriers
         flag = o;   o += 64;                                    // scan scratch / merge flag
@@ -487,14 +491,35 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
     const int c = blockIdx.x;
     const int Hkv = p.Hkv, group = p.group;
 
+    // ---- 0. warm L2 with this CTA's share of the block tables and queries (hints), and
+    //         set up the barriers; both overlap the scan below.
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar);
+    const uint32_t qbar0 = dev::smem_u32(bars + NW * NS);
+    if (tid == 0) {
+        auto slice = [&](const void *base, size_t bytes) {
+            const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + bytes * c / gridDim.x + 15) & ~uintptr_t(15);
+            const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base) + bytes * (c + 1) / gridDim.x) & ~uintptr_t(15);
+            if (a1 > a0) dev::prefetch_l2(reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0));
+        };
+        slice(p.block_tables, (size_t)p.B * p.MB * 4);
+        slice(p.q, (size_t)p.B * p.Hq * D * 2);
+        dev::mbar_init(qbar0, 1);
+        dev::mbar_init(qbar0 + 8, 1);
+    }
+    if (lane == 0)
+        for (int st = 0; st < NS; ++st) dev::mbar_init(dev::smem_u32(bars + warp * NS + st), 1);
+    dev::fence_barrier_init();
+
     // ---- 1. tasks per sequence (Hkv * ceil(L/16); 0 for an invalid length) and their
     //         exclusive prefix, by a block-wide scan; CTA 0 zeroes invalid sequences' rows.
+    int32_t *lens = reinterpret_cast<int32_t *>(smem + lay.lens);
     {
         const int per = (p.B + NTHR - 1) / NTHR;
         const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
         int run = 0;
         for (int b = b0; b < b1; ++b) {
             const int L = __ldg(p.seq_lens + b);
+            lens[b] = L;
             const bool ok = L >= 1 && L <= p.MB * BS;
             if (!ok && c == 0) {
                 dev::flag_error(p.err, PKV_DEVERR_SEQ_LEN);
@@ -516,7 +541,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
         int acc = base + incl - run;                       // exclusive prefix of b0
         for (int b = b0; b < b1; ++b) {
             prefix[b] = acc;
-            const int L = __ldg(p.seq_lens + b);
+            const int L = lens[b];
             const bool ok = L >= 1 && L <= p.MB * BS;
             acc += ok ? Hkv * ((L + BS - 1) / BS) : 0;
         }
@@ -530,18 +555,6 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
     if (c >= G) return;                                    // uniform over the CTA
     const long long s = task_start(c, W, G), e = task_start(c + 1, W, G);
 
-    // ---- 2. barriers
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar);
-    const uint32_t qbar0 = dev::smem_u32(bars + NW * NS);
-    if (lane == 0)
-        for (int st = 0; st < NS; ++st) dev::mbar_init(dev::smem_u32(bars + warp * NS + st), 1);
-    if (tid == 0) {
-        dev::mbar_init(qbar0, 1);
-        dev::mbar_init(qbar0 + 8, 1);
-    }
-    dev::fence_barrier_init();
-    __syncthreads();
-
     // Unit geometry of task r: sequence, head, first task of the unit, blocks in it.
     struct Unit { int b, h, L, nb; long long U0; };
     auto unit_of = [&](long long r) {
@@ -551,7 +564,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
         u.nb = tasks / Hkv;
         u.h = (int)(r - prefix[u.b]) / u.nb;
         u.U0 = prefix[u.b] + (long long)u.h * u.nb;
-        u.L = __ldg(p.seq_lens + u.b);
+        u.L = lens[u.b];
         return u;
     };
     const int qbytes = group * D * 2;
@@ -568,9 +581,11 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
     const int n_mine = (int)max(0LL, (e - s - warp + NW - 1) / NW);
     // tile index (phys * Hkv + h, or -1 if the table entry is invalid) of warp task i, for a
     // chunk of 32 tasks: lane j holds task chunk*32 + j
-    auto load_tiles = [&](int chunk) {
+    // and, when appending, b*16 + the new token's offset if task i is its unit's last block
+    auto load_tiles = [&](int chunk, int &app) {
         const int i = chunk * 32 + lane;
         int t = -1;
+        app = -1;
         if (i < n_mine) {
             const long long r = s + warp + (long long)NW * i;
             const Unit u = unit_of(r);
@@ -578,16 +593,61 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
             const int id = __ldg(p.block_tables + (size_t)u.b * p.MB + blk);
             if (id >= 0 && id < p.num_blocks) t = id * Hkv + u.h;
             else dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+            if (p.k_new && blk == u.nb - 1 && t >= 0) app = u.b * BS + (u.L - 1) % BS;
         }
         return t;
     };
-    int tcur = load_tiles(0), tnext = load_tiles(1);
+    int acur, anext;
+    int tcur = load_tiles(0, acur), tnext = load_tiles(1, anext);
     auto issue = [&](int i) {                              // warp-collective
         if ((i & 31) == 0 && i > 0) {
             tcur = tnext;
-            tnext = load_tiles((i >> 5) + 1);
+            acur = anext;
+            tnext = load_tiles((i >> 5) + 1, anext);
         }
         const int t = __shfl_sync(dev::FULL, tcur, i & 31);
+        const int a = __shfl_sync(dev::FULL, acur, i & 31);
+        if (a >= 0) {
+            // this block holds the new token: write its K/V row into the slot first, then
+            // order those generic writes before the bulk copy that reads the block
+            const int b = a / BS, off = a % BS, h = t % Hkv;
+            const size_t src = ((size_t)b * Hkv + h) * D;
+            const size_t dst = ((size_t)t * BS + off) * D;               // element index
+            constexpr int EPL = D / 32;
+            if constexpr (FP8) {
+                const uint16_t *ks = p.k_new + src + lane * EPL;
+                const uint16_t *vs = p.v_new + src + lane * EPL;
+                uint32_t kc = 0, vc = 0;
+#pragma unroll
+                for (int e = 0; e < EPL; e += 2) {
+                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(ks + e);
+                    const uint32_t vw = *reinterpret_cast<const uint32_t *>(vs + e);
+                    kc |= dev::e4m3x2_satfinite(dev::bf16_lo(kw) * p.inv_k_scale, dev::bf16_hi(kw) * p.inv_k_scale) << (8 * e);
+                    vc |= dev::e4m3x2_satfinite(dev::bf16_lo(vw) * p.inv_v_scale, dev::bf16_hi(vw) * p.inv_v_scale) << (8 * e);
+                }
+                uint8_t *kd = const_cast<uint8_t *>(p.key_cache) + dst + lane * EPL;
+                uint8_t *vd = const_cast<uint8_t *>(p.value_cache) + dst + lane * EPL;
+                if constexpr (EPL == 4) {
+                    *reinterpret_cast<uint32_t *>(kd) = kc;
+                    *reinterpret_cast<uint32_t *>(vd) = vc;
+                } else {
+                    *reinterpret_cast<uint16_t *>(kd) = (uint16_t)kc;
+                    *reinterpret_cast<uint16_t *>(vd) = (uint16_t)vc;
+                }
+            } else {
+                uint16_t *kd = reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(p.key_cache)) + dst + lane * EPL;
+                uint16_t *vd = reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(p.value_cache)) + dst + lane * EPL;
+                if constexpr (EPL == 4) {
+                    *reinterpret_cast<uint2 *>(kd) = *reinterpret_cast<const uint2 *>(p.k_new + src + lane * EPL);
+                    *reinterpret_cast<uint2 *>(vd) = *reinterpret_cast<const uint2 *>(p.v_new + src + lane * EPL);
+                } else {
+                    *reinterpret_cast<uint32_t *>(kd) = *reinterpret_cast<const uint32_t *>(p.k_new + src + lane * EPL);
+                    *reinterpret_cast<uint32_t *>(vd) = *reinterpret_cast<const uint32_t *>(p.v_new + src + lane * EPL);
+                }
+            }
+            dev::fence_proxy_async_global();
+            __syncwarp();
+        }
         if (lane == 0) {
             const int st = i % NS;
             const uint32_t bar = dev::smem_u32(bars + warp * NS + st);
@@ -756,29 +816,45 @@ struct Plan {
 template <class K>
 cudaError_t prepare(K kernel, size_t smem, int threads, int *per_sm)
 {
-    // cudaFuncSetAttribute is cheap but not free; remember per (kernel, device, size).
+    // Once per (kernel, device): allow the device's full opt-in shared memory, so that no
+    // later call can lower the limit below a size that an earlier call relies on.  Once per
+    // (kernel, device, size): the occupancy, cached for the plan.
+    struct Entry { const void *fn; int dev; size_t smem; int per_sm; };
     static std::mutex mu;
-    static const void *seen_fn[256];
-    static int seen_dev[256];
-    static size_t seen_smem[256];
+    static Entry seen[1024];
     static int nseen = 0;
+    static const void *opted_fn[256];
+    static int opted_dev[256];
+    static int nopted = 0;
     int dev = 0;
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> g(mu);
-    bool known = false;
-    for (int i = 0; i < nseen; ++i)
-        if (seen_fn[i] == (const void *)kernel && seen_dev[i] == dev && seen_smem[i] >= smem) known = true;
-    if (!known) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    bool opted = false;
+    for (int i = 0; i < nopted; ++i)
+        if (opted_fn[i] == (const void *)kernel && opted_dev[i] == dev) opted = true;
+    if (!opted) {
+        int limit = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return e;
-        if (nseen < 256) {
-            seen_fn[nseen] = (const void *)kernel;
-            seen_dev[nseen] = dev;
-            seen_smem[nseen] = smem;
-            ++nseen;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+        if (e != cudaSuccess) return e;
+        if (nopted < 256) {
+            opted_fn[nopted] = (const void *)kernel;
+            opted_dev[nopted] = dev;
+            ++nopted;
         }
     }
-    if (per_sm) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kernel, threads, smem);
+    if (!per_sm) return cudaSuccess;
+    for (int i = 0; i < nseen; ++i)
+        if (seen[i].fn == (const void *)kernel && seen[i].dev == dev && seen[i].smem == smem) {
+            *per_sm = seen[i].per_sm;
+            return cudaSuccess;
+        }
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (nseen < 1024) seen[nseen++] = Entry{(const void *)kernel, dev, smem, n};
+    *per_sm = n;
     return cudaSuccess;
 }
 

@@ -46,13 +46,7 @@ __global__ void __launch_bounds__(256) kv_append_bf16_kernel(
     }
 }
 
-// Two floats -> two E4M3 codes (lo in the low byte), round to nearest even, saturating.
-__device__ __forceinline__ uint32_t e4m3x2_satfinite(float lo, float hi)
-{
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
+using dev::e4m3x2_satfinite;
 
 // 8 bf16 values scaled by inv then encoded: 16 bytes in, 8 bytes out.
 __device__ __forceinline__ uint2 encode8(uint4 x, float inv)

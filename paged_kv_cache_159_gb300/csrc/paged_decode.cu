@@ -61,7 +61,8 @@ int make_plan(const pkv_pool_desc &d, int B, int Hq, int MB, const pkv_decode_op
     if (pl.variant != 1 && pl.variant != 2) return PKV_ERR_INVALID;
     if (pl.variant == 1 && group > 8) return PKV_ERR_INVALID;
     pl.nw = o->warps_per_cta ? o->warps_per_cta : 4;
-    pl.ns = o->stages ? o->stages : 2;
+    // default ring: 16 KiB of tiles per warp (2 bf16 or 4 FP8 stages at head_dim 128)
+    pl.ns = o->stages ? o->stages : (elem_bytes(d) == 1 && pl.variant == 2 ? 4 : 2);
     if (o->grid_ctas < 0) return PKV_ERR_INVALID;
     const int tile = BS * d.head_dim * elem_bytes(d);
     pl.smem = Layout(pl.nw, pl.ns, tile, d.head_dim, group, B).total;
@@ -98,15 +99,16 @@ extern "C" size_t pkv_decode_workspace_bytes(const pkv_pool *pool, int32_t batch
     return pl.ws_bytes;
 }
 
-extern "C" int pkv_paged_attention_decode_ex(pkv_pool *pool, const void *q, const void *key_cache,
-                                             const void *value_cache, const int32_t *block_tables,
-                                             const int32_t *seq_lens, int32_t batch,
-                                             int32_t num_q_heads, int32_t max_blocks, float scale,
-                                             void *out, void *workspace, size_t workspace_bytes,
-                                             const pkv_decode_opts *opts, void *stream)
+namespace pkv {
+namespace decode {
+namespace {
+
+int decode_impl(pkv_pool *pool, const void *q, const void *k_new, const void *v_new,
+                const void *key_cache, const void *value_cache, const int32_t *block_tables,
+                const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
+                float scale, void *out, void *workspace, size_t workspace_bytes,
+                const pkv_decode_opts *opts, void *stream)
 {
-    using namespace pkv;
-    using namespace pkv::decode;
     int st = check_attached(pool);
     if (st != PKV_OK) return st;
     if (batch < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID;
@@ -116,6 +118,8 @@ extern "C" int pkv_paged_attention_decode_ex(pkv_pool *pool, const void *q, cons
     if (!aligned(q, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(out, 16) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
         return PKV_ERR_INVALID;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
+    if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))) return PKV_ERR_INVALID;
     const pkv_pool_desc &d = pool->desc;
     Plan pl;
     st = make_plan(d, batch, num_q_heads, max_blocks, opts, pl);
@@ -134,6 +138,8 @@ extern "C" int pkv_paged_attention_decode_ex(pkv_pool *pool, const void *q, cons
     p.part_o = reinterpret_cast<float *>(ws + pl.ws_o);
     p.part_ml = reinterpret_cast<float *>(ws + pl.ws_ml);
     p.err = pool->d_err;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
     p.B = batch;
     p.Hq = num_q_heads;
     p.Hkv = d.num_kv_heads;
@@ -142,10 +148,28 @@ extern "C" int pkv_paged_attention_decode_ex(pkv_pool *pool, const void *q, cons
     p.num_blocks = d.num_blocks;
     p.score_scale = scale * d.k_scale * LOG2E;
     p.out_scale = d.v_scale;
+    p.inv_k_scale = pool->inv_k_scale;
+    p.inv_v_scale = pool->inv_v_scale;
 
     cudaError_t e = dispatch(d, pl, p.group, true, nullptr, static_cast<cudaStream_t>(stream), &p);
     if (e == cudaErrorInvalidConfiguration) return PKV_ERR_INVALID;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace decode
+}  // namespace pkv
+
+extern "C" int pkv_paged_attention_decode_ex(pkv_pool *pool, const void *q, const void *key_cache,
+                                             const void *value_cache, const int32_t *block_tables,
+                                             const int32_t *seq_lens, int32_t batch,
+                                             int32_t num_q_heads, int32_t max_blocks, float scale,
+                                             void *out, void *workspace, size_t workspace_bytes,
+                                             const pkv_decode_opts *opts, void *stream)
+{
+    return pkv::decode::decode_impl(pool, q, nullptr, nullptr, key_cache, value_cache, block_tables,
+                                    seq_lens, batch, num_q_heads, max_blocks, scale, out, workspace,
+                                    workspace_bytes, opts, stream);
 }
 
 extern "C" int pkv_paged_attention_decode(pkv_pool *pool, const void *q, const void *key_cache,
@@ -154,7 +178,19 @@ extern "C" int pkv_paged_attention_decode(pkv_pool *pool, const void *q, const v
                                           int32_t max_blocks, float scale, void *out, void *workspace,
                                           size_t workspace_bytes, void *stream)
 {
-    return pkv_paged_attention_decode_ex(pool, q, key_cache, value_cache, block_tables, seq_lens, batch,
-                                         num_q_heads, max_blocks, scale, out, workspace, workspace_bytes,
-                                         nullptr, stream);
+    return pkv::decode::decode_impl(pool, q, nullptr, nullptr, key_cache, value_cache, block_tables,
+                                    seq_lens, batch, num_q_heads, max_blocks, scale, out, workspace,
+                                    workspace_bytes, nullptr, stream);
+}
+
+extern "C" int pkv_decode_step(pkv_pool *pool, const void *q, const void *k_new, const void *v_new,
+                               void *key_cache, void *value_cache, const int32_t *block_tables,
+                               const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                               int32_t max_blocks, float scale, void *out, void *workspace,
+                               size_t workspace_bytes, const pkv_decode_opts *opts, void *stream)
+{
+    if (!k_new || !v_new) return PKV_ERR_INVALID;
+    return pkv::decode::decode_impl(pool, q, k_new, v_new, key_cache, value_cache, block_tables,
+                                    seq_lens, batch, num_q_heads, max_blocks, scale, out, workspace,
+                                    workspace_bytes, opts, stream);
 }

@@ -145,6 +145,27 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Two floats -> two E4M3 codes (lo in the low byte), round to nearest even, saturating.
+__device__ __forceinline__ uint32_t e4m3x2_satfinite(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Order this thread's earlier generic-proxy global writes before later async-proxy (bulk
+// copy) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Hint: bring [ptr, ptr + bytes) into L2 (16-byte aligned start, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void flag_error(uint32_t *err, uint32_t bits)
 {
     if (err) atomicOr(err, bits);

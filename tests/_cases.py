@@ -67,7 +67,7 @@ def build(name: str, device="cuda", seq_lens=None, overrides=None, free_order=No
     kc[dead[:, None, :, None].expand_as(kc)] = nan
     vc[dead[:, None, :, None].expand_as(vc)] = nan
     slots_dev = torch.from_numpy(slots).to(device)
-    if w.append:                                               # the new token's slot starts as NaN
+    if w.append and w.kv_dtype != "fp8":                       # the new token's slot starts as NaN
         blk, off = slots_dev // 16, slots_dev % 16
         kc[blk, :, off, :] = nan
         vc[blk, :, off, :] = nan
@@ -81,8 +81,10 @@ def build(name: str, device="cuda", seq_lens=None, overrides=None, free_order=No
         blk, off = all_slots // 16, all_slots % 16
         k_src = kc[blk, :, off, :].contiguous()                # [T, Hkv, D]
         v_src = vc[blk, :, off, :].contiguous()
-        k_scale = float(np.float32(k_src.float().abs().max().item()) / np.float32(448.0))
-        v_scale = float(np.float32(v_src.float().abs().max().item()) / np.float32(448.0))
+        kmax = max(k_src.float().abs().max().item(), d.k_new.float().abs().max().item())
+        vmax = max(v_src.float().abs().max().item(), d.v_new.float().abs().max().item())
+        k_scale = float(np.float32(kmax) / np.float32(448.0))
+        v_scale = float(np.float32(vmax) / np.float32(448.0))
         pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim, kv_dtype, k_scale, v_scale, order)
         pool.attach_device(torch.cuda.current_device())
         k8 = torch.full(kc.shape, FP8_NAN, dtype=torch.uint8, device=device)
@@ -96,6 +98,13 @@ def build(name: str, device="cuda", seq_lens=None, overrides=None, free_order=No
                                 oracle.FP8E4M3, k_scale, v_scale) == 0
         pkv.kv_append(pool, k_src, v_src, all_slots, k8, v8)
         torch.cuda.synchronize()
+        if w.append:                                           # the new token's slot starts as NaN
+            blk, off = slots_dev // 16, slots_dev % 16
+            k8[blk, :, off, :] = FP8_NAN
+            v8[blk, :, off, :] = FP8_NAN
+            for sl in slots:
+                key_host[sl // 16, :, sl % 16, :] = FP8_NAN
+                value_host[sl // 16, :, sl % 16, :] = FP8_NAN
         kc, vc = k8, v8
     else:
         pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim, free_order=order)
@@ -107,10 +116,11 @@ def build(name: str, device="cuda", seq_lens=None, overrides=None, free_order=No
 
 
 def oracle_append(c: Case):
-    """The oracle's kv_append on its own host pools (in place)."""
-    assert c.kv_dtype == pkv.KV_BF16
+    """The oracle's kv_append of each sequence's new token on its own host pools (in place)."""
+    fp8 = c.kv_dtype == pkv.KV_FP8E4M3
     st = oracle.kv_append(workloads.bf16_bits(c.k_new), workloads.bf16_bits(c.v_new), c.slots,
-                          c.key_host, c.value_host)
+                          c.key_host, c.value_host, 16, oracle.FP8E4M3 if fp8 else oracle.BF16,
+                          c.k_scale, c.v_scale)
     assert st == 0
 
 

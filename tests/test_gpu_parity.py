@@ -53,6 +53,40 @@ def test_full_size_workload(name):
     print("%s: max abs err %.3g, max rel err %.3g" % (name, mx, rel))
 
 
+@pytest.mark.parametrize("name,overrides", [
+    ("tiny", None),
+    ("llama3_8b", None),
+    ("ragged", None),
+    ("tiny", dict(batch=4, num_q_heads=28, num_kv_heads=4, head_dim=128, lengths="list",
+                  len_list=(1, 16, 17, 700), pool="double", kv_dtype="fp8", append=True, seed=5)),
+    ("tiny", dict(batch=3, num_q_heads=16, num_kv_heads=2, head_dim=64, lengths="list",
+                  len_list=(31, 32, 33), pool="double", kv_dtype="fp8", append=True, seed=6)),
+], ids=["tiny", "llama3_8b", "ragged", "fp8-d128", "fp8-d64"])
+def test_decode_step_equals_append_then_decode(name, overrides):
+    # one launch (append inside the decode kernel) == kv_append + decode, bit for bit, and
+    # the oracle agrees within tolerance
+    c = C.build(name, overrides=overrides)
+    bt, sl, slots = C.device_tables(c)
+    kc2, vc2 = c.key_cache.clone(), c.value_cache.clone()
+    out_two = C.gpu_step(c, dict(grid_ctas=0), append=True)          # kv_append + decode
+    B, Hq, _ = c.q.shape
+    ws = torch.zeros(pkv.decode_workspace_bytes(c.pool, B, Hq, bt.shape[1]), dtype=torch.uint8,
+                     device="cuda")
+    out_one = torch.empty_like(c.q)
+    pkv.decode_step(c.pool, c.q, c.k_new, c.v_new, kc2, vc2, bt, sl, c.w.scale, out_one, ws)
+    assert c.pool.get_device_error() == (pkv.OK, 0)
+    assert torch.equal(kc2.view(torch.uint8), c.key_cache.view(torch.uint8))
+    assert torch.equal(vc2.view(torch.uint8), c.value_cache.view(torch.uint8))
+    assert torch.equal(out_one, out_two)
+    C.oracle_append(c)
+    if c.kv_dtype == pkv.KV_BF16:
+        assert np.array_equal(workloads.bf16_bits(kc2), c.key_host)
+    else:
+        assert np.array_equal(kc2.cpu().numpy(), c.key_host)
+        assert np.array_equal(vc2.cpu().numpy(), c.value_host)
+    C.tol_check(C.bf16_to_f64(out_one), C.oracle_decode(c))
+
+
 def test_fp8_append_matches_oracle_encoder_bit_for_bit():
     # every finite bf16 value, as K and V rows, through the GPU encoder and the oracle's
     D, Hkv = 128, 4
