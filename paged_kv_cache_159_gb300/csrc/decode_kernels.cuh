@@ -54,6 +54,7 @@
 
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -93,18 +94,21 @@ __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / 
 // Shared-memory plan of one CTA (host and device agree on it).
 struct Layout {
     int stage, q, ml, acc, prefix, lens, phys, bar, flag, total;
+    int ml_slot, acc_slot;                                       // bytes of one merge slot
     __host__ __device__ Layout(int NW, int NS, int tile, int D, int group, int B)
     {
         int o = 0;
         stage = o;  o += NW * NS * 2 * tile;                      // K and V tiles per stage
         q = o;      o += 2 * align_up(group * D * 2, 128);       // two segments' q rows
-        ml = o;     o += NW * 16 * 2 * 4;                        // per-warp (max, sum) rows
-        acc = o;    o += align_up(NW * group * (D + ACC_PAD) * 4, 128);
+        ml_slot = NW * 16 * 2 * 4;                               // per-warp (max, sum) rows
+        ml = o;     o += 2 * ml_slot;
+        acc_slot = align_up(NW * group * (D + ACC_PAD) * 4, 128);
+        acc = o;    o += 2 * acc_slot;                           // per-warp accumulators
         prefix = o; o += align_up((B + 1) * 4, 16);              // task prefix over sequences
         lens = o;   o += align_up(B * 4, 16);                    // seq_lens
         phys = o;   o += align_up(NW * NS * 4, 16);              // tile index per stage
-        bar = o;    o += (NW * NS + 2) * 8;                      // stage + q barriers
-        flag = o;   o += 64;                                    // scan scratch / merge flag
+        bar = o;    o += (NW * NS + 6) * 8;                      // stages, q, segment done/free
+        flag = o;   o += 128;                                    // scan scratch, merge flag
         total = o;
     }
 };
@@ -474,14 +478,14 @@ struct SimtCompute {
 };
 
 // ------------------------------------------------------------------------------------
-// The decode kernel body.
+// The decode kernel body: NW streaming warps and one epilogue warp.
 // ------------------------------------------------------------------------------------
 template <int D, bool FP8, int NW, int NS, class Compute>
 __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
 {
     constexpr int ELEM = FP8 ? 1 : 2;
     constexpr int TILE = BS * D * ELEM;
-    constexpr int NTHR = NW * 32;
+    constexpr int NTHR = (NW + 1) * 32;
     extern __shared__ __align__(1024) uint8_t smem[];
     const Layout lay(NW, NS, TILE, D, p.group, p.B);
     int32_t *prefix = reinterpret_cast<int32_t *>(smem + lay.prefix);
@@ -494,7 +498,9 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
     // ---- 0. warm L2 with this CTA's share of the block tables and queries (hints), and
     //         set up the barriers; both overlap the scan below.
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar);
-    const uint32_t qbar0 = dev::smem_u32(bars + NW * NS);
+    const uint32_t qbar0 = dev::smem_u32(bars + NW * NS);         // q slot j full: +8*j
+    const uint32_t done0 = dev::smem_u32(bars + NW * NS + 2);     // merge slot j dumped
+    const uint32_t free0 = dev::smem_u32(bars + NW * NS + 4);     // merge slot j merged
     if (tid == 0) {
         auto slice = [&](const void *base, size_t bytes) {
             const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + bytes * c / gridDim.x + 15) & ~uintptr_t(15);
@@ -503,10 +509,13 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
         };
         slice(p.block_tables, (size_t)p.B * p.MB * 4);
         slice(p.q, (size_t)p.B * p.Hq * D * 2);
-        dev::mbar_init(qbar0, 1);
-        dev::mbar_init(qbar0 + 8, 1);
+        for (int j = 0; j < 2; ++j) {
+            dev::mbar_init(qbar0 + 8 * j, 1);
+            dev::mbar_init(done0 + 8 * j, NW * 32);
+            dev::mbar_init(free0 + 8 * j, 1);
+        }
     }
-    if (lane == 0)
+    if (lane == 0 && warp < NW)
         for (int st = 0; st < NS; ++st) dev::mbar_init(dev::smem_u32(bars + warp * NS + st), 1);
     dev::fence_barrier_init();
 
@@ -516,7 +525,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
     {
         const int per = (p.B + NTHR - 1) / NTHR;
         const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
-        int run = 0;
+        int run = 0, lo = INT_MAX, hi = -1;               // lo/hi: blocks per sequence
         for (int b = b0; b < b1; ++b) {
             const int L = __ldg(p.seq_lens + b);
             lens[b] = L;
@@ -525,7 +534,10 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
                 dev::flag_error(p.err, PKV_DEVERR_SEQ_LEN);
                 for (int e = 0; e < p.Hq * D; ++e) p.out[(size_t)b * p.Hq * D + e] = 0;
             }
-            run += ok ? Hkv * ((L + BS - 1) / BS) : 0;
+            const int nb = ok ? (L + BS - 1) / BS : 0;    // an invalid length breaks uniformity
+            run += Hkv * nb;
+            lo = min(lo, nb);
+            hi = max(hi, nb);
         }
         int incl = run;                                   // inclusive scan over the warp
 #pragma unroll
@@ -533,9 +545,40 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
             const int v = __shfl_up_sync(dev::FULL, incl, o);
             if (lane >= o) incl += v;
         }
-        int *wsum = flag;                                  // NW <= 8 warp totals
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            lo = min(lo, __shfl_xor_sync(dev::FULL, lo, o));
+            hi = max(hi, __shfl_xor_sync(dev::FULL, hi, o));
+        }
+        int *wsum = flag, *wlo = flag + 9, *whi = flag + 18;   // NW + 1 <= 9 warps
         if (lane == 31) wsum[warp] = incl;
+        if (lane == 0) {
+            wlo[warp] = lo;
+            whi[warp] = hi;
+        }
         __syncthreads();
+        if (warp == 0) {
+            // All units the same length (and at least as many units as CTAs): if the unit
+            // count has a divisor within 80% of the grid, work with that many CTAs, so that
+            // every CTA gets whole units and nothing is merged.  Lanes test 32 candidates at
+            // a time; the result goes to flag[30] (0: keep the grid).
+            int glo = INT_MAX, ghi = -1;
+            for (int w = 0; w <= NW; ++w) {
+                glo = min(glo, wlo[w]);
+                ghi = max(ghi, whi[w]);
+            }
+            const int units = p.B * Hkv, grid = (int)gridDim.x;
+            int pick = 0;
+            if (glo == ghi && glo > 0 && units >= grid) {
+                for (int g0 = grid; pick == 0 && 5 * g0 >= 4 * grid; g0 -= 32) {
+                    const int g2 = g0 - lane;
+                    const bool okd = g2 > 0 && 5 * g2 >= 4 * grid && units % g2 == 0;
+                    const unsigned m = __ballot_sync(dev::FULL, okd);
+                    if (m) pick = g0 - (__ffs(m) - 1);       // the largest divisor found
+                }
+            }
+            if (lane == 0) flag[30] = pick;
+        }
         int base = 0;
         for (int w = 0; w < warp; ++w) base += wsum[w];
         int acc = base + incl - run;                       // exclusive prefix of b0
@@ -551,7 +594,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
     const long long W = prefix[p.B];
     // With fewer tasks than CTAs only the first W CTAs work, one task each; every working
     // CTA then owns at least one task, so the CTAs that cut a unit are exactly c0..c1.
-    const int G = (int)(W < (long long)gridDim.x ? W : (long long)gridDim.x);
+    int G = (int)(W < (long long)gridDim.x ? W : (long long)gridDim.x);
+    if (flag[30] > 0) G = flag[30];                        // whole units per CTA (see above)
     if (c >= G) return;                                    // uniform over the CTA
     const long long s = task_start(c, W, G), e = task_start(c + 1, W, G);
 
@@ -569,145 +613,25 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
     };
     const int qbytes = group * D * 2;
     const int qslot_bytes = align_up(qbytes, 128);
-    auto issue_q = [&](const Unit &u, int k) {            // thread 0 only
-        const uint32_t bar = qbar0 + 8 * (k & 1);
-        dev::fence_proxy_async_smem();
-        dev::mbar_arrive_expect_tx(bar, qbytes);
-        dev::bulk_g2s(dev::smem_u32(smem + lay.q + (k & 1) * qslot_bytes),
-                      p.q + ((size_t)u.b * p.Hq + (size_t)u.h * group) * D, qbytes, bar);
-    };
-
-    // ---- 3. per-warp producer: tasks r_i = s + warp + NW*i, copies issued NS ahead
-    const int n_mine = (int)max(0LL, (e - s - warp + NW - 1) / NW);
-    // tile index (phys * Hkv + h, or -1 if the table entry is invalid) of warp task i, for a
-    // chunk of 32 tasks: lane j holds task chunk*32 + j
-    // and, when appending, b*16 + the new token's offset if task i is its unit's last block
-    auto load_tiles = [&](int chunk, int &app) {
-        const int i = chunk * 32 + lane;
-        int t = -1;
-        app = -1;
-        if (i < n_mine) {
-            const long long r = s + warp + (long long)NW * i;
-            const Unit u = unit_of(r);
-            const int blk = (int)(r - u.U0);
-            const int id = __ldg(p.block_tables + (size_t)u.b * p.MB + blk);
-            if (id >= 0 && id < p.num_blocks) t = id * Hkv + u.h;
-            else dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-            if (p.k_new && blk == u.nb - 1 && t >= 0) app = u.b * BS + (u.L - 1) % BS;
-        }
-        return t;
-    };
-    int acur, anext;
-    int tcur = load_tiles(0, acur), tnext = load_tiles(1, anext);
-    auto issue = [&](int i) {                              // warp-collective
-        if ((i & 31) == 0 && i > 0) {
-            tcur = tnext;
-            acur = anext;
-            tnext = load_tiles((i >> 5) + 1, anext);
-        }
-        const int t = __shfl_sync(dev::FULL, tcur, i & 31);
-        const int a = __shfl_sync(dev::FULL, acur, i & 31);
-        if (a >= 0) {
-            // this block holds the new token: write its K/V row into the slot first, then
-            // order those generic writes before the bulk copy that reads the block
-            const int b = a / BS, off = a % BS, h = t % Hkv;
-            const size_t src = ((size_t)b * Hkv + h) * D;
-            const size_t dst = ((size_t)t * BS + off) * D;               // element index
-            constexpr int EPL = D / 32;
-            if constexpr (FP8) {
-                const uint16_t *ks = p.k_new + src + lane * EPL;
-                const uint16_t *vs = p.v_new + src + lane * EPL;
-                uint32_t kc = 0, vc = 0;
-#pragma unroll
-                for (int e = 0; e < EPL; e += 2) {
-                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(ks + e);
-                    const uint32_t vw = *reinterpret_cast<const uint32_t *>(vs + e);
-                    kc |= dev::e4m3x2_satfinite(dev::bf16_lo(kw) * p.inv_k_scale, dev::bf16_hi(kw) * p.inv_k_scale) << (8 * e);
-                    vc |= dev::e4m3x2_satfinite(dev::bf16_lo(vw) * p.inv_v_scale, dev::bf16_hi(vw) * p.inv_v_scale) << (8 * e);
-                }
-                uint8_t *kd = const_cast<uint8_t *>(p.key_cache) + dst + lane * EPL;
-                uint8_t *vd = const_cast<uint8_t *>(p.value_cache) + dst + lane * EPL;
-                if constexpr (EPL == 4) {
-                    *reinterpret_cast<uint32_t *>(kd) = kc;
-                    *reinterpret_cast<uint32_t *>(vd) = vc;
-                } else {
-                    *reinterpret_cast<uint16_t *>(kd) = (uint16_t)kc;
-                    *reinterpret_cast<uint16_t *>(vd) = (uint16_t)vc;
-                }
-            } else {
-                uint16_t *kd = reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(p.key_cache)) + dst + lane * EPL;
-                uint16_t *vd = reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(p.value_cache)) + dst + lane * EPL;
-                if constexpr (EPL == 4) {
-                    *reinterpret_cast<uint2 *>(kd) = *reinterpret_cast<const uint2 *>(p.k_new + src + lane * EPL);
-                    *reinterpret_cast<uint2 *>(vd) = *reinterpret_cast<const uint2 *>(p.v_new + src + lane * EPL);
-                } else {
-                    *reinterpret_cast<uint32_t *>(kd) = *reinterpret_cast<const uint32_t *>(p.k_new + src + lane * EPL);
-                    *reinterpret_cast<uint32_t *>(vd) = *reinterpret_cast<const uint32_t *>(p.v_new + src + lane * EPL);
-                }
-            }
-            dev::fence_proxy_async_global();
-            __syncwarp();
-        }
-        if (lane == 0) {
-            const int st = i % NS;
-            const uint32_t bar = dev::smem_u32(bars + warp * NS + st);
-            uint8_t *stage = smem + lay.stage + (warp * NS + st) * 2 * TILE;
-            stage_tile[warp * NS + st] = t;
-            if (t >= 0) {
-                const size_t off = (size_t)t * TILE;
-                dev::fence_proxy_async_smem();
-                dev::mbar_arrive_expect_tx(bar, 2 * TILE);
-                dev::bulk_g2s(dev::smem_u32(stage), p.key_cache + off, TILE, bar);
-                dev::bulk_g2s(dev::smem_u32(stage + TILE), p.value_cache + off, TILE, bar);
-            } else {
-                dev::mbar_arrive(bar);                    // nothing to copy; block is masked
-            }
-        }
-    };
-    int ip = 0;
-    for (; ip < NS && ip < n_mine; ++ip) issue(ip);
-    if (tid == 0) issue_q(unit_of(s), 0);
-
-    // ---- 4. segments
-    float *ml_all = reinterpret_cast<float *>(smem + lay.ml);
-    float *acc_all = reinterpret_cast<float *>(smem + lay.acc);
+    float *ml_base = reinterpret_cast<float *>(smem + lay.ml);
+    float *acc_base = reinterpret_cast<float *>(smem + lay.acc);
     const int rowstride = D + ACC_PAD;
-    bool aborted = false;
-    int ic = 0;
-    int k = 0;
-    for (long long seg_lo = s; seg_lo < e; ++k) {
-        const Unit u = unit_of(seg_lo);
+
+    // The epilogue of segment k: merge the NW streaming warps' states (merge slot k&1), then
+    // write the output of a whole unit, or this CTA's partial followed by the hand-off (the
+    // last CTA of the unit to arrive merges every partial, in CTA order, and resets the
+    // counter).  Run by the epilogue warp alone for all but the CTA's last segment, which
+    // every warp handles together once streaming is over.
+    auto seg_epilogue = [&](const Unit &u, long long seg_lo, long long seg_hi, int k, bool team_cta) {
         const long long U1 = u.U0 + u.nb;
-        const long long seg_hi = U1 < e ? U1 : e;
-        if (tid == 0 && seg_hi < e) issue_q(unit_of(seg_hi), k + 1);
-        const bool qok = __all_sync(dev::FULL, dev::mbar_wait_bounded(qbar0 + 8 * (k & 1), (uint32_t)((k >> 1) & 1)));
-        aborted |= !qok;
-        cmp.start(reinterpret_cast<const uint16_t *>(smem + lay.q + (k & 1) * qslot_bytes), group, lane);
-        while (!aborted && ic < n_mine && s + warp + (long long)NW * ic < seg_hi) {
-            const int st = ic % NS;
-            const uint32_t bar = dev::smem_u32(bars + warp * NS + st);
-            if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(bar, (uint32_t)((ic / NS) & 1)))) {
-                aborted = true;
-                break;
-            }
-            const long long r = s + warp + (long long)NW * ic;
-            const int blk = (int)(r - u.U0);
-            const int ntok = stage_tile[warp * NS + st] >= 0 ? min(BS, u.L - blk * BS) : 0;
-            if (ntok > 0) {
-                const uint8_t *stage = smem + lay.stage + (warp * NS + st) * 2 * TILE;
-                cmp.block(stage, stage + TILE, ntok, p.score_scale, lane);
-            }
-            __syncwarp();
-            if (ip < n_mine) issue(ip++);
-            ++ic;
-        }
-        // merge the warps' states for this segment
-        cmp.dump(ml_all + warp * 32, acc_all + warp * group * rowstride, group, lane);
-        __syncthreads();
+        const int tt = team_cta ? tid : lane, tn = team_cta ? NTHR : 32;
+        const int twarp = team_cta ? warp : 0, tnw = team_cta ? NW + 1 : 1;
+        const float *ml_all = ml_base + (k & 1) * (lay.ml_slot / 4);
+        const float *acc_all = acc_base + (k & 1) * (lay.acc_slot / 4);
         const bool whole = seg_lo == u.U0 && seg_hi == U1;
         const int slot = k == 0 ? 0 : 1;
         const size_t prow = ((size_t)c * 2 + slot) * group;        // partial rows of this CTA
-        for (int x = tid; x < group * D; x += NTHR) {
+        for (int x = tt; x < group * D; x += tn) {
             const int row = x / D, d = x - row * D;
             const int sd = Compute::slot_of_d(d);
             float M = -INFINITY;
@@ -736,67 +660,281 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
                 }
             }
         }
-        if (!whole) {
-            // hand-off: the last CTA of this unit to arrive merges every CTA's partial
-            __threadfence();
+        if (whole) return;
+        // hand-off.  The team barrier orders every partial store before the release-acquire
+        // add of the team's first thread; the merge's loads follow that add through the next
+        // team barrier.
+        const int c0 = cta_of(u.U0, W, G), c1 = cta_of(U1 - 1, W, G);
+        int *counter = p.counters + (size_t)u.b * Hkv + u.h;
+        int last;
+        if (team_cta) {
             __syncthreads();
-            const int c0 = cta_of(u.U0, W, G), c1 = cta_of(U1 - 1, W, G);
-            if (tid == 0) {
-                const int old = atomicAdd(p.counters + (size_t)u.b * Hkv + u.h, 1);
-                flag[0] = old == c1 - c0;
-            }
+            if (tid == 0) flag[31] = dev::atomic_add_acq_rel_gpu(counter, 1) == c1 - c0;
             __syncthreads();
-            if (flag[0]) {
-                __threadfence();
-                const bool c0_shared = task_start(c0, W, G) < u.U0;   // unit is c0's 2nd+ segment
-                for (int x = tid; x < group * D; x += NTHR) {
-                    const int row = x / D, d = x - row * D;
-                    float M = -INFINITY;
-                    for (int cc = c0; cc <= c1; ++cc) {
+            last = flag[31];
+        } else {
+            __syncwarp();
+            last = 0;
+            if (lane == 0) last = dev::atomic_add_acq_rel_gpu(counter, 1) == c1 - c0;
+            last = __shfl_sync(dev::FULL, last, 0);
+            __syncwarp();
+        }
+        if (!last) return;
+        // merge: a warp per output row, lanes own D/32 columns; an online merge over the
+        // partials in CTA order, four partials' loads in flight at a time
+        const bool c0_shared = task_start(c0, W, G) < u.U0;          // unit is c0's 2nd+ segment
+        constexpr int DPL = D / 32;
+        for (int row = twarp; row < group; row += tnw) {
+            float Mr = -INFINITY, den = 0.f, num[DPL];
+#pragma unroll
+            for (int x = 0; x < DPL; ++x) num[x] = 0.f;
+            for (int cb = c0; cb <= c1; cb += 4) {
+                float2 ml[4];
+                float oc[4][DPL];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int cc = cb + j;
+                    ml[j].x = -INFINITY;
+                    ml[j].y = 0.f;
+#pragma unroll
+                    for (int x = 0; x < DPL; ++x) oc[j][x] = 0.f;
+                    if (cc <= c1) {
                         const int sl = (cc == c0 && c0_shared) ? 1 : 0;
-                        M = fmaxf(M, __ldcg(p.part_ml + (((size_t)cc * 2 + sl) * group + row) * 2));
-                    }
-                    float num = 0.f, den = 0.f;
-                    if (M != -INFINITY) {
-                        for (int cc = c0; cc <= c1; ++cc) {
-                            const int sl = (cc == c0 && c0_shared) ? 1 : 0;
-                            const size_t pr = ((size_t)cc * 2 + sl) * group + row;
-                            const float mc = __ldcg(p.part_ml + pr * 2);
-                            const float wt = mc == -INFINITY ? 0.f : dev::fast_exp2(mc - M);
-                            num += wt * __ldcg(p.part_o + pr * D + d);
-                            den += wt * __ldcg(p.part_ml + pr * 2 + 1);
+                        const size_t pr = ((size_t)cc * 2 + sl) * group + row;
+                        ml[j] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pr * 2));
+                        if constexpr (DPL == 4) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + pr * D) + lane);
+                            oc[j][0] = v.x; oc[j][1] = v.y; oc[j][2] = v.z; oc[j][3] = v.w;
+                        } else {
+                            const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.part_o + pr * D) + lane);
+                            oc[j][0] = v.x; oc[j][1] = v.y;
                         }
                     }
-                    const float o = den > 0.f ? num / den : 0.f;
-                    const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-                    p.out[((size_t)u.b * p.Hq + (size_t)u.h * group + row) * D + d] =
-                        *reinterpret_cast<const uint16_t *>(&ob);
                 }
-                if (tid == 0) atomicExch(p.counters + (size_t)u.b * Hkv + u.h, 0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (ml[j].x == -INFINITY) continue;
+                    const float Mn = fmaxf(Mr, ml[j].x);
+                    const float a = Mr == -INFINITY ? 0.f : dev::fast_exp2(Mr - Mn);
+                    const float bw = dev::fast_exp2(ml[j].x - Mn);
+                    den = den * a + ml[j].y * bw;
+#pragma unroll
+                    for (int x = 0; x < DPL; ++x) num[x] = num[x] * a + oc[j][x] * bw;
+                    Mr = Mn;
+                }
+            }
+            uint16_t *dst = p.out + ((size_t)u.b * p.Hq + (size_t)u.h * group + row) * D + lane * DPL;
+#pragma unroll
+            for (int x = 0; x < DPL; ++x) {
+                const __nv_bfloat16 ob = __float2bfloat16_rn(den > 0.f ? num[x] / den : 0.f);
+                dst[x] = *reinterpret_cast<const uint16_t *>(&ob);
             }
         }
-        __syncthreads();                                  // merge area and q slot reusable
-        seg_lo = seg_hi;
+        if (tt == 0) atomicExch(counter, 0);
+    };
+
+    if (warp == NW) {
+        // ================= epilogue warp: q staging and every segment but the last ========
+        auto issue_q = [&](long long seg_start, int k) {        // lane 0 only
+            const Unit u = unit_of(seg_start);
+            const uint32_t bar = qbar0 + 8 * (k & 1);
+            dev::fence_proxy_async_smem();
+            dev::mbar_arrive_expect_tx(bar, qbytes);
+            dev::bulk_g2s(dev::smem_u32(smem + lay.q + (k & 1) * qslot_bytes),
+                          p.q + ((size_t)u.b * p.Hq + (size_t)u.h * group) * D, qbytes, bar);
+        };
+        long long nxt = s;                                        // first two segments' q rows
+        for (int k = 0; k < 2 && nxt < e; ++k) {
+            const Unit u = unit_of(nxt);
+            if (lane == 0) issue_q(nxt, k);
+            nxt = min(e, u.U0 + (long long)u.nb);
+        }
+        long long seg_lo = s;
+        for (int k = 0; seg_lo < e; ++k) {
+            const Unit u = unit_of(seg_lo);
+            const long long seg_hi = min(e, u.U0 + (long long)u.nb);
+            if (seg_hi == e) break;                               // the last segment: below
+            if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(done0 + 8 * (k & 1), (uint32_t)((k >> 1) & 1)))) {
+                if (lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+                break;
+            }
+            // every streaming warp has dumped segment k, so none reads q slot k&1 again
+            // before segment k+2: stage that segment's q rows into it
+            {
+                const Unit u1 = unit_of(seg_hi);
+                const long long h1 = min(e, u1.U0 + (long long)u1.nb);
+                if (h1 < e && lane == 0) issue_q(h1, k + 2);
+            }
+            seg_epilogue(u, seg_lo, seg_hi, k, false);
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(free0 + 8 * (k & 1)); // merge slot k&1 reusable
+            seg_lo = seg_hi;
+        }
+    } else {
+        // ================= streaming warps ==================================================
+        // ---- 3. per-warp producer: tasks r_i = s + warp + NW*i, copies issued NS ahead
+        const int n_mine = (int)max(0LL, (e - s - warp + NW - 1) / NW);
+        // tile index (phys * Hkv + h, or -1 if the table entry is invalid) of warp task i, for a
+        // chunk of 32 tasks: lane j holds task chunk*32 + j
+        // and, when appending, b*16 + the new token's offset if task i is its unit's last block
+        auto load_tiles = [&](int chunk, int &app) {
+            const int i = chunk * 32 + lane;
+            int t = -1;
+            app = -1;
+            if (i < n_mine) {
+                const long long r = s + warp + (long long)NW * i;
+                const Unit u = unit_of(r);
+                const int blk = (int)(r - u.U0);
+                const int id = __ldg(p.block_tables + (size_t)u.b * p.MB + blk);
+                if (id >= 0 && id < p.num_blocks) t = id * Hkv + u.h;
+                else dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+                if (p.k_new && blk == u.nb - 1 && t >= 0) app = u.b * BS + (u.L - 1) % BS;
+            }
+            return t;
+        };
+        int acur, anext;
+        int tcur = load_tiles(0, acur), tnext = load_tiles(1, anext);
+        auto issue = [&](int i) {                              // warp-collective
+            if ((i & 31) == 0 && i > 0) {
+                tcur = tnext;
+                acur = anext;
+                tnext = load_tiles((i >> 5) + 1, anext);
+            }
+            const int t = __shfl_sync(dev::FULL, tcur, i & 31);
+            const int a = __shfl_sync(dev::FULL, acur, i & 31);
+            if (a >= 0) {
+                // this block holds the new token: write its K/V row into the slot first, then
+                // order those generic writes before the bulk copy that reads the block
+                const int b = a / BS, off = a % BS, h = t % Hkv;
+                const size_t src = ((size_t)b * Hkv + h) * D;
+                const size_t dst = ((size_t)t * BS + off) * D;               // element index
+                constexpr int EPL = D / 32;
+                if constexpr (FP8) {
+                    const uint16_t *ks = p.k_new + src + lane * EPL;
+                    const uint16_t *vs = p.v_new + src + lane * EPL;
+                    uint32_t kc = 0, vc = 0;
+    #pragma unroll
+                    for (int e = 0; e < EPL; e += 2) {
+                        const uint32_t kw = *reinterpret_cast<const uint32_t *>(ks + e);
+                        const uint32_t vw = *reinterpret_cast<const uint32_t *>(vs + e);
+                        kc |= dev::e4m3x2_satfinite(dev::bf16_lo(kw) * p.inv_k_scale, dev::bf16_hi(kw) * p.inv_k_scale) << (8 * e);
+                        vc |= dev::e4m3x2_satfinite(dev::bf16_lo(vw) * p.inv_v_scale, dev::bf16_hi(vw) * p.inv_v_scale) << (8 * e);
+                    }
+                    uint8_t *kd = const_cast<uint8_t *>(p.key_cache) + dst + lane * EPL;
+                    uint8_t *vd = const_cast<uint8_t *>(p.value_cache) + dst + lane * EPL;
+                    if constexpr (EPL == 4) {
+                        *reinterpret_cast<uint32_t *>(kd) = kc;
+                        *reinterpret_cast<uint32_t *>(vd) = vc;
+                    } else {
+                        *reinterpret_cast<uint16_t *>(kd) = (uint16_t)kc;
+                        *reinterpret_cast<uint16_t *>(vd) = (uint16_t)vc;
+                    }
+                } else {
+                    uint16_t *kd = reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(p.key_cache)) + dst + lane * EPL;
+                    uint16_t *vd = reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(p.value_cache)) + dst + lane * EPL;
+                    if constexpr (EPL == 4) {
+                        *reinterpret_cast<uint2 *>(kd) = *reinterpret_cast<const uint2 *>(p.k_new + src + lane * EPL);
+                        *reinterpret_cast<uint2 *>(vd) = *reinterpret_cast<const uint2 *>(p.v_new + src + lane * EPL);
+                    } else {
+                        *reinterpret_cast<uint32_t *>(kd) = *reinterpret_cast<const uint32_t *>(p.k_new + src + lane * EPL);
+                        *reinterpret_cast<uint32_t *>(vd) = *reinterpret_cast<const uint32_t *>(p.v_new + src + lane * EPL);
+                    }
+                }
+                dev::fence_proxy_async_global();
+                __syncwarp();
+            }
+            if (lane == 0) {
+                const int st = i % NS;
+                const uint32_t bar = dev::smem_u32(bars + warp * NS + st);
+                uint8_t *stage = smem + lay.stage + (warp * NS + st) * 2 * TILE;
+                stage_tile[warp * NS + st] = t;
+                if (t >= 0) {
+                    const size_t off = (size_t)t * TILE;
+                    dev::fence_proxy_async_smem();
+                    dev::mbar_arrive_expect_tx(bar, 2 * TILE);
+                    dev::bulk_g2s(dev::smem_u32(stage), p.key_cache + off, TILE, bar);
+                    dev::bulk_g2s(dev::smem_u32(stage + TILE), p.value_cache + off, TILE, bar);
+                } else {
+                    dev::mbar_arrive(bar);                    // nothing to copy; block is masked
+                }
+            }
+        };
+        int ip = 0;
+        for (; ip < NS && ip < n_mine; ++ip) issue(ip);
+
+
+        // ---- 4. segments
+        bool aborted = false;
+        int ic = 0;
+        int k = 0;
+        for (long long seg_lo = s; seg_lo < e; ++k) {
+            const Unit u = unit_of(seg_lo);
+            const long long seg_hi = min(e, u.U0 + (long long)u.nb);
+            const bool qok = __all_sync(dev::FULL, dev::mbar_wait_bounded(qbar0 + 8 * (k & 1), (uint32_t)((k >> 1) & 1)));
+            aborted |= !qok;
+            cmp.start(reinterpret_cast<const uint16_t *>(smem + lay.q + (k & 1) * qslot_bytes), group, lane);
+            while (!aborted && ic < n_mine && s + warp + (long long)NW * ic < seg_hi) {
+                const int st = ic % NS;
+                const uint32_t bar = dev::smem_u32(bars + warp * NS + st);
+                if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(bar, (uint32_t)((ic / NS) & 1)))) {
+                    aborted = true;
+                    break;
+                }
+                const long long r = s + warp + (long long)NW * ic;
+                const int blk = (int)(r - u.U0);
+                const int ntok = stage_tile[warp * NS + st] >= 0 ? min(BS, u.L - blk * BS) : 0;
+                if (ntok > 0) {
+                    const uint8_t *stage = smem + lay.stage + (warp * NS + st) * 2 * TILE;
+                    cmp.block(stage, stage + TILE, ntok, p.score_scale, lane);
+                }
+                __syncwarp();
+                if (ip < n_mine) issue(ip++);
+                ++ic;
+            }
+            // hand this segment's state to the epilogue (merge slot k&1, free once the
+            // epilogue warp has merged segment k-2 out of it)
+            if (k >= 2 && !__all_sync(dev::FULL, dev::mbar_wait_bounded(free0 + 8 * (k & 1), (uint32_t)(((k >> 1) - 1) & 1))))
+                aborted = true;
+            cmp.dump(ml_base + (k & 1) * (lay.ml_slot / 4) + warp * 32,
+                     acc_base + (k & 1) * (lay.acc_slot / 4) + warp * group * rowstride, group, lane);
+            if (seg_hi < e) dev::mbar_arrive(done0 + 8 * (k & 1));
+            seg_lo = seg_hi;
+        }
+        if (aborted) {
+            // A wait gave up: report it, then give the copies still in flight one more
+            // bounded wait so that none lands after this CTA has left.
+            if (lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+            for (int i = ic; i < ip; ++i)
+                (void)dev::mbar_wait_bounded(dev::smem_u32(bars + warp * NS + i % NS), (uint32_t)((i / NS) & 1));
+        }
     }
-    if (aborted) {
-        // A wait gave up: report it, then give the copies still in flight one more bounded
-        // wait so that none lands after this CTA has left.
-        if (lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
-        for (int i = ic; i < ip; ++i)
-            (void)dev::mbar_wait_bounded(dev::smem_u32(bars + warp * NS + i % NS), (uint32_t)((i / NS) & 1));
+
+    // ---- 5. the CTA's last segment, by every warp together
+    __syncthreads();
+    {
+        long long seg_lo = s;
+        int k = 0;
+        Unit u = unit_of(seg_lo);
+        while (min(e, u.U0 + (long long)u.nb) < e) {
+            seg_lo = u.U0 + u.nb;
+            u = unit_of(seg_lo);
+            ++k;
+        }
+        seg_epilogue(u, seg_lo, e, k, true);
     }
 }
 
-// Register budget for 8 resident warps per SM (the shared-memory ring allows no more).
+// Register budget for two CTAs of NW + 1 warps per SM (the shared-memory ring allows no
+// more with NW = 4).
 template <int D, bool FP8, int NW, int NS, bool G16>
-__global__ void __launch_bounds__(NW * 32, 8 / NW) decode_mma_kernel(const DecodeParams p)
+__global__ void __launch_bounds__((NW + 1) * 32, 8 / NW) decode_mma_kernel(const DecodeParams p)
 {
     MmaCompute<D, FP8, G16> cmp;
     decode_body<D, FP8, NW, NS>(p, cmp);
 }
 
 template <int D, bool FP8, int NW, int NS, int GP>
-__global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const DecodeParams p)
+__global__ void __launch_bounds__((NW + 1) * 32) decode_simt_kernel(const DecodeParams p)
 {
     SimtCompute<D, FP8, GP> cmp;
     cmp.sscale = p.score_scale;
@@ -863,7 +1001,7 @@ template <int D, bool FP8, int NW, int NS>
 cudaError_t run_decode(const Plan &pl, int group, bool launch, int *per_sm, cudaStream_t s,
                        const DecodeParams *p)
 {
-    const int threads = NW * 32;
+    const int threads = (NW + 1) * 32;                   // + the epilogue warp
     auto go = [&](auto kernel) -> cudaError_t {
         cudaError_t e = prepare(kernel, pl.smem, threads, launch ? nullptr : per_sm);
         if (e != cudaSuccess || !launch) return e;

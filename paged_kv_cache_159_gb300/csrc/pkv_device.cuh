@@ -166,6 +166,16 @@ __device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
+// Device-scope atomic add with acquire-release semantics: the caller's (and, through a
+// preceding barrier, its CTA's) earlier writes are visible before the add, and writes that
+// other threads released before their adds are visible after it.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *ptr, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void flag_error(uint32_t *err, uint32_t bits)
 {
     if (err) atomicOr(err, bits);
