@@ -151,8 +151,11 @@ def run_ours(args, world, rank, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = workloads.WORKLOADS[args.workload]
+    nl = w.layers
+    if nl > 1 and w.kv_dtype == "fp8":
+        raise SystemExit("layered workloads are bf16")
     d = workloads.draw(w, dev)
-    B, Hq, D = d.q.shape
+    B, Hq, D = d.q.shape[-3:]
     Hkv = w.num_kv_heads
     elem = 1 if w.kv_dtype == "fp8" else 2
 
@@ -163,7 +166,7 @@ def run_ours(args, world, rank, local_rank):
         k_scale = float(np.float32(kc.float().abs().max().item()) / np.float32(448.0))
         v_scale = float(np.float32(vc.float().abs().max().item()) / np.float32(448.0))
     pool = pkv.Pool(d.num_blocks, Hkv, D, pkv.KV_FP8E4M3 if w.kv_dtype == "fp8" else pkv.KV_BF16,
-                    k_scale, v_scale, d.free_order)
+                    k_scale, v_scale, d.free_order, num_layers=nl)
     pool.attach_device(local_rank)
     prefix = pool.alloc(w.prefix_blocks) if w.prefix_blocks else None
     tables = pool.build_block_tables(d.seq_lens, d.max_blocks, prefix)
@@ -189,14 +192,33 @@ def run_ours(args, world, rank, local_rank):
 
     launches_per_step = (1 if w.append and args.separate_append else 0) + 1
     # algorithmic bytes (no credit for tail-slot over-read; shared prefix blocks counted
-    # once per reader here, i.e. logical bytes)
-    kv_read = int(d.seq_lens.astype(np.int64).sum()) * Hkv * D * elem * 2
-    decode_bytes = kv_read + 2 * B * Hq * D * 2 + B * d.max_blocks * 4 + B * 4
-    append_bytes = (2 * B * Hkv * D * (2 + elem) + (B * 8 if args.separate_append else 0)) if w.append else 0
+    # once per reader here, i.e. logical bytes); every layer reads its own K/V, queries and
+    # outputs, and all layers share one read of the tables
+    kv_read = nl * int(d.seq_lens.astype(np.int64).sum()) * Hkv * D * elem * 2
+    decode_bytes = kv_read + nl * 2 * B * Hq * D * 2 + B * d.max_blocks * 4 + B * 4
+    new_rows = nl * 2 * B * Hkv * D * (2 + elem)              # read k/v_new, write the rows
+    append_bytes = (new_rows + (B * 8 if args.separate_append else 0)) if w.append else 0
     step_bytes = decode_bytes + append_bytes
     # bytes of the timed decode launch: with decode_step it also reads k_new/v_new and writes
     # the new rows
-    launch_bytes = decode_bytes + (2 * B * Hkv * D * (2 + elem) if w.append and not args.separate_append else 0)
+    launch_bytes = decode_bytes + (new_rows if w.append and not args.separate_append else 0)
+
+    def append_call(stream=None):
+        if nl > 1:
+            pkv.kv_append_layers(pool, d.k_new, d.v_new, sm, kc, vc, stream=stream)
+        else:
+            pkv.kv_append(pool, d.k_new, d.v_new, sm, kc, vc, stream=stream)
+
+    def decode_call(fused: bool, stream=None):
+        if nl > 1:
+            pkv.decode_step_layers(pool, d.q, d.k_new if fused else None, d.v_new if fused else None,
+                                   kc, vc, bt, sl, w.scale, out, ws, opts=decode_opts, stream=stream)
+        elif fused:
+            pkv.decode_step(pool, d.q, d.k_new, d.v_new, kc, vc, bt, sl, w.scale, out, ws,
+                            opts=decode_opts, stream=stream)
+        else:
+            pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws, opts=decode_opts,
+                                       stream=stream)
 
     # same-process bandwidth denominator: the library's copy probe over 2 x 1 GiB
     src = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
@@ -234,14 +256,9 @@ def run_ours(args, world, rank, local_rank):
         flush_l2()                                # L2 flush (read), outside the timed interval
         starts[i].record(stream)
         if w.append and args.separate_append:
-            pkv.kv_append(pool, d.k_new, d.v_new, sm, kc, vc, stream=stream)
+            append_call(stream)
         mids[i].record(stream)
-        if w.append and not args.separate_append:  # append + decode in one launch
-            pkv.decode_step(pool, d.q, d.k_new, d.v_new, kc, vc, bt, sl, w.scale, out, ws,
-                            opts=decode_opts, stream=stream)
-        else:
-            pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws, opts=decode_opts,
-                                       stream=stream)
+        decode_call(w.append and not args.separate_append, stream)   # fused: one launch
         ends[i].record(stream)
 
     with torch.cuda.stream(stream):
@@ -304,13 +321,12 @@ def run_ours(args, world, rank, local_rank):
             d.v_new.copy_(host["v"], non_blocking=True)
             if args.separate_append:
                 sm.copy_(sm_h, non_blocking=True)
-                pkv.kv_append(pool, d.k_new, d.v_new, sm, kc, vc)
-                pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws, opts=decode_opts)
+                append_call()
+                decode_call(False)
             else:
-                pkv.decode_step(pool, d.q, d.k_new, d.v_new, kc, vc, bt, sl, w.scale, out, ws,
-                                opts=decode_opts)
+                decode_call(True)
         else:
-            pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws, opts=decode_opts)
+            decode_call(False)
         host["out"].copy_(out, non_blocking=True)
         ee[1].record()
         ee[1].synchronize()
@@ -332,14 +348,14 @@ def run_ours(args, world, rank, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8e4m3-kv/bf16-q" if w.kv_dtype == "fp8" else "bf16", "data": "synthetic",
         "config": {
-            "workload": "%s: batch %d, q heads %d / kv heads %d, head_dim %d, block 16, "
-                        "seq_lens %s, kv %s" % (w.name, B, Hq, Hkv, D,
+            "workload": "%s: %sbatch %d, q heads %d / kv heads %d, head_dim %d, block 16, "
+                        "seq_lens %s, kv %s" % (w.name, "%d layers, " % nl if nl > 1 else "", B, Hq, Hkv, D,
                                                  "all %d" % d.seq_lens[0] if w.lengths == "fixed"
                                                  else "%s (sum %d)" % (w.lengths, int(d.seq_lens.sum())),
                                                  w.kv_dtype),
-            "step": ("kv_append + paged_attention_decode" if args.separate_append else
-                     "decode_step (append at L-1 + paged decode, one launch)") if w.append
-                    else "paged_attention_decode",
+            "step": (("kv_append + paged_attention_decode" if args.separate_append else
+                      "decode_step (append at L-1 + paged decode, one launch)") if w.append
+                     else "paged_attention_decode") + (", all %d layers per launch" % nl if nl > 1 else ""),
             "decode_opts": decode_opts,
             "l2": "flushed between steps (read of a 2x L2 buffer); inputs also exceed L2",
             "parallelism": "replicas",
@@ -350,8 +366,9 @@ def run_ours(args, world, rank, local_rank):
         "step_bytes": step_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_mma_kernel (%s)" % ("decode_step" if w.append and not args.separate_append
-                                                           else "paged_attention_decode"),
+                     "kernel": "decode_mma_kernel (%s%s)" % ("decode_step" if w.append and not args.separate_append
+                                                             else "paged_attention_decode",
+                                                             ", %d layers" % nl if nl > 1 else ""),
                      "bytes_per_launch": launch_bytes, "peak_source": peak_src + " hbm_gbs",
                      "same_run_copy_gbs": round(copy_gbs, 1)},
         "e2e": {"value": round(world * kv_read / e2e_step / 1e9, 1), "unit": "GB/s",
@@ -374,7 +391,7 @@ def _oracle_case(w, nseq):
     L = workloads.draw_seq_lens(w)[:nseq]
     sub = workloads.Workload(**{**w.__dict__, "batch": nseq, "lengths": "list",
                                 "len_list": tuple(int(x) for x in L), "pool": "exact",
-                                "prefix_blocks": 0})
+                                "prefix_blocks": 0, "layers": 1})
     d = workloads.draw(sub, "cpu")
     a = oracle.BlockAllocator(d.num_blocks, d.free_order)
     tables = oracle.build_block_tables(a, d.seq_lens, d.max_blocks)

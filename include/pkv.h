@@ -27,6 +27,10 @@
  *             groups of g = Hq / Hkv.
  *   [Quant]   same page, section "KV 量化": K/V stored in FP8 (1 byte) with higher-precision
  *             arithmetic.
+ *   [Bytes]   same page, section "KV Cache 有多大：一张显存账单": every layer keeps K and V
+ *             for every token, 2 * layers * kv_heads * head_dim * element-bytes per token;
+ *             "一个请求为什么越生成越占内存?" (learning-field-guides), capacity derivation:
+ *             the same count summed over layers, positions and sequences.
  */
 #ifndef PKV_H
 #define PKV_H
@@ -55,11 +59,17 @@ typedef enum {
 
 typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8E4M3 = 1 } pkv_kv_dtype;
 
-/* Shape and element type of one layer's paged K/V pool [Layout]: two caller-owned device
- * tensors key_cache and value_cache, each [num_blocks, num_kv_heads, block_size, head_dim],
- * contiguous, 16-byte aligned.  block_size must be 16 [Paged]; head_dim 64 or 128.
- * FP8 pools store OCP E4M3 codes of x / scale with one scale per tensor [Quant]; k_scale
- * and v_scale must be positive and finite (ignored for bf16). */
+/* Shape and element type of a paged K/V pool [Layout]: two caller-owned device tensors
+ * key_cache and value_cache, each [num_layers, num_blocks, num_kv_heads, block_size,
+ * head_dim], contiguous, 16-byte aligned.  block_size must be 16 [Paged]; head_dim 64 or
+ * 128.  A block id names the same block_size positions in every layer, so one block table
+ * per sequence serves all layers, and a token costs 2 * num_layers * num_kv_heads *
+ * head_dim * element-bytes of cache [Bytes].  The single-layer entry points take the base
+ * of one layer (cache + layer * pkv_pool_layer_bytes()); the *_layers entry points take the
+ * base of layer 0 and cover all layers in one launch.  num_layers 0 means 1; at most 4096,
+ * with num_layers * num_blocks * num_kv_heads < 2^31.  FP8 pools store OCP E4M3 codes of
+ * x / scale with one scale per tensor [Quant]; k_scale and v_scale must be positive and
+ * finite (ignored for bf16). */
 typedef struct {
     int32_t num_blocks;
     int32_t block_size;
@@ -68,6 +78,7 @@ typedef struct {
     int32_t kv_dtype;      /* pkv_kv_dtype */
     float k_scale;
     float v_scale;
+    int32_t num_layers;    /* layers stacked in each cache tensor (0 = 1) */
 } pkv_pool_desc;
 
 typedef struct pkv_pool pkv_pool;   /* host allocator state + the device error word */
@@ -81,8 +92,13 @@ int pkv_pool_create(const pkv_pool_desc *desc, const int32_t *free_order, pkv_po
 /* Free the pool, its allocator and (if attached) its device error word. */
 int pkv_pool_destroy(pkv_pool *pool);
 
-/* Copy the pool's descriptor to *out. */
+/* Copy the pool's descriptor to *out (num_layers >= 1). */
 int pkv_pool_get_desc(const pkv_pool *pool, pkv_pool_desc *out);
+
+/* Bytes of one layer of one cache tensor: num_blocks * num_kv_heads * block_size *
+ * head_dim * element-bytes [Layout][Bytes].  Each of key_cache and value_cache holds
+ * num_layers times this.  0 for a NULL pool. */
+size_t pkv_pool_layer_bytes(const pkv_pool *pool);
 
 /* Number of blocks currently free. */
 int pkv_pool_num_free(const pkv_pool *pool, int32_t *out);
@@ -139,6 +155,14 @@ int pkv_pool_attach_device(pkv_pool *pool, int device);
 int pkv_kv_append(pkv_pool *pool, const void *k, const void *v, const int64_t *slot_mapping,
                   int32_t num_tokens, void *key_cache, void *value_cache, void *stream);
 
+/* pkv_kv_append for every layer of the pool in one launch [Slot][Bytes]: k, v are device
+ * bf16 [num_layers, num_tokens, Hkv, D]; token t of layer l goes to slot slot_mapping[t] of
+ * layer l (the same slot in every layer, since blocks span all layers).  key_cache and
+ * value_cache are the whole stacked tensors.  Otherwise as pkv_kv_append. */
+int pkv_kv_append_layers(pkv_pool *pool, const void *k, const void *v,
+                         const int64_t *slot_mapping, int32_t num_tokens, void *key_cache,
+                         void *value_cache, void *stream);
+
 /* Tuning knobs for pkv_paged_attention_decode_ex; zero fields mean "choose". */
 typedef struct {
     int32_t grid_ctas;        /* CTAs of the persistent grid (0 = SM count x CTAs per SM) */
@@ -148,7 +172,8 @@ typedef struct {
 } pkv_decode_opts;
 
 /* Device workspace bytes the decode needs for this shape and these opts (0 if the shape or
- * opts are invalid).  Queries the current device. */
+ * opts are invalid), for any of the decode entry points on this pool: the counters cover
+ * all of the pool's layers.  Queries the current device. */
 size_t pkv_decode_workspace_bytes(const pkv_pool *pool, int32_t batch, int32_t num_q_heads,
                                   int32_t max_blocks, const pkv_decode_opts *opts);
 
@@ -199,6 +224,20 @@ int pkv_decode_step(pkv_pool *pool, const void *q, const void *k_new, const void
                     const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
                     float scale, void *out, void *workspace, size_t workspace_bytes,
                     const pkv_decode_opts *opts, void *stream);
+
+/* Decode every layer of the pool in one launch [Decode][Bytes]: the same computation as
+ * pkv_decode_step (k_new and v_new given) or pkv_paged_attention_decode_ex (both NULL),
+ * applied independently to each layer l of the stacked caches with layer l's queries and
+ * new rows.  Device pointers: q, out bf16 [num_layers, batch, num_q_heads, D]; k_new,
+ * v_new bf16 [num_layers, batch, Hkv, D] or both NULL; key_cache, value_cache the whole
+ * stacked tensors; one block_tables / seq_lens for all layers.  Every (layer, sequence,
+ * KV head) is a unit of the same persistent schedule, so one launch streams all layers.
+ * Workspace, opts and errors as pkv_decode_step. */
+int pkv_decode_step_layers(pkv_pool *pool, const void *q, const void *k_new, const void *v_new,
+                           void *key_cache, void *value_cache, const int32_t *block_tables,
+                           const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                           int32_t max_blocks, float scale, void *out, void *workspace,
+                           size_t workspace_bytes, const pkv_decode_opts *opts, void *stream);
 
 /* Bytes of the fixed device scratch behind pkv_paged_attention_decode_noalloc. */
 #define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -14,6 +14,8 @@ Names follow the C ABI without the ``pkv_`` prefix:
 * ``paged_attention_decode(pool, q, key_cache, value_cache, block_tables, seq_lens, scale,
   out, workspace=None, opts=None)``.
 * ``decode_step(...)`` -- append each new token at position L-1 and decode, one launch.
+* ``kv_append_layers``, ``decode_step_layers`` -- the same over every layer of a pool whose
+  caches stack ``num_layers`` layers (``Pool(..., num_layers=L)``), one launch each.
 * ``decode_workspace_bytes``, ``probe_copy``, ``device_sm_count``.
 """
 from __future__ import annotations
@@ -35,7 +37,8 @@ EXPORTED = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_get_desc", "pkv_pool_num_free",
     "pkv_pool_refcount", "pkv_pool_alloc", "pkv_pool_share", "pkv_pool_free",
     "pkv_build_block_tables", "pkv_slot_mapping", "pkv_slot_mapping_all",
-    "pkv_pool_attach_device", "pkv_kv_append",
+    "pkv_pool_attach_device", "pkv_kv_append", "pkv_pool_layer_bytes", "pkv_kv_append_layers",
+    "pkv_decode_step_layers",
     "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
     "pkv_paged_attention_decode_ex", "pkv_decode_step", "pkv_paged_attention_decode_noalloc",
     "pkv_get_device_error", "pkv_probe_copy",
@@ -53,7 +56,7 @@ class pool_desc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
-                ("v_scale", ctypes.c_float)]
+                ("v_scale", ctypes.c_float), ("num_layers", ctypes.c_int32)]
 
 
 class decode_opts(ctypes.Structure):
@@ -88,6 +91,8 @@ def lib():
             "pkv_slot_mapping_all": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P]),
             "pkv_pool_attach_device": (ctypes.c_int, [_P, ctypes.c_int]),
             "pkv_kv_append": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P]),
+            "pkv_kv_append_layers": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P]),
+            "pkv_pool_layer_bytes": (ctypes.c_size_t, [_P]),
             "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32, _I32, ctypes.POINTER(decode_opts)]),
             "pkv_paged_attention_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
                                                           ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
@@ -97,6 +102,9 @@ def lib():
             "pkv_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
                                                ctypes.c_float, _P, _P, ctypes.c_size_t,
                                                ctypes.POINTER(decode_opts), _P]),
+            "pkv_decode_step_layers": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
+                                                      ctypes.c_float, _P, _P, ctypes.c_size_t,
+                                                      ctypes.POINTER(decode_opts), _P]),
             "pkv_paged_attention_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32,
                                                                   _I32, ctypes.c_float, _P, _P]),
             "pkv_get_device_error": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -150,9 +158,10 @@ class Pool:
     """A paged K/V pool descriptor with its host block allocator (pkv_pool_*)."""
 
     def __init__(self, num_blocks, num_kv_heads, head_dim, kv_dtype=KV_BF16, k_scale=1.0,
-                 v_scale=1.0, free_order=None, block_size=BLOCK_SIZE):
+                 v_scale=1.0, free_order=None, block_size=BLOCK_SIZE, num_layers=1):
         self.desc = pool_desc(int(num_blocks), int(block_size), int(num_kv_heads),
-                              int(head_dim), int(kv_dtype), float(k_scale), float(v_scale))
+                              int(head_dim), int(kv_dtype), float(k_scale), float(v_scale),
+                              int(num_layers))
         h = ctypes.c_void_p()
         order = None
         if free_order is not None:
@@ -178,6 +187,15 @@ class Pool:
             self.close()
         except Exception:
             pass
+
+    def get_desc(self) -> pool_desc:
+        out = pool_desc()
+        _check(lib().pkv_pool_get_desc(self._h, ctypes.byref(out)), "pool_get_desc")
+        return out
+
+    def layer_bytes(self) -> int:
+        """Bytes of one layer of one cache tensor (pkv_pool_layer_bytes)."""
+        return int(lib().pkv_pool_layer_bytes(self._h))
 
     def num_free(self) -> int:
         n = _I32()
@@ -249,6 +267,16 @@ def kv_append(pool: Pool, k, v, slots, key_cache, value_cache, stream=None):
                                _stream_ptr(stream)), "kv_append")
 
 
+def kv_append_layers(pool: Pool, k, v, slots, key_cache, value_cache, stream=None):
+    """k, v: bf16 CUDA [layers, T, Hkv, D]; slots: int64 CUDA [T] (the same slot in every
+    layer); caches: the pool's stacked CUDA tensors [layers, NB, Hkv, 16, D]."""
+    _check(lib().pkv_kv_append_layers(pool.handle, _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                      _dev_ptr(slots, "slot_mapping"), int(slots.numel()),
+                                      _dev_ptr(key_cache, "key_cache"),
+                                      _dev_ptr(value_cache, "value_cache"), _stream_ptr(stream)),
+           "kv_append_layers")
+
+
 def _opts(opts):
     if opts is None:
         return None
@@ -295,6 +323,22 @@ def decode_step(pool: Pool, q, k_new, v_new, key_cache, value_cache, block_table
         int(block_tables.shape[1]), float(scale), _dev_ptr(out, "out"),
         _dev_ptr(workspace, "workspace"), int(ws_bytes), ctypes.byref(o) if o else None,
         _stream_ptr(stream)), "decode_step")
+
+
+def decode_step_layers(pool: Pool, q, k_new, v_new, key_cache, value_cache, block_tables,
+                       seq_lens, scale: float, out, workspace, opts=None, stream=None):
+    """Every layer of a stacked pool in one launch: q/out bf16 CUDA [layers, B, Hq, D];
+    k_new/v_new bf16 CUDA [layers, B, Hkv, D], or both None for attention only."""
+    _, B, Hq, _ = q.shape
+    o = _opts(opts)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pkv_decode_step_layers(
+        pool.handle, _dev_ptr(q, "q"), _dev_ptr(k_new, "k_new"), _dev_ptr(v_new, "v_new"),
+        _dev_ptr(key_cache, "key_cache"), _dev_ptr(value_cache, "value_cache"),
+        _dev_ptr(block_tables, "block_tables"), _dev_ptr(seq_lens, "seq_lens"), int(B), int(Hq),
+        int(block_tables.shape[1]), float(scale), _dev_ptr(out, "out"),
+        _dev_ptr(workspace, "workspace"), int(ws_bytes), ctypes.byref(o) if o else None,
+        _stream_ptr(stream)), "decode_step_layers")
 
 
 def paged_attention_decode_noalloc(pool: Pool, q, key_cache, value_cache, block_tables,

@@ -71,18 +71,19 @@ constexpr float RESCALE_TAU = 8.0f;       // raise the running max only beyond 2
 constexpr int ACC_PAD = 8;                // floats of padding per merge-area row
 
 struct DecodeParams {
-    const uint16_t *q;            // bf16 [B, Hq, D]
-    const uint8_t *key_cache;     // [NB, Hkv, 16, D] of bf16 or e4m3
+    const uint16_t *q;            // bf16 [layers, B, Hq, D]
+    const uint8_t *key_cache;     // [layers, NB, Hkv, 16, D] of bf16 or e4m3
     const uint8_t *value_cache;
-    const int32_t *block_tables;  // [B, MB]
+    const int32_t *block_tables;  // [B, MB], shared by all layers
     const int32_t *seq_lens;      // [B]
-    uint16_t *out;                // bf16 [B, Hq, D]
-    int32_t *counters;            // [B * Hkv] arrival counts of split units (kept at zero)
+    uint16_t *out;                // bf16 [layers, B, Hq, D]
+    int32_t *counters;            // [layers * B * Hkv] arrival counts of split units (kept at zero)
     float *part_o;                // [G][2][group][D]   unnormalised partial outputs
     float *part_ml;               // [G][2][group][2]   (running max in log2 units, sum)
     uint32_t *err;
-    const uint16_t *k_new;        // bf16 [B, Hkv, D]: appended at position L-1 (or null)
+    const uint16_t *k_new;        // bf16 [layers, B, Hkv, D]: appended at position L-1 (or null)
     const uint16_t *v_new;
+    int layers;                   // layers decoded by this launch (stacked layer-major)
     int B, Hq, Hkv, group, MB, num_blocks;
     float score_scale;            // scale * k_scale * log2(e)
     float out_scale;              // v_scale (1 for bf16 pools)
@@ -508,7 +509,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
             if (a1 > a0) dev::prefetch_l2(reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0));
         };
         slice(p.block_tables, (size_t)p.B * p.MB * 4);
-        slice(p.q, (size_t)p.B * p.Hq * D * 2);
+        slice(p.q, (size_t)p.layers * p.B * p.Hq * D * 2);
         for (int j = 0; j < 2; ++j) {
             dev::mbar_init(qbar0 + 8 * j, 1);
             dev::mbar_init(done0 + 8 * j, NW * 32);
@@ -532,7 +533,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
             const bool ok = L >= 1 && L <= p.MB * BS;
             if (!ok && c == 0) {
                 dev::flag_error(p.err, PKV_DEVERR_SEQ_LEN);
-                for (int e = 0; e < p.Hq * D; ++e) p.out[(size_t)b * p.Hq * D + e] = 0;
+                for (int l = 0; l < p.layers; ++l)
+                    for (int e = 0; e < p.Hq * D; ++e) p.out[((size_t)l * p.B + b) * p.Hq * D + e] = 0;
             }
             const int nb = ok ? (L + BS - 1) / BS : 0;    // an invalid length breaks uniformity
             run += Hkv * nb;
@@ -567,7 +569,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
                 glo = min(glo, wlo[w]);
                 ghi = max(ghi, whi[w]);
             }
-            const int units = p.B * Hkv, grid = (int)gridDim.x;
+            const int units = p.layers * p.B * Hkv, grid = (int)gridDim.x;
             int pick = 0;
             if (glo == ghi && glo > 0 && units >= grid) {
                 for (int g0 = grid; pick == 0 && 5 * g0 >= 4 * grid; g0 -= 32) {
@@ -591,7 +593,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
         if (tid == NTHR - 1) prefix[p.B] = base + incl;
         __syncthreads();
     }
-    const long long W = prefix[p.B];
+    const int W1 = prefix[p.B];                            // tasks of one layer
+    const long long W = (long long)W1 * p.layers;
     // With fewer tasks than CTAs only the first W CTAs work, one task each; every working
     // CTA then owns at least one task, so the CTAs that cut a unit are exactly c0..c1.
     int G = (int)(W < (long long)gridDim.x ? W : (long long)gridDim.x);
@@ -599,15 +602,20 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
     if (c >= G) return;                                    // uniform over the CTA
     const long long s = task_start(c, W, G), e = task_start(c + 1, W, G);
 
-    // Unit geometry of task r: sequence, head, first task of the unit, blocks in it.
-    struct Unit { int b, h, L, nb; long long U0; };
+    // Unit geometry of task r: layer, sequence, (layer, sequence) row lb = l * B + b, head,
+    // first task of the unit, blocks in it.  Layers are laid end to end, each with the same
+    // task layout.
+    struct Unit { int l, b, lb, h, L, nb; long long U0; };
     auto unit_of = [&](long long r) {
         Unit u;
-        u.b = find_seq(prefix, p.B, (int)r);
+        u.l = p.layers > 1 ? (int)(r / W1) : 0;
+        const int rl = (int)(r - (long long)u.l * W1);
+        u.b = find_seq(prefix, p.B, rl);
+        u.lb = u.l * p.B + u.b;
         const int tasks = prefix[u.b + 1] - prefix[u.b];
         u.nb = tasks / Hkv;
-        u.h = (int)(r - prefix[u.b]) / u.nb;
-        u.U0 = prefix[u.b] + (long long)u.h * u.nb;
+        u.h = (rl - prefix[u.b]) / u.nb;
+        u.U0 = (long long)u.l * W1 + prefix[u.b] + (long long)u.h * u.nb;
         u.L = lens[u.b];
         return u;
     };
@@ -650,7 +658,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
             if (whole) {
                 const float o = den > 0.f ? num / den * p.out_scale : 0.f;
                 const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-                p.out[((size_t)u.b * p.Hq + (size_t)u.h * group + row) * D + d] =
+                p.out[((size_t)u.lb * p.Hq + (size_t)u.h * group + row) * D + d] =
                     *reinterpret_cast<const uint16_t *>(&ob);
             } else {
                 p.part_o[(prow + row) * D + d] = num * p.out_scale;
@@ -665,7 +673,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
         // add of the team's first thread; the merge's loads follow that add through the next
         // team barrier.
         const int c0 = cta_of(u.U0, W, G), c1 = cta_of(U1 - 1, W, G);
-        int *counter = p.counters + (size_t)u.b * Hkv + u.h;
+        int *counter = p.counters + (size_t)u.lb * Hkv + u.h;
         int last;
         if (team_cta) {
             __syncthreads();
@@ -723,7 +731,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
                     Mr = Mn;
                 }
             }
-            uint16_t *dst = p.out + ((size_t)u.b * p.Hq + (size_t)u.h * group + row) * D + lane * DPL;
+            uint16_t *dst = p.out + ((size_t)u.lb * p.Hq + (size_t)u.h * group + row) * D + lane * DPL;
 #pragma unroll
             for (int x = 0; x < DPL; ++x) {
                 const __nv_bfloat16 ob = __float2bfloat16_rn(den > 0.f ? num[x] / den : 0.f);
@@ -741,7 +749,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
             dev::fence_proxy_async_smem();
             dev::mbar_arrive_expect_tx(bar, qbytes);
             dev::bulk_g2s(dev::smem_u32(smem + lay.q + (k & 1) * qslot_bytes),
-                          p.q + ((size_t)u.b * p.Hq + (size_t)u.h * group) * D, qbytes, bar);
+                          p.q + ((size_t)u.lb * p.Hq + (size_t)u.h * group) * D, qbytes, bar);
         };
         long long nxt = s;                                        // first two segments' q rows
         for (int k = 0; k < 2 && nxt < e; ++k) {
@@ -774,9 +782,10 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
         // ================= streaming warps ==================================================
         // ---- 3. per-warp producer: tasks r_i = s + warp + NW*i, copies issued NS ahead
         const int n_mine = (int)max(0LL, (e - s - warp + NW - 1) / NW);
-        // tile index (phys * Hkv + h, or -1 if the table entry is invalid) of warp task i, for a
-        // chunk of 32 tasks: lane j holds task chunk*32 + j
-        // and, when appending, b*16 + the new token's offset if task i is its unit's last block
+        // tile index ((layer * NB + phys) * Hkv + h, or -1 if the table entry is invalid) of
+        // warp task i, for a chunk of 32 tasks: lane j holds task chunk*32 + j; and, when
+        // appending, (layer * B + b) * 16 + the new token's offset if task i is its unit's last
+        // block
         auto load_tiles = [&](int chunk, int &app) {
             const int i = chunk * 32 + lane;
             int t = -1;
@@ -786,9 +795,9 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
                 const Unit u = unit_of(r);
                 const int blk = (int)(r - u.U0);
                 const int id = __ldg(p.block_tables + (size_t)u.b * p.MB + blk);
-                if (id >= 0 && id < p.num_blocks) t = id * Hkv + u.h;
+                if (id >= 0 && id < p.num_blocks) t = (u.l * p.num_blocks + id) * Hkv + u.h;
                 else dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-                if (p.k_new && blk == u.nb - 1 && t >= 0) app = u.b * BS + (u.L - 1) % BS;
+                if (p.k_new && blk == u.nb - 1 && t >= 0) app = u.lb * BS + (u.L - 1) % BS;
             }
             return t;
         };
@@ -805,8 +814,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
             if (a >= 0) {
                 // this block holds the new token: write its K/V row into the slot first, then
                 // order those generic writes before the bulk copy that reads the block
-                const int b = a / BS, off = a % BS, h = t % Hkv;
-                const size_t src = ((size_t)b * Hkv + h) * D;
+                const int lb = a / BS, off = a % BS, h = t % Hkv;
+                const size_t src = ((size_t)lb * Hkv + h) * D;
                 const size_t dst = ((size_t)t * BS + off) * D;               // element index
                 constexpr int EPL = D / 32;
                 if constexpr (FP8) {

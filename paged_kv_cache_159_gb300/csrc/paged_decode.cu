@@ -55,6 +55,7 @@ int make_plan(const pkv_pool_desc &d, int B, int Hq, int MB, const pkv_decode_op
     const int group = Hq / d.num_kv_heads;
     if (group > 16) return PKV_ERR_INVALID;
     if ((long long)B * MB * d.num_kv_heads >= (1LL << 31)) return PKV_ERR_INVALID;
+    if ((long long)d.num_layers * B * d.num_kv_heads >= (1LL << 31)) return PKV_ERR_INVALID;
     pkv_decode_opts z{};
     if (!o) o = &z;
     pl.variant = o->variant ? o->variant : 2;
@@ -78,7 +79,7 @@ int make_plan(const pkv_pool_desc &d, int B, int Hq, int MB, const pkv_decode_op
     }
     const size_t rows = (size_t)pl.grid * 2 * group;
     pl.ws_counters = 0;
-    pl.ws_o = ((size_t)B * d.num_kv_heads * 4 + 255) / 256 * 256;
+    pl.ws_o = ((size_t)d.num_layers * B * d.num_kv_heads * 4 + 255) / 256 * 256;   // counters
     pl.ws_ml = pl.ws_o + (rows * d.head_dim * 4 + 255) / 256 * 256;
     pl.ws_bytes = pl.ws_ml + (rows * 2 * 4 + 255) / 256 * 256;
     return PKV_OK;
@@ -103,7 +104,7 @@ namespace pkv {
 namespace decode {
 namespace {
 
-int decode_impl(pkv_pool *pool, const void *q, const void *k_new, const void *v_new,
+int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, const void *v_new,
                 const void *key_cache, const void *value_cache, const int32_t *block_tables,
                 const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
                 float scale, void *out, void *workspace, size_t workspace_bytes,
@@ -140,6 +141,7 @@ int decode_impl(pkv_pool *pool, const void *q, const void *k_new, const void *v_
     p.err = pool->d_err;
     p.k_new = static_cast<const uint16_t *>(k_new);
     p.v_new = static_cast<const uint16_t *>(v_new);
+    p.layers = layers;
     p.B = batch;
     p.Hq = num_q_heads;
     p.Hkv = d.num_kv_heads;
@@ -167,7 +169,7 @@ extern "C" int pkv_paged_attention_decode_ex(pkv_pool *pool, const void *q, cons
                                              void *out, void *workspace, size_t workspace_bytes,
                                              const pkv_decode_opts *opts, void *stream)
 {
-    return pkv::decode::decode_impl(pool, q, nullptr, nullptr, key_cache, value_cache, block_tables,
+    return pkv::decode::decode_impl(pool, 1, q, nullptr, nullptr, key_cache, value_cache, block_tables,
                                     seq_lens, batch, num_q_heads, max_blocks, scale, out, workspace,
                                     workspace_bytes, opts, stream);
 }
@@ -178,7 +180,7 @@ extern "C" int pkv_paged_attention_decode(pkv_pool *pool, const void *q, const v
                                           int32_t max_blocks, float scale, void *out, void *workspace,
                                           size_t workspace_bytes, void *stream)
 {
-    return pkv::decode::decode_impl(pool, q, nullptr, nullptr, key_cache, value_cache, block_tables,
+    return pkv::decode::decode_impl(pool, 1, q, nullptr, nullptr, key_cache, value_cache, block_tables,
                                     seq_lens, batch, num_q_heads, max_blocks, scale, out, workspace,
                                     workspace_bytes, nullptr, stream);
 }
@@ -190,7 +192,21 @@ extern "C" int pkv_decode_step(pkv_pool *pool, const void *q, const void *k_new,
                                size_t workspace_bytes, const pkv_decode_opts *opts, void *stream)
 {
     if (!k_new || !v_new) return PKV_ERR_INVALID;
-    return pkv::decode::decode_impl(pool, q, k_new, v_new, key_cache, value_cache, block_tables,
+    return pkv::decode::decode_impl(pool, 1, q, k_new, v_new, key_cache, value_cache, block_tables,
                                     seq_lens, batch, num_q_heads, max_blocks, scale, out, workspace,
                                     workspace_bytes, opts, stream);
+}
+
+extern "C" int pkv_decode_step_layers(pkv_pool *pool, const void *q, const void *k_new,
+                                      const void *v_new, void *key_cache, void *value_cache,
+                                      const int32_t *block_tables, const int32_t *seq_lens,
+                                      int32_t batch, int32_t num_q_heads, int32_t max_blocks,
+                                      float scale, void *out, void *workspace,
+                                      size_t workspace_bytes, const pkv_decode_opts *opts,
+                                      void *stream)
+{
+    if (!pool) return PKV_ERR_INVALID;
+    return pkv::decode::decode_impl(pool, pool->desc.num_layers, q, k_new, v_new, key_cache,
+                                    value_cache, block_tables, seq_lens, batch, num_q_heads,
+                                    max_blocks, scale, out, workspace, workspace_bytes, opts, stream);
 }

@@ -28,8 +28,12 @@ bool valid_desc(const pkv_pool_desc *d)
         if (!(d->k_scale > 0.0f) || !std::isfinite(d->k_scale)) return false;
         if (!(d->v_scale > 0.0f) || !std::isfinite(d->v_scale)) return false;
     }
-    // the largest element offset of a cache must fit in int64 and the slot count in int32
+    // the slot count must fit in int32, and so must the (layer, block, head) tile index the
+    // kernels use
     if ((int64_t)d->num_blocks * d->block_size > INT32_MAX) return false;
+    const int64_t layers = d->num_layers == 0 ? 1 : d->num_layers;
+    if (layers < 1 || layers > 4096) return false;
+    if (layers * d->num_blocks * d->num_kv_heads >= ((int64_t)1 << 31)) return false;
     return true;
 }
 
@@ -57,6 +61,7 @@ int pkv_pool_create(const pkv_pool_desc *desc, const int32_t *free_order, pkv_po
     pkv_pool *p = new (std::nothrow) pkv_pool();
     if (!p) return PKV_ERR_OOM;
     p->desc = *desc;
+    if (p->desc.num_layers == 0) p->desc.num_layers = 1;
     const int32_t nb = desc->num_blocks;
     p->refcount.assign((size_t)nb, 0);
     if (free_order) {
@@ -104,6 +109,13 @@ int pkv_pool_get_desc(const pkv_pool *pool, pkv_pool_desc *out)
     if (!pool || !out) return PKV_ERR_INVALID;
     *out = pool->desc;
     return PKV_OK;
+}
+
+size_t pkv_pool_layer_bytes(const pkv_pool *pool)
+{
+    if (!pool) return 0;
+    const pkv_pool_desc &d = pool->desc;
+    return (size_t)d.num_blocks * d.num_kv_heads * d.block_size * d.head_dim * pkv::elem_bytes(d);
 }
 
 int pkv_pool_num_free(const pkv_pool *pool, int32_t *out)

@@ -155,3 +155,131 @@ def gpu_step(c: Case, opts=None, append=True):
     counters = ws[:B * c.w.num_kv_heads * 4].view(torch.int32)
     assert int(torch.count_nonzero(counters)) == 0, "split counters not returned to zero"
     return out
+
+
+# ------------------------------------------------------------------------------------
+# Multi-layer cases: caches stacked [layers, NB, Hkv, 16, D], one table for every layer.
+# The oracle has no layer dimension: each layer is a pool of its own, decoded and appended
+# by the single-layer oracle functions.
+# ------------------------------------------------------------------------------------
+@dataclasses.dataclass
+class LayerCase:
+    w: workloads.Workload
+    seq_lens: np.ndarray
+    tables: np.ndarray
+    slots: np.ndarray
+    pool: "pkv.Pool"
+    key_cache: torch.Tensor      # [layers, NB, Hkv, 16, D] (bf16 or uint8 codes)
+    value_cache: torch.Tensor
+    q: torch.Tensor              # bf16 [layers, B, Hq, D]
+    k_new: torch.Tensor          # bf16 [layers, B, Hkv, D]
+    v_new: torch.Tensor
+    k_scale: float
+    v_scale: float
+    kv_dtype: int
+    key_host: list               # per layer: the oracle's host pool before any append
+    value_host: list
+
+
+def build_layers(name: str, device="cuda", overrides=None, host_layers=None) -> LayerCase:
+    """host_layers: the layers given host copies for the oracle (default: all)."""
+    w = workloads.WORKLOADS[name]
+    if overrides:
+        w = dataclasses.replace(w, **overrides)
+    d = workloads.draw(w, device)
+    nl = w.layers
+    assert nl > 1
+    host_layers = range(nl) if host_layers is None else host_layers
+    alloc = oracle.BlockAllocator(d.num_blocks, d.free_order)
+    prefix = alloc.alloc(w.prefix_blocks) if w.prefix_blocks else []
+    tables = oracle.build_block_tables(alloc, d.seq_lens, d.max_blocks, 16, prefix)
+    slots = oracle.slot_mapping(tables, d.seq_lens)
+    live = torch.from_numpy(oracle.live_positions(tables, d.seq_lens, d.num_blocks)).to(device)
+    dead = ~live
+    kc, vc = d.key_cache, d.value_cache
+    nan = torch.tensor(NAN16, dtype=torch.int16, device=device).view(torch.bfloat16)
+    for l in range(nl):                                        # unread positions are NaN
+        kc[l][dead[:, None, :, None].expand_as(kc[l])] = nan
+        vc[l][dead[:, None, :, None].expand_as(vc[l])] = nan
+    slots_dev = torch.from_numpy(slots).to(device)
+    blk, off = slots_dev // 16, slots_dev % 16
+    fp8 = w.kv_dtype == "fp8"
+    k_scale = v_scale = 1.0
+    if fp8:
+        all_slots = torch.from_numpy(oracle.all_slots(tables, d.seq_lens)).to(device)
+        ab, ao = all_slots // 16, all_slots % 16
+        k_src = torch.stack([kc[l][ab, :, ao, :] for l in range(nl)])   # [layers, T, Hkv, D]
+        v_src = torch.stack([vc[l][ab, :, ao, :] for l in range(nl)])
+        kmax = max(k_src.float().abs().max().item(), d.k_new.float().abs().max().item())
+        vmax = max(v_src.float().abs().max().item(), d.v_new.float().abs().max().item())
+        k_scale = float(np.float32(kmax) / np.float32(448.0))
+        v_scale = float(np.float32(vmax) / np.float32(448.0))
+        pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim, pkv.KV_FP8E4M3, k_scale, v_scale,
+                        d.free_order, num_layers=nl)
+        pool.attach_device(torch.cuda.current_device())
+        k8 = torch.full(kc.shape, FP8_NAN, dtype=torch.uint8, device=device)
+        v8 = torch.full(vc.shape, FP8_NAN, dtype=torch.uint8, device=device)
+        pkv.kv_append_layers(pool, k_src, v_src, all_slots, k8, v8)
+        torch.cuda.synchronize()
+        key_host, value_host = [], []
+        sl_host = all_slots.cpu().numpy()
+        for l in host_layers:
+            kh = np.full(kc.shape[1:], FP8_NAN, dtype=np.uint8)
+            vh = np.full(vc.shape[1:], FP8_NAN, dtype=np.uint8)
+            assert oracle.kv_append(workloads.bf16_bits(k_src[l]), workloads.bf16_bits(v_src[l]),
+                                    sl_host, kh, vh, 16, oracle.FP8E4M3, k_scale, v_scale) == 0
+            key_host.append(kh)
+            value_host.append(vh)
+        if w.append:                                           # new token's slot starts as NaN
+            k8[:, blk, :, off, :] = FP8_NAN
+            v8[:, blk, :, off, :] = FP8_NAN
+            for kh, vh in zip(key_host, value_host):
+                for sl in slots:
+                    kh[sl // 16, :, sl % 16, :] = FP8_NAN
+                    vh[sl // 16, :, sl % 16, :] = FP8_NAN
+        kc, vc = k8, v8
+        kv_dtype = pkv.KV_FP8E4M3
+    else:
+        if w.append:
+            kc[:, blk, :, off, :] = nan
+            vc[:, blk, :, off, :] = nan
+        pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim, free_order=d.free_order,
+                        num_layers=nl)
+        pool.attach_device(torch.cuda.current_device())
+        key_host = [workloads.bf16_bits(kc[l]) for l in host_layers]
+        value_host = [workloads.bf16_bits(vc[l]) for l in host_layers]
+        kv_dtype = pkv.KV_BF16
+    return LayerCase(w, d.seq_lens, tables, slots, pool, kc, vc, d.q, d.k_new, d.v_new, k_scale,
+                     v_scale, kv_dtype, key_host, value_host)
+
+
+def oracle_layer(c: LayerCase, l: int, i: int, append: bool, threads=None):
+    """The single-layer oracle on layer l (host copy i): append (optionally), then decode."""
+    fp8 = c.kv_dtype == pkv.KV_FP8E4M3
+    dt = oracle.FP8E4M3 if fp8 else oracle.BF16
+    kh, vh = c.key_host[i].copy(), c.value_host[i].copy()
+    if append:
+        assert oracle.kv_append(workloads.bf16_bits(c.k_new[l]), workloads.bf16_bits(c.v_new[l]),
+                                c.slots, kh, vh, 16, dt, c.k_scale, c.v_scale) == 0
+    st, out = oracle.paged_decode(workloads.bf16_bits(c.q[l]), kh, vh, c.tables, c.seq_lens,
+                                  c.w.scale, c.w.num_kv_heads, 16, dt, c.k_scale, c.v_scale,
+                                  num_threads=threads or oracle.max_threads())
+    assert st == 0
+    return out, kh, vh
+
+
+def gpu_layers(c: LayerCase, append: bool, opts=None):
+    """decode_step_layers (with or without the fused append); returns out [layers, B, Hq, D]."""
+    bt, sl, _ = device_tables(c)
+    nl, B, Hq, D = c.q.shape
+    out = torch.empty_like(c.q)
+    nbytes = pkv.decode_workspace_bytes(c.pool, B, Hq, bt.shape[1], opts)
+    assert nbytes > 0
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=c.q.device)
+    pkv.decode_step_layers(c.pool, c.q, c.k_new if append else None, c.v_new if append else None,
+                           c.key_cache, c.value_cache, bt, sl, c.w.scale, out, ws, opts)
+    st, bits = c.pool.get_device_error()
+    assert st == pkv.OK and bits == 0, (st, bits)
+    counters = ws[:nl * B * c.w.num_kv_heads * 4].view(torch.int32)
+    assert int(torch.count_nonzero(counters)) == 0, "split counters not returned to zero"
+    return out

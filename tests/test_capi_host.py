@@ -138,3 +138,48 @@ def test_device_calls_need_an_attached_pool(lib):
     st = lib.pkv_paged_attention_decode(p.handle, None, None, None, None, None, 1, 8, 1, 0.125,
                                         None, None, 0, None)
     assert st == pkv.ERR_INVALID
+
+
+def test_pool_layers_descriptor(lib):
+    # num_layers 0 means one layer; the stored descriptor says so
+    assert pkv.Pool(4, 2, 64, num_layers=0).get_desc().num_layers == 1
+    assert pkv.Pool(4, 2, 64, num_layers=80).get_desc().num_layers == 80
+    for bad in (-1, 4097):
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.Pool(4, 2, 64, num_layers=bad)
+        assert e.value.status == pkv.ERR_INVALID
+    # the kernels' (layer, block, head) tile index must fit in int32
+    with pytest.raises(pkv.PkvError):
+        pkv.Pool(1 << 20, 8, 128, num_layers=256)
+    pkv.Pool((1 << 20) - 1, 8, 128, num_layers=255)
+
+
+@pytest.mark.parametrize("layers,kv_heads,head_dim,elem", [
+    (32, 8, 128, 2),      # Llama-3-8B: 128 KiB per token
+    (80, 8, 128, 2),      # Llama-2/3-70B: 320 KiB per token
+    (40, 32, 128, 2),     # the ~7B MHA worked example
+    (32, 8, 128, 1),      # the same cache in FP8: half
+])
+def test_pool_bytes_per_token_equal_the_byte_formula(lib, layers, kv_heads, head_dim, elem):
+    """A pool of L stacked layers costs exactly the pages' per-token byte count: K and V, every
+    layer, every KV head, head_dim elements ("KV Cache 与推理优化", byte table; pinned in
+    tests/golden/capacity.txt through oracle.kv_bytes)."""
+    nb = 7
+    p = pkv.Pool(nb, kv_heads, head_dim, pkv.KV_FP8E4M3 if elem == 1 else pkv.KV_BF16,
+                 num_layers=layers)
+    per_token = 2 * layers * p.layer_bytes() / (nb * pkv.BLOCK_SIZE)
+    assert per_token == oracle.kv_bytes(layers, kv_heads, head_dim, elem, 1, 1)
+
+
+def test_layer_workspace_counts_every_layer(lib):
+    one = pkv.decode_workspace_bytes(pkv.Pool(64, 8, 128), 64, 32, 128, {"grid_ctas": 300})
+    many = pkv.decode_workspace_bytes(pkv.Pool(64, 8, 128, num_layers=32), 64, 32, 128,
+                                      {"grid_ctas": 300})
+    assert many - one == (32 - 1) * 64 * 8 * 4        # one int32 counter per (layer, seq, head)
+
+
+def test_layer_calls_need_an_attached_pool(lib):
+    p = pkv.Pool(8, 2, 64, num_layers=3)
+    assert lib.pkv_kv_append_layers(p.handle, None, None, None, 1, None, None, None) == pkv.ERR_INVALID
+    assert lib.pkv_decode_step_layers(p.handle, None, None, None, None, None, None, None, 1, 8, 1,
+                                      0.125, None, None, 0, None, None) == pkv.ERR_INVALID

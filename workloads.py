@@ -38,6 +38,7 @@ class Workload:
     k_gain: float = 1.0          # K drawn as k_gain * N(0,1)
     append: bool = True          # one kv_append per sequence before decode
     kv_dtype: str = "bf16"       # "bf16" or "fp8"
+    layers: int = 1              # layers stacked in each cache (one table for all)
     seed: int = 159000
 
     @property
@@ -63,6 +64,11 @@ WORKLOADS = {
     "qwen25_7b_prefix_fp8": Workload("qwen25_7b_prefix_fp8", 128, 28, 4, 128, "lognormal",
                                      max_len=8192, prefix_blocks=32, append=False,
                                      kv_dtype="fp8", seed=159004),
+    # every layer of a model in one step: caches [layers, NB, Hkv, 16, D]
+    "tiny_layers": Workload("tiny_layers", 2, 8, 2, 64, "list", len_list=(18, 33), pool="fixed",
+                            fixed_blocks=8, layers=3, seed=159005),
+    "llama3_8b_32l": Workload("llama3_8b_32l", 64, 32, 8, 128, "fixed", fixed_len=2048,
+                              layers=32, seed=159006),
 }
 
 
@@ -141,6 +147,7 @@ class Draw:
     num_blocks: int
     max_blocks: int
     free_order: np.ndarray       # int32 [num_blocks]
+    # with w.layers > 1 every tensor below gets a leading [layers] dimension
     q: torch.Tensor              # bf16 [B, Hq, D]
     key_cache: torch.Tensor      # bf16 [NB, Hkv, 16, D]  (history; source of an fp8 pool)
     value_cache: torch.Tensor    # bf16 [NB, Hkv, 16, D]
@@ -154,15 +161,21 @@ def draw(w: Workload, device="cpu", seq_lens=None) -> Draw:
     mb = max_blocks(w, L)
     B, Hq, Hkv, D = len(L), w.num_q_heads, w.num_kv_heads, w.head_dim
     s = w.seed * 16
+    nl = w.layers
+    lead = (nl,) if nl > 1 else ()
+    rows = max(1, (1 << 24) // (Hkv * BLOCK_SIZE * D))
+
+    def pool(seed, gain=1.0):               # drawn as [layers * NB, ...], then viewed
+        t = randn_bf16((nl * nb, Hkv, BLOCK_SIZE, D), seed, device, gain, chunk_rows=rows)
+        return t.view(lead + (nb, Hkv, BLOCK_SIZE, D))
+
     return Draw(
         w=w, seq_lens=L, num_blocks=nb, max_blocks=mb, free_order=draw_free_order(w, nb),
-        q=randn_bf16((B, Hq, D), s + 1, device),
-        key_cache=randn_bf16((nb, Hkv, BLOCK_SIZE, D), s + 2, device, w.k_gain,
-                             chunk_rows=max(1, (1 << 24) // (Hkv * BLOCK_SIZE * D))),
-        value_cache=randn_bf16((nb, Hkv, BLOCK_SIZE, D), s + 3, device,
-                               chunk_rows=max(1, (1 << 24) // (Hkv * BLOCK_SIZE * D))),
-        k_new=randn_bf16((B, Hkv, D), s + 4, device, w.k_gain),
-        v_new=randn_bf16((B, Hkv, D), s + 5, device),
+        q=randn_bf16(lead + (B, Hq, D), s + 1, device),
+        key_cache=pool(s + 2, w.k_gain),
+        value_cache=pool(s + 3),
+        k_new=randn_bf16(lead + (B, Hkv, D), s + 4, device, w.k_gain),
+        v_new=randn_bf16(lead + (B, Hkv, D), s + 5, device),
     )
 
 
