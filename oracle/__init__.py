@@ -18,6 +18,10 @@ Pieces and the passage each follows (page title, section):
   pool, use, return), "理解 KV Cache" §3.5; block tables mapping logical to physical
   blocks and shared prefix blocks referenced by many tables, "KV Cache 与推理优化",
   section "PagedAttention：把 KV Cache 当虚拟内存管".
+* ``copy_on_write`` / ``copy_blocks`` -- a shared prefix block is stored once and referenced
+  by many tables until a request diverges, when the diverging request gets its own copy
+  before it writes ("KV Cache 与推理优化", section "PagedAttention：把 KV Cache 当虚拟内存管",
+  its benefits table and summary tree: 分歧时写时复制).
 * ``kv_append`` / ``paged_decode`` / FP8 codec -- C code in ``pkv_oracle.c`` (fp64).
 """
 from __future__ import annotations
@@ -166,6 +170,55 @@ def build_block_tables(allocator: BlockAllocator, seq_lens, max_blocks: int,
         fresh = allocator.alloc(nblk - len(shared))
         tables[b, :nblk] = shared + fresh
     return tables
+
+
+def copy_on_write(allocator: BlockAllocator, block_tables, seq_lens, block_size: int = 16):
+    """Make the block each sequence is about to write private, in batch order.
+
+    Sequence b writes its newest position L_b - 1, in logical block (L_b - 1) // block_size.
+    If that physical block is referenced more than once, the sequence diverges from the
+    others sharing it: it takes a fresh block from the free pool, gives up its reference to
+    the shared one, and its table entry is pointed at the fresh block, whose content must be
+    a copy of the shared block's before anything is written.  A block whose other holders
+    have all diverged already has one reference left and is written in place.
+
+    Returns (tables, pairs): a new int32 table array and int32 [n, 2] (shared, fresh) pairs
+    in the order they were made.  On exhaustion the allocator is left as it was and
+    MemoryError is raised."""
+    tables = np.array(block_tables, dtype=np.int32, copy=True)
+    saved_free, saved_ref = list(allocator.free), list(allocator.refcount)
+    pairs = []
+    try:
+        for b, L in enumerate(seq_lens):
+            L = int(L)
+            if L < 1 or blocks_needed(L, block_size) > tables.shape[1]:
+                raise ValueError("sequence length outside its table")
+            j = (L - 1) // block_size
+            shared = int(tables[b, j])
+            if shared < 0 or shared >= allocator.num_blocks or allocator.refcount[shared] < 1:
+                raise ValueError("table entry is not an allocated block")
+            if allocator.refcount[shared] == 1:
+                continue                                   # private already
+            fresh = allocator.alloc(1)[0]
+            allocator.release([shared])                    # stays > 0: others still hold it
+            tables[b, j] = fresh
+            pairs.append((shared, fresh))
+    except Exception:
+        allocator.free, allocator.refcount = saved_free, saved_ref
+        raise
+    return tables, np.array(pairs, dtype=np.int32).reshape(-1, 2)
+
+
+def copy_blocks(key_cache: np.ndarray, value_cache: np.ndarray, pairs, layered: bool = False):
+    """cache[dst] = cache[src] for each (src, dst) pair, K and V; with ``layered`` the caches
+    are [layers, NB, ...] and every layer is copied.  In place."""
+    for src, dst in np.asarray(pairs, dtype=np.int64).reshape(-1, 2):
+        if layered:
+            key_cache[:, dst] = key_cache[:, src]
+            value_cache[:, dst] = value_cache[:, src]
+        else:
+            key_cache[dst] = key_cache[src]
+            value_cache[dst] = value_cache[src]
 
 
 def live_positions(block_tables, seq_lens, num_blocks: int, block_size: int = 16) -> np.ndarray:
