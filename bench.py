@@ -170,6 +170,12 @@ def run_ours(args, world, rank, local_rank):
     pool.attach_device(local_rank)
     prefix = pool.alloc(w.prefix_blocks) if w.prefix_blocks else None
     tables = pool.build_block_tables(d.seq_lens, d.max_blocks, prefix)
+    cow_pairs = np.zeros((0, 2), np.int32)
+    if w.append and w.prefix_blocks:
+        # sequences whose newest position lies in a shared block diverge: copy-on-write
+        # bookkeeping once on the host; the block copies run in every timed step (each step
+        # is the step in which those sequences diverge)
+        tables, cow_pairs = pool.cow_prepare(tables, d.seq_lens)
     slots = pkv.slot_mapping(tables, d.seq_lens)
     if w.kv_dtype == "fp8":                      # encode the history through kv_append
         alls = torch.from_numpy(pkv.slot_mapping_all(tables, d.seq_lens)).to(dev)
@@ -190,7 +196,9 @@ def run_ours(args, world, rank, local_rank):
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    launches_per_step = (1 if w.append and args.separate_append else 0) + 1
+    cow_src = torch.from_numpy(cow_pairs[:, 0].copy()).to(dev)
+    cow_dst = torch.from_numpy(cow_pairs[:, 1].copy()).to(dev)
+    launches_per_step = (1 if w.append and args.separate_append else 0) + 1 + (1 if len(cow_pairs) else 0)
     # algorithmic bytes (no credit for tail-slot over-read; shared prefix blocks counted
     # once per reader here, i.e. logical bytes); every layer reads its own K/V, queries and
     # outputs, and all layers share one read of the tables
@@ -198,10 +206,15 @@ def run_ours(args, world, rank, local_rank):
     decode_bytes = kv_read + nl * 2 * B * Hq * D * 2 + B * d.max_blocks * 4 + B * 4
     new_rows = nl * 2 * B * Hkv * D * (2 + elem)              # read k/v_new, write the rows
     append_bytes = (new_rows + (B * 8 if args.separate_append else 0)) if w.append else 0
-    step_bytes = decode_bytes + append_bytes
+    cow_bytes = 2 * 2 * len(cow_pairs) * pool.layer_bytes() // d.num_blocks * nl   # K+V, read+write
+    step_bytes = decode_bytes + append_bytes + cow_bytes
     # bytes of the timed decode launch: with decode_step it also reads k_new/v_new and writes
     # the new rows
     launch_bytes = decode_bytes + (new_rows if w.append and not args.separate_append else 0)
+
+    def cow_call(stream=None):
+        if len(cow_pairs):
+            pkv.copy_blocks(pool, kc, vc, cow_src, cow_dst, stream=stream)
 
     def append_call(stream=None):
         if nl > 1:
@@ -255,6 +268,7 @@ def run_ours(args, world, rank, local_rank):
     def timed_step(i):
         flush_l2()                                # L2 flush (read), outside the timed interval
         starts[i].record(stream)
+        cow_call(stream)
         if w.append and args.separate_append:
             append_call(stream)
         mids[i].record(stream)
@@ -299,8 +313,10 @@ def run_ours(args, world, rank, local_rank):
     tables_host = tables
     h2d = (host["q"].numel() * 2 + (host["k"].numel() * 2 * 2 if w.append else 0)
            + tables_host.nbytes + host["sl"].numel() * 4
-           + (B * 8 if w.append and args.separate_append else 0))
+           + (B * 8 if w.append and args.separate_append else 0) + cow_pairs.nbytes)
     d2h = host["out"].numel() * 2
+    cow_src_h = torch.from_numpy(cow_pairs[:, 0].copy()).pin_memory()
+    cow_dst_h = torch.from_numpy(cow_pairs[:, 1].copy()).pin_memory()
     e2e_steps = max(5, min(K, 200))
     bt_h = torch.from_numpy(tables_host).pin_memory()
     sm_h = torch.empty(B, dtype=torch.int64).pin_memory()
@@ -314,11 +330,15 @@ def run_ours(args, world, rank, local_rank):
             slots_np = pkv.slot_mapping(tables_host, d.seq_lens)        # host allocator side
             sm_h[:] = torch.from_numpy(slots_np)
         d.q.copy_(host["q"], non_blocking=True)
+        if len(cow_pairs):
+            cow_src.copy_(cow_src_h, non_blocking=True)
+            cow_dst.copy_(cow_dst_h, non_blocking=True)
         bt.copy_(bt_h, non_blocking=True)
         sl.copy_(host["sl"], non_blocking=True)
         if w.append:
             d.k_new.copy_(host["k"], non_blocking=True)
             d.v_new.copy_(host["v"], non_blocking=True)
+            cow_call()
             if args.separate_append:
                 sm.copy_(sm_h, non_blocking=True)
                 append_call()
@@ -353,7 +373,9 @@ def run_ours(args, world, rank, local_rank):
                                                  "all %d" % d.seq_lens[0] if w.lengths == "fixed"
                                                  else "%s (sum %d)" % (w.lengths, int(d.seq_lens.sum())),
                                                  w.kv_dtype),
-            "step": (("kv_append + paged_attention_decode" if args.separate_append else
+            "copy_on_write_pairs": int(len(cow_pairs)),
+            "step": ("copy_blocks + " if len(cow_pairs) else "") +
+                    (("kv_append + paged_attention_decode" if args.separate_append else
                       "decode_step (append at L-1 + paged decode, one launch)") if w.append
                      else "paged_attention_decode") + (", all %d layers per launch" % nl if nl > 1 else ""),
             "decode_opts": decode_opts,

@@ -129,6 +129,28 @@ int pkv_build_block_tables(pkv_pool *pool, const int32_t *seq_lens, int32_t batc
                            int32_t max_blocks, const int32_t *prefix_ids, int32_t num_prefix,
                            int32_t *tables_out);
 
+/* Copy-on-write before an append [Paged][Life]: sequence b (in batch order) is about to
+ * write position L_b - 1 = seq_lens[b] - 1, in logical block (L_b - 1) / block_size.  If the
+ * block that entry names is held by more than one reference, the sequence diverges from the
+ * other holders: a fresh block is taken from the front of the free list, the shared block
+ * loses one reference, the table entry (host int32 tables [batch, max_blocks], updated in
+ * place) is pointed at the fresh block, and the pair is recorded -- src_out[i] = shared,
+ * dst_out[i] = fresh (host int32, room for batch entries each), *num_copies = the count.
+ * The last holder of a shared block writes it in place.  The content is not copied here:
+ * run pkv_copy_blocks on the pairs before the append.  INVALID (nothing changed) on a
+ * length outside [1, max_blocks * block_size] or an entry that is not an allocated block;
+ * OOM (nothing changed, tables restored) if the free list runs dry. */
+int pkv_cow_prepare(pkv_pool *pool, int32_t *tables, const int32_t *seq_lens, int32_t batch,
+                    int32_t max_blocks, int32_t *src_out, int32_t *dst_out, int32_t *num_copies);
+
+/* Copy whole blocks [Paged][Layout]: for each pair i and every layer of the pool, the K and
+ * V content of block src[i] is copied to block dst[i] (device int32 arrays, num_pairs
+ * entries; caches the whole stacked tensors).  The dst ids must be distinct and none may be
+ * a src of this call.  An id outside [0, num_blocks) sets PKV_DEVERR_BLOCK_ID and that pair
+ * is skipped. */
+int pkv_copy_blocks(pkv_pool *pool, void *key_cache, void *value_cache, const int32_t *src,
+                    const int32_t *dst, int32_t num_pairs, void *stream);
+
 /* Slot of each sequence's newest token, at position seq_lens[b]-1 [Slot]:
  * slot = tables[b][(L-1) / block_size] * block_size + (L-1) % block_size.  Host arrays:
  * tables int32 [batch, max_blocks], seq_lens int32 [batch], slots_out int64 [batch].

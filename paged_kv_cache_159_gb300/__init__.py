@@ -16,6 +16,7 @@ Names follow the C ABI without the ``pkv_`` prefix:
 * ``decode_step(...)`` -- append each new token at position L-1 and decode, one launch.
 * ``kv_append_layers``, ``decode_step_layers`` -- the same over every layer of a pool whose
   caches stack ``num_layers`` layers (``Pool(..., num_layers=L)``), one launch each.
+* ``Pool.cow_prepare`` and ``copy_blocks`` -- copy-on-write of shared blocks before an append.
 * ``decode_workspace_bytes``, ``probe_copy``, ``device_sm_count``.
 """
 from __future__ import annotations
@@ -38,7 +39,7 @@ EXPORTED = (
     "pkv_pool_refcount", "pkv_pool_alloc", "pkv_pool_share", "pkv_pool_free",
     "pkv_build_block_tables", "pkv_slot_mapping", "pkv_slot_mapping_all",
     "pkv_pool_attach_device", "pkv_kv_append", "pkv_pool_layer_bytes", "pkv_kv_append_layers",
-    "pkv_decode_step_layers",
+    "pkv_decode_step_layers", "pkv_cow_prepare", "pkv_copy_blocks",
     "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
     "pkv_paged_attention_decode_ex", "pkv_decode_step", "pkv_paged_attention_decode_noalloc",
     "pkv_get_device_error", "pkv_probe_copy",
@@ -93,6 +94,8 @@ def lib():
             "pkv_kv_append": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P]),
             "pkv_kv_append_layers": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P]),
             "pkv_pool_layer_bytes": (ctypes.c_size_t, [_P]),
+            "pkv_cow_prepare": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _P, _P, ctypes.POINTER(_I32)]),
+            "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P]),
             "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32, _I32, ctypes.POINTER(decode_opts)]),
             "pkv_paged_attention_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
                                                           ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
@@ -229,6 +232,19 @@ class Pool:
                                             _np_ptr(out)), "build_block_tables")
         return out
 
+    def cow_prepare(self, tables, seq_lens):
+        """Copy-on-write bookkeeping before an append (pkv_cow_prepare): returns (new tables,
+        int32 [n, 2] (shared, fresh) pairs); the input tables are not modified."""
+        tables = np.array(tables, dtype=np.int32, copy=True, order="C")
+        seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        src = np.empty(max(1, seq_lens.size), dtype=np.int32)
+        dst = np.empty_like(src)
+        n = _I32()
+        _check(lib().pkv_cow_prepare(self._h, _np_ptr(tables), _np_ptr(seq_lens), seq_lens.size,
+                                     tables.shape[1], _np_ptr(src), _np_ptr(dst), ctypes.byref(n)),
+               "cow_prepare")
+        return tables, np.stack([src[:n.value], dst[:n.value]], axis=1)
+
     def attach_device(self, device: int = 0):
         _check(lib().pkv_pool_attach_device(self._h, int(device)), "pool_attach_device")
 
@@ -275,6 +291,14 @@ def kv_append_layers(pool: Pool, k, v, slots, key_cache, value_cache, stream=Non
                                       _dev_ptr(key_cache, "key_cache"),
                                       _dev_ptr(value_cache, "value_cache"), _stream_ptr(stream)),
            "kv_append_layers")
+
+
+def copy_blocks(pool: Pool, key_cache, value_cache, src, dst, stream=None):
+    """Copy blocks src[i] -> dst[i] (int32 CUDA tensors) in every layer, K and V."""
+    _check(lib().pkv_copy_blocks(pool.handle, _dev_ptr(key_cache, "key_cache"),
+                                 _dev_ptr(value_cache, "value_cache"), _dev_ptr(src, "src"),
+                                 _dev_ptr(dst, "dst"), int(src.numel()), _stream_ptr(stream)),
+           "copy_blocks")
 
 
 def _opts(opts):

@@ -222,6 +222,56 @@ int pkv_build_block_tables(pkv_pool *pool, const int32_t *seq_lens, int32_t batc
     return PKV_OK;
 }
 
+// Copy-on-write before an append ("KV Cache 与推理优化", PagedAttention section: a shared
+// prefix block is stored once; a request that diverges gets its own copy first).  Sequences
+// are taken in batch order, so the holders of a shared block that write it get copies one
+// after another until a single reference is left, and that last holder writes in place.
+int pkv_cow_prepare(pkv_pool *pool, int32_t *tables, const int32_t *seq_lens, int32_t batch,
+                    int32_t max_blocks, int32_t *src_out, int32_t *dst_out, int32_t *num_copies)
+{
+    if (!pool || batch < 0 || max_blocks < 1 || !num_copies) return PKV_ERR_INVALID;
+    if (batch > 0 && (!tables || !seq_lens || !src_out || !dst_out)) return PKV_ERR_INVALID;
+    const int32_t bs = pool->desc.block_size;
+    // validate first: nothing changes on INVALID
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t L = seq_lens[b];
+        if (L < 1 || (L - 1) / bs >= max_blocks) return PKV_ERR_INVALID;
+        const int32_t e = tables[(size_t)b * max_blocks + (L - 1) / bs];
+        if (e < 0 || e >= pool->desc.num_blocks || pool->refcount[(size_t)e] < 1) return PKV_ERR_INVALID;
+    }
+    int32_t n = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        int32_t &entry = tables[(size_t)b * max_blocks + (seq_lens[b] - 1) / bs];
+        const int32_t shared = entry;
+        if (pool->refcount[(size_t)shared] == 1) continue;    // private already
+        if (pool->free_list.empty()) {
+            // undo in reverse: fresh blocks go back to the front of the free list in the
+            // order they were taken, references and table entries are restored
+            for (int32_t i = n - 1; i >= 0; --i) {
+                pool->refcount[(size_t)dst_out[i]] = 0;
+                pool->free_list.push_front(dst_out[i]);
+                pool->refcount[(size_t)src_out[i]] += 1;
+            }
+            for (int32_t bb = 0, i = 0; bb < b && i < n; ++bb) {
+                int32_t &e2 = tables[(size_t)bb * max_blocks + (seq_lens[bb] - 1) / bs];
+                if (e2 == dst_out[i]) e2 = src_out[i++];
+            }
+            *num_copies = 0;
+            return PKV_ERR_OOM;
+        }
+        const int32_t fresh = pool->free_list.front();
+        pool->free_list.pop_front();
+        pool->refcount[(size_t)fresh] = 1;
+        pool->refcount[(size_t)shared] -= 1;                  // still >= 1: others hold it
+        entry = fresh;
+        src_out[n] = shared;
+        dst_out[n] = fresh;
+        ++n;
+    }
+    *num_copies = n;
+    return PKV_OK;
+}
+
 int pkv_slot_mapping(const int32_t *tables, const int32_t *seq_lens, int32_t batch,
                      int32_t max_blocks, int32_t block_size, int64_t *slots_out)
 {

@@ -48,6 +48,7 @@ class Case:
     # oracle-side pools (host), before any append
     key_host: np.ndarray
     value_host: np.ndarray
+    alloc: "oracle.BlockAllocator" = None    # the oracle's allocator after the tables
 
 
 def build(name: str, device="cuda", seq_lens=None, overrides=None, free_order=None) -> Case:
@@ -66,8 +67,11 @@ def build(name: str, device="cuda", seq_lens=None, overrides=None, free_order=No
     nan = torch.tensor(NAN16, dtype=torch.int16, device=device).view(torch.bfloat16)
     kc[dead[:, None, :, None].expand_as(kc)] = nan
     vc[dead[:, None, :, None].expand_as(vc)] = nan
-    slots_dev = torch.from_numpy(slots).to(device)
-    if w.append and w.kv_dtype != "fp8":                       # the new token's slot starts as NaN
+    # the new token's slot starts as NaN, unless it lies in a block other sequences share (and
+    # read): there the sequence must diverge by copy-on-write before it writes
+    private = np.array([alloc.refcount[int(s) // 16] == 1 for s in slots], dtype=bool)
+    slots_dev = torch.from_numpy(slots[private]).to(device)
+    if w.append and w.kv_dtype != "fp8":
         blk, off = slots_dev // 16, slots_dev % 16
         kc[blk, :, off, :] = nan
         vc[blk, :, off, :] = nan
@@ -102,7 +106,7 @@ def build(name: str, device="cuda", seq_lens=None, overrides=None, free_order=No
             blk, off = slots_dev // 16, slots_dev % 16
             k8[blk, :, off, :] = FP8_NAN
             v8[blk, :, off, :] = FP8_NAN
-            for sl in slots:
+            for sl in slots[private]:
                 key_host[sl // 16, :, sl % 16, :] = FP8_NAN
                 value_host[sl // 16, :, sl % 16, :] = FP8_NAN
         kc, vc = k8, v8
@@ -112,7 +116,7 @@ def build(name: str, device="cuda", seq_lens=None, overrides=None, free_order=No
         key_host = workloads.bf16_bits(kc)
         value_host = workloads.bf16_bits(vc)
     return Case(w, d.seq_lens, tables, slots, pool, kc, vc, d.q, d.k_new, d.v_new, k_scale,
-                v_scale, kv_dtype, key_host, value_host)
+                v_scale, kv_dtype, key_host, value_host, alloc)
 
 
 def oracle_append(c: Case):

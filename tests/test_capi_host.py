@@ -183,3 +183,94 @@ def test_layer_calls_need_an_attached_pool(lib):
     assert lib.pkv_kv_append_layers(p.handle, None, None, None, 1, None, None, None) == pkv.ERR_INVALID
     assert lib.pkv_decode_step_layers(p.handle, None, None, None, None, None, None, None, 1, 8, 1,
                                       0.125, None, None, 0, None, None) == pkv.ERR_INVALID
+
+
+def _both_allocators(nb, order, prefix_n, lens, mb):
+    a = oracle.BlockAllocator(nb, order)
+    p = pkv.Pool(nb, 2, 64, free_order=order)
+    pre_a = a.alloc(prefix_n) if prefix_n else []
+    pre_p = p.alloc(prefix_n) if prefix_n else None
+    ta = oracle.build_block_tables(a, lens, mb, 16, pre_a)
+    tp = p.build_block_tables(lens, mb, pre_p)
+    np.testing.assert_array_equal(ta, tp)
+    return a, p, ta
+
+
+def _same_state(a, p):
+    assert [p.refcount(i) for i in range(a.num_blocks)] == a.refcount
+    assert p.num_free() == len(a.free)
+    if a.free:                                  # the free list's order: take them all
+        q = p.alloc(len(a.free))
+        assert q.tolist() == a.free
+        p.free(q)
+
+
+@pytest.mark.parametrize("name", ["qwen25_7b_prefix_cow", "seeded"])
+def test_cow_prepare_equals_the_oracle(lib, name):
+    if name == "seeded":
+        rng = np.random.Generator(np.random.PCG64(5))
+        lens = rng.integers(1, 80, size=40).astype(np.int32)
+        nb, prefix_n = 400, 4
+        order = rng.permutation(nb).astype(np.int32)
+    else:
+        w = workloads.WORKLOADS[name]
+        lens = workloads.draw_seq_lens(w)
+        nb = workloads.pool_blocks(w, lens)
+        order, prefix_n = workloads.draw_free_order(w, nb), w.prefix_blocks
+    mb = int(max(oracle.blocks_needed(int(L), 16) for L in lens))
+    a, p, t = _both_allocators(nb, order, prefix_n, lens, mb)
+    ta, pa = oracle.copy_on_write(a, t, lens)
+    tp, pp = p.cow_prepare(t, lens)
+    assert len(pa) > 0
+    np.testing.assert_array_equal(tp, ta)
+    np.testing.assert_array_equal(pp, pa)
+    _same_state(a, p)
+
+
+def test_cow_prepare_hand_example_and_errors(lib):
+    p = pkv.Pool(8, 2, 64)
+    pre = p.alloc(2)
+    lens = np.array([20, 32, 40, 17], np.int32)
+    t = p.build_block_tables(lens, 3, pre)
+    t2, pairs = p.cow_prepare(t, lens)
+    assert t2.tolist() == [[0, 3, -1], [0, 4, -1], [0, 1, 2], [0, 5, -1]]
+    assert pairs.tolist() == [[1, 3], [1, 4], [1, 5]]
+    assert [p.refcount(i) for i in range(8)] == [5, 2, 1, 1, 1, 1, 0, 0]
+    # INVALID: nothing changes
+    with pytest.raises(pkv.PkvError) as e:
+        p.cow_prepare(t2, np.array([20, 32, 40, 49], np.int32))     # needs a 4th entry
+    assert e.value.status == pkv.ERR_INVALID
+    bad = t2.copy()
+    bad[3, 1] = 7                                                   # a free block
+    with pytest.raises(pkv.PkvError):
+        p.cow_prepare(bad, lens)
+    assert [p.refcount(i) for i in range(8)] == [5, 2, 1, 1, 1, 1, 0, 0]
+
+
+def test_cow_prepare_exhaustion_restores_everything(lib):
+    for lens in ([3, 3, 3], [3, 3, 3, 3]):
+        p = pkv.Pool(3, 2, 64, free_order=[0, 1, 2])
+        blk = p.alloc(1)
+        for _ in range(len(lens) - 1):
+            p.share(blk)
+        t = np.zeros((len(lens), 1), np.int32)
+        a = oracle.BlockAllocator(3, [0, 1, 2])
+        a.alloc(1)
+        a.share([0] * (len(lens) - 1))
+        if len(lens) == 3:                      # two copies fit: 0 -> 1, 0 -> 2
+            t2, pairs = p.cow_prepare(t, np.array(lens, np.int32))
+            ta, pa = oracle.copy_on_write(a, t, lens)
+            np.testing.assert_array_equal(t2, ta)
+            np.testing.assert_array_equal(pairs, pa)
+            continue
+        tables = t.copy()                       # three copies needed, two blocks free
+        src = np.empty(4, np.int32)
+        dst = np.empty(4, np.int32)
+        n = pkv.ctypes.c_int32()
+        st = lib.pkv_cow_prepare(p.handle, pkv._np_ptr(tables), pkv._np_ptr(np.array(lens, np.int32)),
+                                 len(lens), 1, pkv._np_ptr(src), pkv._np_ptr(dst), pkv.ctypes.byref(n))
+        assert st == pkv.ERR_OOM and n.value == 0
+        np.testing.assert_array_equal(tables, t)
+        with pytest.raises(MemoryError):
+            oracle.copy_on_write(a, t, lens)
+        _same_state(a, p)

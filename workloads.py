@@ -64,6 +64,10 @@ WORKLOADS = {
     "qwen25_7b_prefix_fp8": Workload("qwen25_7b_prefix_fp8", 128, 28, 4, 128, "lognormal",
                                      max_len=8192, prefix_blocks=32, append=False,
                                      kv_dtype="fp8", seed=159004),
+    # the prefix-sharing batch with appends: sequences whose newest position falls in a
+    # shared block diverge and get a private copy first (copy-on-write)
+    "qwen25_7b_prefix_cow": Workload("qwen25_7b_prefix_cow", 128, 28, 4, 128, "lognormal",
+                                     max_len=8192, prefix_blocks=32, append=True, seed=159004),
     # every layer of a model in one step: caches [layers, NB, Hkv, 16, D]
     "tiny_layers": Workload("tiny_layers", 2, 8, 2, 64, "list", len_list=(18, 33), pool="fixed",
                             fixed_blocks=8, layers=3, seed=159005),
@@ -105,6 +109,8 @@ def pool_blocks(w: Workload, seq_lens) -> int:
     if w.prefix_blocks:
         need = w.prefix_blocks + sum(max(0, _blocks(int(L)) - w.prefix_blocks)
                                      for L in seq_lens)
+        if w.append:                       # room for one private copy per sequence
+            need += len(seq_lens)
     if w.pool == "exact":
         return need
     if w.pool == "double":
