@@ -22,6 +22,13 @@ Pieces and the passage each follows (page title, section):
   by many tables until a request diverges, when the diverging request gets its own copy
   before it writes ("KV Cache 与推理优化", section "PagedAttention：把 KV Cache 当虚拟内存管",
   its benefits table and summary tree: 分歧时写时复制).
+* ``fnv1a_64`` / ``block_hashes`` / ``PrefixCache`` -- automatic prefix caching: a hash
+  per full block, a new request reuses the cached physical blocks of its longest cached
+  prefix, and the lookup stops at the first block that misses ("KV Cache 与推理优化",
+  section "APC：连计算都省了"); reuse must match the token sequence, the positions and the
+  model ("一个请求为什么越生成越占内存?", paging section, on prefix sharing), so each block's
+  hash chains the previous block's hash and starts from a per-model salt.  The hash is
+  64-bit FNV-1a (Fowler, Noll, Vo), written from its definition.
 * ``kv_append`` / ``paged_decode`` / FP8 codec -- C code in ``pkv_oracle.c`` (fp64).
 """
 from __future__ import annotations
@@ -219,6 +226,138 @@ def copy_blocks(key_cache: np.ndarray, value_cache: np.ndarray, pairs, layered: 
         else:
             key_cache[dst] = key_cache[src]
             value_cache[dst] = value_cache[src]
+
+
+# ------------------------------------------------------------------------------------
+# Automatic prefix caching ("KV Cache 与推理优化", section "APC：连计算都省了").
+# ------------------------------------------------------------------------------------
+FNV64_OFFSET = 0xCBF29CE484222325
+FNV64_PRIME = 0x100000001B3
+_M64 = (1 << 64) - 1
+
+
+def fnv1a_64(data: bytes, h: int = FNV64_OFFSET) -> int:
+    """64-bit FNV-1a: for each byte, xor it into the state, then multiply by the prime."""
+    for byte in data:
+        h = ((h ^ byte) * FNV64_PRIME) & _M64
+    return h
+
+
+def block_hashes(tokens, salt: int = 0, block_size: int = 16):
+    """Hash of every full block of a token sequence (a partial last block has none).
+    Block i hashes the 8 little-endian bytes of the previous block's hash (the salt for
+    block 0) followed by its tokens as 4 little-endian bytes each, so equal hashes mean an
+    equal salt and equal tokens in every position up to the end of that block."""
+    out, prev = [], int(salt) & _M64
+    for i in range(len(tokens) // block_size):
+        data = prev.to_bytes(8, "little") + b"".join(
+            int(t & 0xFFFFFFFF).to_bytes(4, "little") for t in tokens[i * block_size:(i + 1) * block_size])
+        prev = fnv1a_64(data)
+        out.append(prev)
+    return out
+
+
+class PrefixCache:
+    """Cached full blocks, each held by one reference of its own while it is cached.
+
+    An entry is (hash, block, parent block or -1, salt, tokens).  A lookup walks a request's
+    full blocks in order; block i hits an entry with its hash whose parent is the block hit
+    for i-1, whose salt is the request's and whose tokens are block i's tokens (so a hash
+    collision can never hand out the wrong block), and the walk stops at the first miss.
+    Every hit or insert stamps its entry from a counter; eviction takes the entry with the
+    smallest stamp among those with no cached child whose block no table holds."""
+
+    def __init__(self, block_size: int = 16):
+        self.bs = block_size
+        self.entries = {}             # block -> dict
+        self.clock = 0
+
+    def _touch(self, e):
+        self.clock += 1
+        e["stamp"] = self.clock
+
+    def _match(self, h, parent, salt, toks):
+        for e in self.entries.values():
+            if e["hash"] == h and e["parent"] == parent and e["salt"] == salt and e["tokens"] == toks:
+                return e
+        return None
+
+    def _blocks(self, tokens):
+        return [list(map(int, tokens[i * self.bs:(i + 1) * self.bs]))
+                for i in range(len(tokens) // self.bs)]
+
+    def lookup(self, tokens, salt: int = 0):
+        """Physical blocks of the longest cached prefix (full blocks only)."""
+        hits, parent = [], -1
+        for h, toks in zip(block_hashes(tokens, salt, self.bs), self._blocks(tokens)):
+            e = self._match(h, parent, salt, toks)
+            if e is None:
+                break
+            self._touch(e)
+            hits.append(e["block"])
+            parent = e["block"]
+        return hits
+
+    def insert(self, allocator: BlockAllocator, tokens, salt: int, table_row):
+        """Cache every full block of a request whose table row is ``table_row``; blocks
+        already cached (by an equal chain) are only stamped.  Returns how many blocks were
+        added.  A row block that is cached under another chain makes the call fail with
+        nothing changed (ValueError)."""
+        hs, blocks = block_hashes(tokens, salt, self.bs), self._blocks(tokens)
+        if len(table_row) < len(hs):
+            raise ValueError("table row shorter than the full blocks")
+        plan, parent = [], -1                       # validate before changing anything
+        for i, (h, toks) in enumerate(zip(hs, blocks)):
+            e = self._match(h, parent, salt, toks)
+            if e is not None:
+                plan.append(("hit", e))
+                parent = e["block"]
+                continue
+            b = int(table_row[i])
+            if b < 0 or b >= allocator.num_blocks or allocator.refcount[b] < 1 or b in self.entries:
+                raise ValueError("row block is not an allocated, uncached block")
+            plan.append(("new", (h, b, parent, toks)))
+            parent = b
+        added = 0
+        for kind, x in plan:
+            if kind == "hit":
+                self._touch(x)
+                continue
+            h, b, par, toks = x
+            e = {"hash": h, "block": b, "parent": par, "salt": int(salt), "tokens": toks,
+                 "children": 0, "stamp": 0}
+            self._touch(e)
+            self.entries[b] = e
+            if par >= 0:
+                self.entries[par]["children"] += 1
+            allocator.share([b])
+            added += 1
+        return added
+
+    def _drop(self, allocator: BlockAllocator, e):
+        del self.entries[e["block"]]
+        if e["parent"] >= 0:
+            self.entries[e["parent"]]["children"] -= 1
+        allocator.release([e["block"]])
+
+    def evict(self, allocator: BlockAllocator, n: int):
+        """Free up to n cached blocks, least recently used first; returns their ids."""
+        out = []
+        while len(out) < n:
+            cand = [e for e in self.entries.values()
+                    if e["children"] == 0 and allocator.refcount[e["block"]] == 1]
+            if not cand:
+                break
+            e = min(cand, key=lambda x: x["stamp"])
+            self._drop(allocator, e)
+            out.append(e["block"])
+        return out
+
+    def clear(self, allocator: BlockAllocator):
+        """Drop every entry (children before parents: leaves by stamp, repeatedly)."""
+        while self.entries:
+            leaves = [e for e in self.entries.values() if e["children"] == 0]
+            self._drop(allocator, min(leaves, key=lambda x: x["stamp"]))
 
 
 def live_positions(block_tables, seq_lens, num_blocks: int, block_size: int = 16) -> np.ndarray:
