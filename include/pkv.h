@@ -27,6 +27,10 @@
  *             groups of g = Hq / Hkv.
  *   [Quant]   same page, section "KV 量化": K/V stored in FP8 (1 byte) with higher-precision
  *             arithmetic.
+ *   [APC]     same page, section "APC：连计算都省了": a hash per full block; a request whose
+ *             prefix matches a cached one reuses those physical blocks; the lookup stops at
+ *             the first miss.  "一个请求为什么越生成越占内存?" (learning-field-guides), paging
+ *             section: reuse must match the tokens, their positions and the model.
  *   [Bytes]   same page, section "KV Cache 有多大：一张显存账单": every layer keeps K and V
  *             for every token, 2 * layers * kv_heads * head_dim * element-bytes per token;
  *             "一个请求为什么越生成越占内存?" (learning-field-guides), capacity derivation:
@@ -163,6 +167,49 @@ int pkv_slot_mapping(const int32_t *tables, const int32_t *seq_lens, int32_t bat
  * Host arrays as in pkv_slot_mapping; same errors. */
 int pkv_slot_mapping_all(const int32_t *tables, const int32_t *seq_lens, int32_t batch,
                          int32_t max_blocks, int32_t block_size, int64_t *slots_out);
+
+/* Automatic prefix caching [APC] (host only).  A full block of block_size tokens is
+ * identified by a chained hash: block i hashes, with 64-bit FNV-1a, the 8 little-endian
+ * bytes of block i-1's hash (of `salt` for block 0) followed by its tokens as 4
+ * little-endian bytes each.  Equal hashes thus stand for an equal salt (a model / adapter
+ * identity: another model must never reuse the blocks) and equal tokens at every position
+ * up to the end of the block.  A partial last block has no hash and is never shared.
+ *
+ * pkv_block_hashes: hashes_out (host, num_tokens / block_size entries) receives the hash of
+ * every full block of tokens (host int32 token ids).  Needs no pool. */
+int pkv_block_hashes(const int32_t *tokens, int32_t num_tokens, int32_t block_size, uint64_t salt,
+                     uint64_t *hashes_out);
+
+/* The physical blocks holding the longest cached prefix of a request [APC]: block i hits an
+ * entry with its hash whose parent is the block hit for i-1 and whose stored salt and
+ * tokens are the request's (so a hash collision never returns another prefix's block); the
+ * walk stops at the first miss.  block_ids_out (host, room for num_tokens / block_size)
+ * receives the hits in order, *num_hits their count.  Takes no references: pass the ids
+ * as prefix_ids to pkv_build_block_tables, which does.  Marks the hits as recently used. */
+int pkv_prefix_lookup(pkv_pool *pool, const int32_t *tokens, int32_t num_tokens, uint64_t salt,
+                      int32_t *block_ids_out, int32_t *num_hits);
+
+/* Cache every full block of a request whose block table row is table_row (host, row_len >=
+ * num_tokens / block_size entries) [APC].  A block whose chain is cached already is only
+ * marked as used; every other one is entered under its hash and gets one more reference,
+ * held by the cache until it is evicted, so it outlives the request.  *num_added receives
+ * the number of blocks entered.  INVALID (nothing changed) if a row block that would be
+ * entered is not allocated, is cached under another chain, or appears twice. */
+int pkv_prefix_insert(pkv_pool *pool, const int32_t *tokens, int32_t num_tokens, uint64_t salt,
+                      const int32_t *table_row, int32_t row_len, int32_t *num_added);
+
+/* Evict up to max_blocks cached blocks [APC][Life]: repeatedly the least recently used entry
+ * that has no cached child and whose block only the cache holds (reference count 1) loses
+ * its entry and the cache's reference, which returns the block to the back of the free
+ * list.  evicted_out (host, room for max_blocks) receives their ids in order. */
+int pkv_prefix_evict(pkv_pool *pool, int32_t max_blocks, int32_t *evicted_out, int32_t *num_evicted);
+
+/* Drop every cache entry (least recently used leaves first), releasing the cache's
+ * references; blocks still held by tables stay allocated. */
+int pkv_prefix_clear(pkv_pool *pool);
+
+/* Number of cached blocks. */
+int pkv_prefix_cached_blocks(const pkv_pool *pool, int32_t *out);
 
 /* Bind the pool to a CUDA device: allocates its 4-byte device error word (cudaMalloc) on
  * that device.  Required once before pkv_kv_append / pkv_paged_attention_decode. */

@@ -306,7 +306,7 @@ class PrefixCache:
         hs, blocks = block_hashes(tokens, salt, self.bs), self._blocks(tokens)
         if len(table_row) < len(hs):
             raise ValueError("table row shorter than the full blocks")
-        plan, parent = [], -1                       # validate before changing anything
+        plan, parent, planned = [], -1, set()       # validate before changing anything
         for i, (h, toks) in enumerate(zip(hs, blocks)):
             e = self._match(h, parent, salt, toks)
             if e is not None:
@@ -314,8 +314,10 @@ class PrefixCache:
                 parent = e["block"]
                 continue
             b = int(table_row[i])
-            if b < 0 or b >= allocator.num_blocks or allocator.refcount[b] < 1 or b in self.entries:
+            if (b < 0 or b >= allocator.num_blocks or allocator.refcount[b] < 1 or
+                    b in self.entries or b in planned):
                 raise ValueError("row block is not an allocated, uncached block")
+            planned.add(b)
             plan.append(("new", (h, b, parent, toks)))
             parent = b
         added = 0

@@ -17,6 +17,8 @@ Names follow the C ABI without the ``pkv_`` prefix:
 * ``kv_append_layers``, ``decode_step_layers`` -- the same over every layer of a pool whose
   caches stack ``num_layers`` layers (``Pool(..., num_layers=L)``), one launch each.
 * ``Pool.cow_prepare`` and ``copy_blocks`` -- copy-on-write of shared blocks before an append.
+* ``block_hashes``, ``Pool.prefix_lookup / prefix_insert / prefix_evict / prefix_clear`` --
+  automatic prefix caching on the host.
 * ``decode_workspace_bytes``, ``probe_copy``, ``device_sm_count``.
 """
 from __future__ import annotations
@@ -40,6 +42,8 @@ EXPORTED = (
     "pkv_build_block_tables", "pkv_slot_mapping", "pkv_slot_mapping_all",
     "pkv_pool_attach_device", "pkv_kv_append", "pkv_pool_layer_bytes", "pkv_kv_append_layers",
     "pkv_decode_step_layers", "pkv_cow_prepare", "pkv_copy_blocks",
+    "pkv_block_hashes", "pkv_prefix_lookup", "pkv_prefix_insert", "pkv_prefix_evict",
+    "pkv_prefix_clear", "pkv_prefix_cached_blocks",
     "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
     "pkv_paged_attention_decode_ex", "pkv_decode_step", "pkv_paged_attention_decode_noalloc",
     "pkv_get_device_error", "pkv_probe_copy",
@@ -96,6 +100,13 @@ def lib():
             "pkv_pool_layer_bytes": (ctypes.c_size_t, [_P]),
             "pkv_cow_prepare": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _P, _P, ctypes.POINTER(_I32)]),
             "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P]),
+            "pkv_block_hashes": (ctypes.c_int, [_P, _I32, _I32, ctypes.c_uint64, _P]),
+            "pkv_prefix_lookup": (ctypes.c_int, [_P, _P, _I32, ctypes.c_uint64, _P, ctypes.POINTER(_I32)]),
+            "pkv_prefix_insert": (ctypes.c_int, [_P, _P, _I32, ctypes.c_uint64, _P, _I32,
+                                                 ctypes.POINTER(_I32)]),
+            "pkv_prefix_evict": (ctypes.c_int, [_P, _I32, _P, ctypes.POINTER(_I32)]),
+            "pkv_prefix_clear": (ctypes.c_int, [_P]),
+            "pkv_prefix_cached_blocks": (ctypes.c_int, [_P, ctypes.POINTER(_I32)]),
             "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32, _I32, ctypes.POINTER(decode_opts)]),
             "pkv_paged_attention_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
                                                           ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
@@ -245,6 +256,39 @@ class Pool:
                "cow_prepare")
         return tables, np.stack([src[:n.value], dst[:n.value]], axis=1)
 
+    # ---- automatic prefix caching (host)
+    def prefix_lookup(self, tokens, salt: int = 0) -> np.ndarray:
+        """Physical blocks of the longest cached prefix of ``tokens`` (pkv_prefix_lookup)."""
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+        out = np.empty(max(1, tokens.size // BLOCK_SIZE), dtype=np.int32)
+        n = _I32()
+        _check(lib().pkv_prefix_lookup(self._h, _np_ptr(tokens), tokens.size, int(salt) & (2**64 - 1),
+                                       _np_ptr(out), ctypes.byref(n)), "prefix_lookup")
+        return out[:n.value]
+
+    def prefix_insert(self, tokens, salt: int, table_row) -> int:
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+        row = np.ascontiguousarray(table_row, dtype=np.int32)
+        n = _I32()
+        _check(lib().pkv_prefix_insert(self._h, _np_ptr(tokens), tokens.size, int(salt) & (2**64 - 1),
+                                       _np_ptr(row), row.size, ctypes.byref(n)), "prefix_insert")
+        return n.value
+
+    def prefix_evict(self, max_blocks: int) -> np.ndarray:
+        out = np.empty(max(1, int(max_blocks)), dtype=np.int32)
+        n = _I32()
+        _check(lib().pkv_prefix_evict(self._h, int(max_blocks), _np_ptr(out), ctypes.byref(n)),
+               "prefix_evict")
+        return out[:n.value]
+
+    def prefix_clear(self):
+        _check(lib().pkv_prefix_clear(self._h), "prefix_clear")
+
+    def prefix_cached_blocks(self) -> int:
+        n = _I32()
+        _check(lib().pkv_prefix_cached_blocks(self._h, ctypes.byref(n)), "prefix_cached_blocks")
+        return n.value
+
     def attach_device(self, device: int = 0):
         _check(lib().pkv_pool_attach_device(self._h, int(device)), "pool_attach_device")
 
@@ -273,6 +317,15 @@ def slot_mapping_all(tables, seq_lens, block_size: int = BLOCK_SIZE) -> np.ndarr
                                       tables.shape[1], int(block_size), _np_ptr(out)),
            "slot_mapping_all")
     return out
+
+
+def block_hashes(tokens, salt: int = 0, block_size: int = BLOCK_SIZE) -> np.ndarray:
+    """Chained 64-bit hash of every full block of ``tokens`` (pkv_block_hashes)."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    out = np.empty(max(1, tokens.size // int(block_size)), dtype=np.uint64)
+    _check(lib().pkv_block_hashes(_np_ptr(tokens), tokens.size, int(block_size),
+                                  int(salt) & (2**64 - 1), _np_ptr(out)), "block_hashes")
+    return out[:tokens.size // int(block_size)]
 
 
 def kv_append(pool: Pool, k, v, slots, key_cache, value_cache, stream=None):

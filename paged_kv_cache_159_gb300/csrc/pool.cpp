@@ -100,6 +100,7 @@ int pkv_pool_destroy(pkv_pool *pool)
         if (cudaFree(pool->d_err) != cudaSuccess) st = PKV_ERR_CUDA;
         if (prev >= 0 && prev != pool->device) cudaSetDevice(prev);
     }
+    pkv::destroy_prefix_cache(pool);
     delete pool;
     return st;
 }

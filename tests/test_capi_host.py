@@ -274,3 +274,77 @@ def test_cow_prepare_exhaustion_restores_everything(lib):
         with pytest.raises(MemoryError):
             oracle.copy_on_write(a, t, lens)
         _same_state(a, p)
+
+
+def test_block_hashes_equal_the_oracle(lib):
+    rng = np.random.Generator(np.random.PCG64(11))
+    for n, salt in ((0, 0), (15, 3), (16, 0), (100, 2**64 - 1), (2048, 12345)):
+        toks = rng.integers(-2**31, 2**31, size=n, dtype=np.int64).astype(np.int32)
+        got = pkv.block_hashes(toks, salt)
+        assert [int(x) for x in got] == oracle.block_hashes(toks.tolist(), salt)
+
+
+def test_prefix_cache_follows_the_oracle_through_a_serving_trace(lib):
+    """Requests with shared system prompts arrive, look up their cached prefix, take the
+    rest from the free list, cache their blocks, finish and release; the pool evicts under
+    pressure.  Every return value and the whole allocator state match the oracle's."""
+    rng = np.random.Generator(np.random.PCG64(12))
+    nb = 32                  # small enough that the trace evicts (38 blocks) and hits (150)
+    order = rng.permutation(nb).astype(np.int32)
+    a, c = oracle.BlockAllocator(nb, order), oracle.PrefixCache()
+    p = pkv.Pool(nb, 2, 64, free_order=order)
+    prompts = [rng.integers(0, 50000, size=int(n)).tolist() for n in (48, 64, 32)]
+    live, hits, evicted = [], 0, 0
+    for step in range(120):
+        if live and (rng.random() < 0.45 or len(live) > 5):
+            row = live.pop(int(rng.integers(len(live))))
+            a.release(list(row))
+            p.free(row)
+        else:
+            sysp = prompts[int(rng.integers(len(prompts)))]
+            toks = sysp + rng.integers(0, 50000, size=int(rng.integers(0, 40))).tolist()
+            salt = int(rng.integers(2))
+            ha = c.lookup(toks, salt)
+            hp = p.prefix_lookup(toks, salt)
+            assert hp.tolist() == ha
+            hits += len(ha)
+            nblk = oracle.blocks_needed(len(toks), 16)
+            need = nblk - len(ha)
+            if need > len(a.free):                           # make room
+                ea = c.evict(a, need - len(a.free))
+                ep = p.prefix_evict(need - p.num_free())
+                assert ep.tolist() == ea
+                evicted += len(ea)
+                if need > len(a.free):
+                    continue
+            ta = oracle.build_block_tables(a, [len(toks)], nblk, 16, ha)[0]
+            tp = p.build_block_tables([len(toks)], nblk, hp)[0]
+            assert tp.tolist() == ta.tolist()
+            assert p.prefix_insert(toks, salt, tp) == c.insert(a, toks, salt, ta)
+            live.append(tp)
+        assert p.prefix_cached_blocks() == len(c.entries)
+        assert [p.refcount(i) for i in range(nb)] == a.refcount
+    assert hits > 100 and evicted > 20
+    for row in live:
+        a.release(list(row))
+        p.free(row)
+    c.clear(a)
+    p.prefix_clear()
+    assert p.prefix_cached_blocks() == 0 and p.num_free() == nb
+    assert p.alloc(nb).tolist() == a.free                  # the free list's order too
+
+
+def test_prefix_insert_errors_change_nothing(lib):
+    p = pkv.Pool(8, 2, 64)
+    row = p.alloc(2)
+    toks = list(range(32))
+    assert p.prefix_insert(toks, 0, row) == 2
+    with pytest.raises(pkv.PkvError):
+        p.prefix_insert(list(range(100, 132)), 0, row)     # blocks cached under another chain
+    other = p.alloc(1)
+    with pytest.raises(pkv.PkvError):
+        p.prefix_insert(list(range(200, 232)), 0, [other[0], other[0]])   # the same block twice
+    with pytest.raises(pkv.PkvError):
+        p.prefix_insert(list(range(300, 316)), 0, [7])                    # a free block
+    assert p.prefix_cached_blocks() == 2 and p.refcount(int(other[0])) == 1
+    assert p.prefix_lookup(toks + [5] * 3).tolist() == row.tolist()
