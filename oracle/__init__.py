@@ -29,6 +29,13 @@ Pieces and the passage each follows (page title, section):
   model ("一个请求为什么越生成越占内存?", paging section, on prefix sharing), so each block's
   hash chains the previous block's hash and starts from a per-model salt.  The hash is
   64-bit FNV-1a (Fowler, Noll, Vo), written from its definition.
+* ``paged_prefill`` -- a prompt (or a chunk of one) of P tokens after C cached positions:
+  query i sits at position C + i and attends causally over positions 0 .. C + i ("理解 KV
+  Cache" §1.2: position i aggregates only positions <= i; §2.1: prefill computes every
+  prompt position at once; "KV Cache 与推理优化", pitfalls table: packed sequences need a
+  per-sequence (block-diagonal) causal mask).  Each query is therefore a decode query whose
+  sequence length is its position + 1, and ``paged_prefill`` is ``paged_decode`` over those
+  per-query lengths.
 * ``kv_append`` / ``paged_decode`` / FP8 codec -- C code in ``pkv_oracle.c`` (fp64).
 """
 from __future__ import annotations
@@ -449,3 +456,29 @@ def paged_decode(q_bits, key_cache, value_cache, block_tables, seq_lens, scale: 
         B, Hq, num_kv_heads, D, block_tables.shape[1], block_size, key_cache.shape[0],
         kv_dtype, k_scale, v_scale, scale, pptr, npairs, num_threads, _ptr(out))
     return int(st), out
+
+
+def paged_prefill(q_bits, key_cache, value_cache, block_tables, seq_lens, cu_q, scale: float,
+                  num_kv_heads: int, block_size: int = 16, kv_dtype=BF16, k_scale=1.0,
+                  v_scale=1.0, num_threads: int = 1):
+    """fp64 causal attention of packed prompt chunks over the paged cache.
+
+    q_bits: uint16 [T, Hq, D] (bf16 patterns), rows cu_q[b] .. cu_q[b+1]-1 belonging to
+    sequence b; seq_lens[b] counts the sequence's positions including the chunk (whose K/V
+    are already in the cache).  Row cu_q[b] + i is position seq_lens[b] - P_b + i and sees
+    positions 0 .. that position.  Returns (status, out float64 [T, Hq, D])."""
+    cu_q = np.asarray(cu_q, dtype=np.int64)
+    rows, lens = [], []
+    for b in range(len(seq_lens)):
+        P = int(cu_q[b + 1] - cu_q[b])
+        first = int(seq_lens[b]) - P
+        if P < 0 or first < 0:
+            return 1, None
+        for i in range(P):
+            rows.append(b)
+            lens.append(first + i + 1)
+    tables = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32)[np.asarray(rows, dtype=np.int64)]
+                                  if rows else np.zeros((0, np.asarray(block_tables).shape[1]), np.int32))
+    return paged_decode(q_bits, key_cache, value_cache, tables, np.asarray(lens, dtype=np.int32),
+                        scale, num_kv_heads, block_size, kv_dtype, k_scale, v_scale,
+                        num_threads=num_threads)
