@@ -60,6 +60,7 @@ typedef enum {
 #define PKV_DEVERR_BLOCK_ID 0x2u   /* decode: a needed table entry outside [0, num_blocks) */
 #define PKV_DEVERR_SEQ_LEN  0x4u   /* decode: seq_len outside [1, max_blocks * block_size] */
 #define PKV_DEVERR_TIMEOUT  0x8u   /* a pipeline wait exceeded its bound (about 1 s) */
+#define PKV_DEVERR_PLAN     0x10u  /* prefill: the plan does not match the call (nothing ran) */
 
 typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8E4M3 = 1 } pkv_kv_dtype;
 
@@ -211,6 +212,15 @@ int pkv_prefix_clear(pkv_pool *pool);
 /* Number of cached blocks. */
 int pkv_prefix_cached_blocks(const pkv_pool *pool, int32_t *out);
 
+/* Slots of each prompt chunk's positions [Slot]: sequence b's chunk is rows cu_q[b] ..
+ * cu_q[b+1]-1 (host int32 [batch+1], cu_q[0] = 0), positions L_b - P_b .. L_b - 1 with
+ * P_b = cu_q[b+1] - cu_q[b] and L_b = seq_lens[b] (the length including the chunk);
+ * slots_out (host int64, cu_q[batch] entries) receives their slots in row order -- the
+ * slot mapping of a prefill's kv_append.  INVALID as pkv_slot_mapping, or if P_b < 0 or
+ * P_b > L_b. */
+int pkv_slot_mapping_chunks(const int32_t *tables, const int32_t *seq_lens, const int32_t *cu_q,
+                            int32_t batch, int32_t max_blocks, int32_t block_size, int64_t *slots_out);
+
 /* Bind the pool to a CUDA device: allocates its 4-byte device error word (cudaMalloc) on
  * that device.  Required once before pkv_kv_append / pkv_paged_attention_decode. */
 int pkv_pool_attach_device(pkv_pool *pool, int device);
@@ -307,6 +317,43 @@ int pkv_decode_step_layers(pkv_pool *pool, const void *q, const void *k_new, con
                            const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                            int32_t max_blocks, float scale, void *out, void *workspace,
                            size_t workspace_bytes, const pkv_decode_opts *opts, void *stream);
+
+/* ---- Prefill and chunked prefill [Decode][Attn][GQA][Paged] ----
+ * A batch packs, per sequence b, a chunk of P_b = cu_q[b+1] - cu_q[b] query rows (rows
+ * cu_q[b] .. cu_q[b+1]-1 of q) whose K/V are already in the cache (pkv_kv_append with
+ * pkv_slot_mapping_chunks), behind C_b = seq_lens[b] - P_b earlier positions.  Row
+ * cu_q[b] + i is position C_b + i and attends causally over positions 0 .. C_b + i of its
+ * own sequence:  out[row][hq] = sum_{j <= C_b + i} softmax_j(scale * q[row][hq] . K_j) V_j,
+ * K_j, V_j gathered through block_tables[b] from KV head hq / (Hq / Hkv).  C_b = 0 is the
+ * prefill of a whole prompt; C_b > 0 a later chunk of a long prompt.
+ *
+ * The work is planned on the host once per batch (every layer of a model can reuse the
+ * plan) and run on the device per layer.  pkv_prefill_plan_bytes: an upper bound of the
+ * plan's size for batch sequences and total_q packed rows (0 if the shape is invalid).
+ * pkv_prefill_plan: cu_q (host int32 [batch+1], cu_q[0] = 0) and seq_lens (host int32
+ * [batch], each >= its P_b, >= 1, needing at most max_blocks table entries) give the units
+ * (sequence, KV head, tile of 128 / g query positions) and their assignment to a one-wave
+ * persistent grid, heaviest unit first to the least-loaded CTA; plan_out (host,
+ * plan_bytes) receives it and *grid_out the grid.  The caller copies the plan to device
+ * memory (32-byte aligned) for pkv_paged_prefill.  Requires Hq a multiple of Hkv with
+ * g <= 16.  Queries the current device's SM count. */
+size_t pkv_prefill_plan_bytes(const pkv_pool *pool, int32_t batch, int32_t num_q_heads, int32_t total_q);
+int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const int32_t *seq_lens, int32_t batch,
+                     int32_t num_q_heads, int32_t max_blocks, void *plan_out, size_t plan_bytes,
+                     int32_t *grid_out);
+
+/* Run a plan: q bf16 [total_q, num_q_heads, D] (device); caches of one layer as in
+ * pkv_pool_desc (bf16 pools only; FP8 pools are INVALID); block_tables int32
+ * [batch, max_blocks] (device); plan the device copy of pkv_prefill_plan's output and grid
+ * its grid; out bf16 [total_q, num_q_heads, D] (device, fp32 accumulation, rounded to
+ * nearest even).  Rows are computed on the tcgen05 tensor cores: S = Q.K^T and O += P.V in
+ * tensor memory, P in bf16.  Positions a row may not see are never used, whatever the
+ * cache holds there.  A plan that does not match the call sets PKV_DEVERR_PLAN and
+ * computes nothing; a table entry outside the pool sets PKV_DEVERR_BLOCK_ID (that
+ * sequence's rows are then unspecified). */
+int pkv_paged_prefill(pkv_pool *pool, const void *q, const void *key_cache, const void *value_cache,
+                      const int32_t *block_tables, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
+                      int32_t total_q, float scale, const void *plan, int32_t grid, void *out, void *stream);
 
 /* Bytes of the fixed device scratch behind pkv_paged_attention_decode_noalloc. */
 #define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)

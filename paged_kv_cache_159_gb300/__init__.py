@@ -19,6 +19,8 @@ Names follow the C ABI without the ``pkv_`` prefix:
 * ``Pool.cow_prepare`` and ``copy_blocks`` -- copy-on-write of shared blocks before an append.
 * ``block_hashes``, ``Pool.prefix_lookup / prefix_insert / prefix_evict / prefix_clear`` --
   automatic prefix caching on the host.
+* ``slot_mapping_chunks``, ``prefill_plan``, ``paged_prefill`` -- prefill and chunked
+  prefill on the tcgen05 tensor cores (plan on the host once per batch, run per layer).
 * ``decode_workspace_bytes``, ``probe_copy``, ``device_sm_count``.
 """
 from __future__ import annotations
@@ -43,7 +45,8 @@ EXPORTED = (
     "pkv_pool_attach_device", "pkv_kv_append", "pkv_pool_layer_bytes", "pkv_kv_append_layers",
     "pkv_decode_step_layers", "pkv_cow_prepare", "pkv_copy_blocks",
     "pkv_block_hashes", "pkv_prefix_lookup", "pkv_prefix_insert", "pkv_prefix_evict",
-    "pkv_prefix_clear", "pkv_prefix_cached_blocks",
+    "pkv_prefix_clear", "pkv_prefix_cached_blocks", "pkv_slot_mapping_chunks",
+    "pkv_prefill_plan_bytes", "pkv_prefill_plan", "pkv_paged_prefill",
     "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
     "pkv_paged_attention_decode_ex", "pkv_decode_step", "pkv_paged_attention_decode_noalloc",
     "pkv_get_device_error", "pkv_probe_copy",
@@ -107,6 +110,12 @@ def lib():
             "pkv_prefix_evict": (ctypes.c_int, [_P, _I32, _P, ctypes.POINTER(_I32)]),
             "pkv_prefix_clear": (ctypes.c_int, [_P]),
             "pkv_prefix_cached_blocks": (ctypes.c_int, [_P, ctypes.POINTER(_I32)]),
+            "pkv_slot_mapping_chunks": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _P]),
+            "pkv_prefill_plan_bytes": (ctypes.c_size_t, [_P, _I32, _I32, _I32]),
+            "pkv_prefill_plan": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _P, ctypes.c_size_t,
+                                                ctypes.POINTER(_I32)]),
+            "pkv_paged_prefill": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
+                                                 ctypes.c_float, _P, _I32, _P, _P]),
             "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32, _I32, ctypes.POINTER(decode_opts)]),
             "pkv_paged_attention_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
                                                           ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
@@ -326,6 +335,46 @@ def block_hashes(tokens, salt: int = 0, block_size: int = BLOCK_SIZE) -> np.ndar
     _check(lib().pkv_block_hashes(_np_ptr(tokens), tokens.size, int(block_size),
                                   int(salt) & (2**64 - 1), _np_ptr(out)), "block_hashes")
     return out[:tokens.size // int(block_size)]
+
+
+def slot_mapping_chunks(tables, seq_lens, cu_q, block_size: int = BLOCK_SIZE) -> np.ndarray:
+    """Slots of every prompt-chunk row: row cu_q[b] + i is position seq_lens[b] - P_b + i."""
+    tables = np.ascontiguousarray(tables, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    cu_q = np.ascontiguousarray(cu_q, dtype=np.int32)
+    out = np.empty(max(1, int(cu_q[-1])), dtype=np.int64)
+    _check(lib().pkv_slot_mapping_chunks(_np_ptr(tables), _np_ptr(seq_lens), _np_ptr(cu_q), seq_lens.size,
+                                         tables.shape[1], int(block_size), _np_ptr(out)),
+           "slot_mapping_chunks")
+    return out[:int(cu_q[-1])]
+
+
+def prefill_plan(pool: Pool, cu_q, seq_lens, num_q_heads: int, max_blocks: int):
+    """Host plan of a prefill batch (pkv_prefill_plan): (uint8 plan bytes, grid).  Copy the
+    bytes to the device (e.g. torch.from_numpy(plan).cuda()) for paged_prefill."""
+    cu_q = np.ascontiguousarray(cu_q, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    nbytes = int(lib().pkv_prefill_plan_bytes(pool.handle, seq_lens.size, int(num_q_heads), int(cu_q[-1])))
+    if nbytes == 0:
+        raise PkvError(ERR_INVALID, "prefill_plan_bytes")
+    buf = np.zeros(nbytes, dtype=np.uint8)
+    grid = _I32()
+    _check(lib().pkv_prefill_plan(pool.handle, _np_ptr(cu_q), _np_ptr(seq_lens), seq_lens.size,
+                                  int(num_q_heads), int(max_blocks), _np_ptr(buf), nbytes, ctypes.byref(grid)),
+           "prefill_plan")
+    return buf, grid.value
+
+
+def paged_prefill(pool: Pool, q, key_cache, value_cache, block_tables, scale: float, plan, grid: int,
+                  out, stream=None):
+    """q/out: bf16 CUDA [T, Hq, D]; block_tables int32 CUDA [B, MB]; plan: the device copy
+    (uint8 CUDA tensor) of prefill_plan's bytes, grid its grid."""
+    T, Hq, _ = q.shape
+    _check(lib().pkv_paged_prefill(pool.handle, _dev_ptr(q, "q"), _dev_ptr(key_cache, "key_cache"),
+                                   _dev_ptr(value_cache, "value_cache"), _dev_ptr(block_tables, "block_tables"),
+                                   int(block_tables.shape[0]), int(Hq), int(block_tables.shape[1]), int(T),
+                                   float(scale), _dev_ptr(plan, "plan"), int(grid), _dev_ptr(out, "out"),
+                                   _stream_ptr(stream)), "paged_prefill")
 
 
 def kv_append(pool: Pool, k, v, slots, key_cache, value_cache, stream=None):

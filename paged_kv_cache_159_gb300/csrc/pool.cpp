@@ -273,6 +273,29 @@ int pkv_cow_prepare(pkv_pool *pool, int32_t *tables, const int32_t *seq_lens, in
     return PKV_OK;
 }
 
+int pkv_slot_mapping_chunks(const int32_t *tables, const int32_t *seq_lens, const int32_t *cu_q,
+                            int32_t batch, int32_t max_blocks, int32_t block_size, int64_t *slots_out)
+{
+    if (batch < 0 || max_blocks < 1 || block_size < 1) return PKV_ERR_INVALID;
+    if (batch > 0 && (!tables || !seq_lens || !cu_q || !slots_out)) return PKV_ERR_INVALID;
+    if (batch > 0 && cu_q[0] != 0) return PKV_ERR_INVALID;
+    for (int32_t b = 0; b < batch; ++b) {           // validate first
+        const int64_t P = (int64_t)cu_q[b + 1] - cu_q[b], L = seq_lens[b];
+        if (P < 0 || P > L || L < 1 || L > (int64_t)max_blocks * block_size) return PKV_ERR_INVALID;
+        for (int64_t pos = L - P; pos < L; ++pos)
+            if (tables[(int64_t)b * max_blocks + pos / block_size] < 0) return PKV_ERR_INVALID;
+    }
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t P = (int64_t)cu_q[b + 1] - cu_q[b], L = seq_lens[b];
+        int64_t *out = slots_out + cu_q[b];
+        for (int64_t i = 0; i < P; ++i) {
+            const int64_t pos = L - P + i;
+            out[i] = (int64_t)tables[(int64_t)b * max_blocks + pos / block_size] * block_size + pos % block_size;
+        }
+    }
+    return PKV_OK;
+}
+
 int pkv_slot_mapping(const int32_t *tables, const int32_t *seq_lens, int32_t batch,
                      int32_t max_blocks, int32_t block_size, int64_t *slots_out)
 {

@@ -1,0 +1,587 @@
+// prefill.cu -- paged prefill and chunked-prefill attention on the tcgen05 tensor cores.
+//
+// What is computed (the pages' definitions):
+//   * "理解 KV Cache" (steinslab.io) §1.2: Attention(Q, K, V) = softmax(Q K^T / sqrt(d_k) + M) V
+//     with the causal mask M: position i aggregates positions <= i only.  §2.1: prefill
+//     processes every prompt position at once, a matrix-matrix product bound by compute,
+//     the work tensor cores are made for.
+//   * "KV Cache 与推理优化" (note.yj-dis.top): prefill fills every position of the cache;
+//     sequences packed into one batch need a per-sequence (block-diagonal) causal mask
+//     (pitfalls table); GQA query heads hq = h*g .. h*g+g-1 share KV head h.
+//   A batch packs, per sequence b, a chunk of P_b query rows (rows cu_q[b] .. cu_q[b+1]-1 of
+//   q) whose K/V are already in the paged cache (kv_append) behind C_b = L_b - P_b earlier
+//   positions.  Row cu_q[b] + i is position C_b + i and attends over positions 0 .. C_b + i
+//   of its own sequence, gathered through its block table.  C_b = 0 is a whole-prompt
+//   prefill; C_b > 0 a chunk of a longer prompt (chunked prefill).
+//
+// GB300 design:
+//   * Work unit = (sequence, KV head, query tile).  A tile is 128 rows: TP = 128 / g query
+//     positions times the g query heads of the KV head, so each K/V tile read serves the
+//     whole GQA group.  Rows r = position * g + head; for g that does not divide 128 the last
+//     rows are padding.
+//   * A host plan (pkv_prefill_plan) lists the units and assigns them, heaviest first, to
+//     the CTAs of a persistent one-wave grid (longest-processing-time first).  The same plan
+//     serves every layer of a batch.
+//   * One CTA per SM, 6 warps: warp 0 issues the tiled bulk-tensor (TMA) loads, warp 1
+//     issues the tcgen05.mma instructions, warps 2-5 (one per tensor-memory lane quarter)
+//     run the softmax and the epilogue with one query row per thread.
+//   * Per KV tile of 128 keys (8 paged blocks): S = Q.K^T (M 128, N 128, K D) into tensor
+//     memory; the softmax warps read their row of S, mask (causal, by select), update the
+//     running max and sum (exp2 domain, rescaling the output accumulator only when the max
+//     rises by more than 2^8), write P as bf16 into shared memory; then O += P.V (M 128,
+//     N D, K 128) accumulates in tensor memory.  S of the next tile is issued as soon as
+//     the softmax has read S, so it overlaps the softmax; P.V overlaps the next softmax.
+//   * K and V tiles stream through a 2-stage ring.  Each 16-token block of one KV head is a
+//     contiguous [16, D] tile of the cache, loaded by TMA with a 128-byte swizzle as rows
+//     of the [128 keys, D] operand.  V rows past the last key any query of the unit may see
+//     are zeroed in shared memory before P.V, so whatever the cache holds there (unused
+//     tail slots, NaN included) never meets the tensor core: P is 0 there, but 0 x NaN is
+//     not.
+//   * All waits are bounded (about 1 s, then PKV_DEVERR_TIMEOUT and a bounded drain).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <queue>
+#include <vector>
+
+#include "pkv_internal.h"
+#include "tc_device.cuh"
+
+namespace pkv {
+namespace prefill {
+
+constexpr int BM = 128;            // query rows per tile
+constexpr int BN = 128;            // keys per KV tile
+constexpr int BS = 16;             // tokens per block
+constexpr int NTHREADS = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 softmax + epilogue
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float TAU = 8.0f;        // raise the running max only beyond 2^8
+constexpr uint32_t PLAN_MAGIC = 0x504b5650u;   // "PVKP"
+constexpr uint32_t TMEM_COLS = 256;            // S: 128 columns, O: D columns
+
+// A plan: header, per-CTA unit ranges, units.
+struct PlanHeader { uint32_t magic; int32_t num_units, grid, group, tp, hq, hkv, pad; };
+struct Unit { int32_t b, h, row0, pos0, npos, nkv, kmax, pad; };
+
+__host__ __device__ inline size_t plan_units_offset(int grid)
+{
+    return (sizeof(PlanHeader) + sizeof(int32_t) * (size_t)(grid + 1) + 31) / 32 * 32;
+}
+
+struct Params {
+    const int32_t *tables;
+    const uint8_t *plan;
+    uint16_t *out;
+    uint32_t *err;
+    int MB, Hq, Hkv, group, TP, num_blocks, grid;
+    float score_scale;           // scale * log2(e)
+};
+
+template <int D>
+struct Smem {
+    static constexpr int H = D / 64;                  // 64-column atom columns per row
+    static constexpr int Q = 0;                       // H x [128][64]
+    static constexpr int P = Q + H * 16384;           // 2 x [128][64] (128 keys)
+    static constexpr int KV = P + 2 * 16384;          // 2 stages x (K, V) x H x [128][64]
+    static constexpr int V_OFF = H * 16384;
+    static constexpr int STAGE = 2 * H * 16384;
+    static constexpr int BAR = KV + 2 * STAGE;
+    static constexpr int TOTAL = BAR + 128;
+    static constexpr int ALLOC = TOTAL + 1024;        // alignment slack
+};
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+               const __grid_constant__ CUtensorMap vmap, const Params p)
+{
+    using L = Smem<D>;
+    constexpr int H = L::H;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t base = dev::smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t bars = base + L::BAR;
+    const uint32_t q_full = bars, s_full = bars + 24, s_free = bars + 32, p_full = bars + 40,
+                   o_free = bars + 64;
+    auto kv_full = [&](int s) { return bars + 8 + 8 * s; };
+    auto o_done = [&](int s) { return bars + 48 + 8 * s; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 72);
+
+    const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(p.plan);
+    const int32_t *cta_off = reinterpret_cast<const int32_t *>(p.plan + sizeof(PlanHeader));
+    const Unit *units = reinterpret_cast<const Unit *>(p.plan + plan_units_offset(p.grid));
+    if (hdr->magic != PLAN_MAGIC || hdr->grid != p.grid || hdr->group != p.group || hdr->hq != p.Hq ||
+        hdr->hkv != p.Hkv || hdr->tp != p.TP) {
+        if (tid == 0 && blockIdx.x == 0) dev::flag_error(p.err, PKV_DEVERR_PLAN);
+        return;
+    }
+    const int u0 = cta_off[blockIdx.x], u1 = cta_off[blockIdx.x + 1];
+
+    if (tid == 0) {
+        dev::mbar_init(q_full, 1);
+        dev::mbar_init(kv_full(0), 1);
+        dev::mbar_init(kv_full(1), 1);
+        dev::mbar_init(s_full, 1);
+        dev::mbar_init(s_free, 4);
+        dev::mbar_init(p_full, 4);
+        dev::mbar_init(o_done(0), 1);
+        dev::mbar_init(o_done(1), 1);
+        dev::mbar_init(o_free, 4);
+        dev::fence_barrier_init();
+    }
+    if (warp == 1) tc::tmem_alloc(dev::smem_u32(tmem_slot), TMEM_COLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tS = *tmem_slot, tO = tS + 128;
+
+    if (warp == 0) {
+        // ============================ TMA producer ============================
+        if (lane == 0) {
+            int J = 0, uq = 0, q_arms = 0, kv_arms[2] = {0, 0};
+            bool ok = true;
+            for (int u = u0; u < u1 && ok; ++u, ++uq) {
+                const Unit un = units[u];
+                // the previous unit's MMAs are done with Q once its last P.V completed
+                if (uq > 0 && !dev::mbar_wait_bounded(o_done((J - 1) & 1), ((J - 1) >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                dev::mbar_arrive_expect_tx(q_full, (uint32_t)(H * 64 * p.group * p.TP * 2));
+                ++q_arms;
+                for (int hf = 0; hf < H; ++hf)
+                    tc::tma_load_3d(base + L::Q + hf * 16384, &qmap, hf * 64, un.h * p.group, un.row0, q_full);
+                const int nblk = un.kmax / BS + 1;               // blocks holding keys 0..kmax
+                for (int j = 0; j < un.nkv; ++j, ++J) {
+                    const int s = J & 1;
+                    if (J >= 2 && !dev::mbar_wait_bounded(o_done(s), ((J - 2) >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t kst = base + L::KV + s * L::STAGE, vst = kst + L::V_OFF;
+                    int ids[8], n = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int blk = j * 8 + i;
+                        int id = -1;
+                        if (blk < nblk && blk < p.MB) {
+                            id = __ldg(p.tables + (size_t)un.b * p.MB + blk);
+                            if (id < 0 || id >= p.num_blocks) {
+                                dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+                                id = -1;
+                            }
+                        }
+                        ids[i] = id;
+                        n += id >= 0;
+                    }
+                    dev::mbar_arrive_expect_tx(kv_full(s), (uint32_t)(n * 2 * H * 2048));
+                    ++kv_arms[s];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (ids[i] < 0) continue;
+                        const int z = ids[i] * p.Hkv + un.h;
+                        for (int hf = 0; hf < H; ++hf) {
+                            tc::tma_load_3d(kst + hf * 16384 + i * 2048, &kmap, hf * 64, 0, z, kv_full(s));
+                            tc::tma_load_3d(vst + hf * 16384 + i * 2048, &vmap, hf * 64, 0, z, kv_full(s));
+                        }
+                    }
+                }
+            }
+            if (!ok) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+            // no copy may land after the CTA has left: wait (bounded) for the last of each
+            if (q_arms) (void)dev::mbar_wait_bounded(q_full, (q_arms - 1) & 1);
+            for (int s = 0; s < 2; ++s)
+                if (kv_arms[s]) (void)dev::mbar_wait_bounded(kv_full(s), (kv_arms[s] - 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ============================ MMA issuer ============================
+        if (lane == 0) {
+            constexpr uint32_t IDS = tc::idesc_bf16(BM, BN, 0);   // S = Q K^T
+            constexpr uint32_t IDO = tc::idesc_bf16(BM, D, 1);    // O += P V, V MN-major
+            int J = 0, uq = 0;
+            bool ok = true;
+            auto issue_s = [&](int Jn) -> bool {
+                if (!dev::mbar_wait_bounded(kv_full(Jn & 1), (Jn >> 1) & 1)) return false;
+                if (Jn >= 1 && !dev::mbar_wait_bounded(s_free, (Jn - 1) & 1)) return false;
+                tc::fence_after_sync();
+                const uint32_t kst = base + L::KV + (Jn & 1) * L::STAGE;
+#pragma unroll
+                for (int k = 0; k < 4 * H; ++k) {
+                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                    tc::mma_bf16(tS, tc::smem_desc_sw128(base + L::Q + off, 16, 1024),
+                                 tc::smem_desc_sw128(kst + off, 16, 1024), IDS, k > 0);
+                }
+                tc::commit(s_full);
+                return true;
+            };
+            for (int u = u0; u < u1 && ok; ++u, ++uq) {
+                const Unit un = units[u];
+                if (!dev::mbar_wait_bounded(q_full, uq & 1) || !issue_s(J)) {
+                    ok = false;
+                    break;
+                }
+                for (int j = 0; j < un.nkv; ++j) {
+                    const int Jc = J + j;
+                    if (j + 1 < un.nkv && !issue_s(Jc + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!dev::mbar_wait_bounded(p_full, Jc & 1) ||
+                        (j == 0 && uq > 0 && !dev::mbar_wait_bounded(o_free, (uq - 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t vst = base + L::KV + (Jc & 1) * L::STAGE + L::V_OFF;
+#pragma unroll
+                    for (int k = 0; k < BN / 16; ++k) {
+                        const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
+                        tc::mma_bf16(tO, tc::smem_desc_sw128(base + L::P + aoff, 16, 1024),
+                                     tc::smem_desc_sw128(vst + k * 2048, 16384, 1024), IDO, (j > 0) || (k > 0));
+                    }
+                    tc::commit(o_done(Jc & 1));
+                }
+                J += un.nkv;
+            }
+            if (!ok) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+        }
+    } else {
+        // ============================ softmax + epilogue ============================
+        const int q4 = warp & 3;                           // this warp's tensor-memory lane quarter
+        const int r = 32 * q4 + lane;                      // its row of the tile
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        const int st = tid - 64;                           // 0..127 over the four warps
+        int J = 0;
+        bool ok = true;
+        for (int u = u0; u < u1 && ok; ++u) {
+            const Unit un = units[u];
+            const int pl = r / p.group, hh = r - pl * p.group;
+            const bool valid = r < p.TP * p.group && pl < un.npos;
+            const int qpos = un.pos0 + pl;                 // keys 0..qpos are visible
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < un.nkv; ++j, ++J) {
+                if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(s_full, J & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                float x[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(tS + lane_off + 32 * c, v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(v[i]);
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(s_free);     // S may be overwritten now
+                const int kb = j * BN;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    const bool vis = valid && kb + c <= qpos;
+                    x[c] = vis ? x[c] * p.score_scale : -INFINITY;
+                    mx = fmaxf(mx, x[c]);
+                }
+                // raise the running max (and rescale O, which holds earlier tiles) only when
+                // it grows by more than 2^TAU; warp-uniform because tensor-memory access is
+                const bool raise = mx > m + TAU;
+                const bool rescale = raise && m != -INFINITY;
+                bool waited = false;
+                if (__any_sync(dev::FULL, rescale)) {
+                    if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(o_done((J - 1) & 1), ((J - 1) >> 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    waited = true;
+                    tc::fence_after_sync();
+                    const float f = rescale ? dev::fast_exp2(m - mx) : 1.f;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        tc::tmem_ld32(tO + lane_off + 32 * c, v);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                        tc::tmem_st32(tO + lane_off + 32 * c, v);
+                    }
+                    tc::tmem_wait_st();
+                    l *= f;
+                }
+                if (raise) m = mx;
+                // P = exp2(x - m) as bf16 into row r of the P tile (once P.V of the previous
+                // tile has finished reading it)
+                if (!waited && J >= 1 &&
+                    !__all_sync(dev::FULL, dev::mbar_wait_bounded(o_done((J - 1) & 1), ((J - 1) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const float mm = m == -INFINITY ? 0.f : m;
+                float psum = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < BN / 8; ++cc) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = dev::fast_exp2(x[8 * cc + 2 * e] - mm);
+                        const float b2 = dev::fast_exp2(x[8 * cc + 2 * e + 1] - mm);
+                        psum += a + b2;
+                        w[e] = dev::pack_bf16x2(a, b2);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + L::P + (cc >> 3) * 16384 + tc::sw128_offset(r, (cc & 7) * 8)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                l += psum;
+                // last tile: zero the V rows past the unit's last visible key
+                if (j == un.nkv - 1) {
+                    const int first = un.kmax + 1 - kb;
+                    if (first < BN) {
+                        if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(kv_full(J & 1), (J >> 1) & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *vst = sm + L::KV + (J & 1) * L::STAGE + L::V_OFF;
+                        const int chunks = (BN - first) * 8;     // 16-byte chunks per atom column
+                        for (int hf = 0; hf < H; ++hf)
+                            for (int c = st; c < chunks; c += 128)
+                                *reinterpret_cast<uint4 *>(vst + hf * 16384 + first * 128 + c * 16) =
+                                    make_uint4(0, 0, 0, 0);
+                    }
+                }
+                dev::fence_proxy_async_smem();               // P and zeroed rows -> tensor core
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(p_full);
+            }
+            if (!ok) break;
+            // epilogue: O / l of this row, bf16, to out[row0 + pl][h*g + hh]
+            if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(o_done((J - 1) & 1), ((J - 1) >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint16_t *dst = p.out + ((size_t)(un.row0 + pl) * p.Hq + (size_t)un.h * p.group + hh) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tc::tmem_ld32(tO + lane_off + 32 * c, v);
+                tc::tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            w[t] = dev::pack_bf16x2(__uint_as_float(v[8 * e + 2 * t]) * inv,
+                                                    __uint_as_float(v[8 * e + 2 * t + 1]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * e) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(o_free);
+        }
+        if (!ok && lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tS, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// Host side.
+// ------------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool encode_3d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+               uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2}, strides[2] = {s1, s2};
+    const cuuint32_t box[3] = {b0, b1, b2}, es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+template <int D>
+cudaError_t launch(const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm, const Params &p,
+                   cudaStream_t s)
+{
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::ALLOC);
+    });
+    if (attr != cudaSuccess) return attr;
+    prefill_kernel<D><<<p.grid, NTHREADS, Smem<D>::ALLOC, s>>>(qm, km, vm, p);
+    return cudaGetLastError();
+}
+
+int tile_positions(int group) { return BM / group; }
+
+}  // namespace prefill
+}  // namespace pkv
+
+extern "C" size_t pkv_prefill_plan_bytes(const pkv_pool *pool, int32_t batch, int32_t num_q_heads,
+                                         int32_t total_q)
+{
+    using namespace pkv::prefill;
+    if (!pool || batch < 1 || num_q_heads < 1 || total_q < 0 || num_q_heads % pool->desc.num_kv_heads) return 0;
+    const int g = num_q_heads / pool->desc.num_kv_heads;
+    if (g > 16) return 0;
+    const int tp = tile_positions(g);
+    const size_t units = (size_t)pool->desc.num_kv_heads * ((size_t)total_q / tp + batch);
+    const int grid = std::max(1, sm_count());
+    return plan_units_offset(grid) + units * sizeof(Unit);
+}
+
+extern "C" int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const int32_t *seq_lens,
+                                int32_t batch, int32_t num_q_heads, int32_t max_blocks, void *plan_out,
+                                size_t plan_bytes, int32_t *grid_out)
+{
+    using namespace pkv::prefill;
+    if (!pool || !cu_q || !seq_lens || !plan_out || !grid_out || batch < 1 || num_q_heads < 1 || max_blocks < 1)
+        return PKV_ERR_INVALID;
+    const int Hkv = pool->desc.num_kv_heads;
+    if (num_q_heads % Hkv) return PKV_ERR_INVALID;
+    const int g = num_q_heads / Hkv;
+    if (g > 16) return PKV_ERR_INVALID;
+    const int tp = tile_positions(g);
+    if (cu_q[0] != 0) return PKV_ERR_INVALID;
+    std::vector<Unit> units;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t P = (int64_t)cu_q[b + 1] - cu_q[b], L = seq_lens[b];
+        if (P < 0 || L < P || L < 1 || (L + BS - 1) / BS > max_blocks) return PKV_ERR_INVALID;
+        const int64_t C = L - P;
+        for (int64_t qt = 0; qt * tp < P; ++qt) {
+            Unit u;
+            u.b = b;
+            u.row0 = (int32_t)(cu_q[b] + qt * tp);
+            u.pos0 = (int32_t)(C + qt * tp);
+            u.npos = (int32_t)std::min<int64_t>(tp, P - qt * tp);
+            u.kmax = u.pos0 + u.npos - 1;
+            u.nkv = u.kmax / BN + 1;
+            u.pad = 0;
+            for (int h = 0; h < Hkv; ++h) {
+                u.h = h;
+                units.push_back(u);
+            }
+        }
+    }
+    const int sms = sm_count();
+    if (sms < 1) return PKV_ERR_CUDA;
+    const int grid = std::max(1, std::min<int>(sms, (int)units.size()));
+    const size_t need = plan_units_offset(grid) + units.size() * sizeof(Unit);
+    if (need > plan_bytes) return PKV_ERR_INVALID;
+    // longest processing time first: heaviest unit to the least-loaded CTA
+    std::vector<int> order(units.size());
+    for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int a, int b) { return units[(size_t)a].nkv > units[(size_t)b].nkv; });
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int c = 0; c < grid; ++c) heap.push({0, c});
+    std::vector<std::vector<int>> per(grid);
+    for (int i : order) {
+        Load top = heap.top();
+        heap.pop();
+        per[(size_t)top.second].push_back(i);
+        top.first += units[(size_t)i].nkv + 2;            // + Q load and epilogue
+        heap.push(top);
+    }
+    uint8_t *out = static_cast<uint8_t *>(plan_out);
+    PlanHeader hdr{PLAN_MAGIC, (int32_t)units.size(), grid, g, tp, num_q_heads, Hkv, 0};
+    std::memcpy(out, &hdr, sizeof(hdr));
+    int32_t *off = reinterpret_cast<int32_t *>(out + sizeof(PlanHeader));
+    Unit *dst = reinterpret_cast<Unit *>(out + plan_units_offset(grid));
+    int32_t n = 0;
+    for (int c = 0; c < grid; ++c) {
+        off[c] = n;
+        for (int i : per[(size_t)c]) dst[n++] = units[(size_t)i];
+    }
+    off[grid] = n;
+    *grid_out = grid;
+    return PKV_OK;
+}
+
+extern "C" int pkv_paged_prefill(pkv_pool *pool, const void *q, const void *key_cache, const void *value_cache,
+                                 const int32_t *block_tables, int32_t batch, int32_t num_q_heads,
+                                 int32_t max_blocks, int32_t total_q, float scale, const void *plan,
+                                 int32_t grid, void *out, void *stream)
+{
+    using namespace pkv::prefill;
+    int st = pkv::check_attached(pool);
+    if (st != PKV_OK) return st;
+    const pkv_pool_desc &d = pool->desc;
+    if (d.kv_dtype != PKV_KV_BF16) return PKV_ERR_INVALID;       // bf16 pools only
+    if (batch < 1 || num_q_heads < 1 || max_blocks < 1 || total_q < 0 || grid < 1 || !std::isfinite(scale))
+        return PKV_ERR_INVALID;
+    if (total_q == 0) return PKV_OK;
+    if (!q || !key_cache || !value_cache || !block_tables || !plan || !out) return PKV_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(key_cache) & 15u) ||
+        (reinterpret_cast<uintptr_t>(value_cache) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u) ||
+        (reinterpret_cast<uintptr_t>(plan) & 31u))
+        return PKV_ERR_INVALID;
+    if (num_q_heads % d.num_kv_heads) return PKV_ERR_INVALID;
+    const int g = num_q_heads / d.num_kv_heads;
+    if (g > 16) return PKV_ERR_INVALID;
+    const int tp = tile_positions(g);
+    const int D = d.head_dim;
+    CUtensorMap qm, km, vm;
+    const uint64_t rows = (uint64_t)d.num_blocks * d.num_kv_heads;
+    if (!encode_3d(&qm, q, D, num_q_heads, total_q, (uint64_t)D * 2, (uint64_t)num_q_heads * D * 2, 64, g, tp) ||
+        !encode_3d(&km, key_cache, D, BS, rows, (uint64_t)D * 2, (uint64_t)BS * D * 2, 64, BS, 1) ||
+        !encode_3d(&vm, value_cache, D, BS, rows, (uint64_t)D * 2, (uint64_t)BS * D * 2, 64, BS, 1))
+        return PKV_ERR_CUDA;
+    Params p;
+    p.tables = block_tables;
+    p.plan = static_cast<const uint8_t *>(plan);
+    p.out = static_cast<uint16_t *>(out);
+    p.err = pool->d_err;
+    p.MB = max_blocks;
+    p.Hq = num_q_heads;
+    p.Hkv = d.num_kv_heads;
+    p.group = g;
+    p.TP = tp;
+    p.num_blocks = d.num_blocks;
+    p.grid = grid;
+    p.score_scale = scale * LOG2E;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = D == 128 ? launch<128>(qm, km, vm, p, s) : launch<64>(qm, km, vm, p, s);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

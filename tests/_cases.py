@@ -287,3 +287,83 @@ def gpu_layers(c: LayerCase, append: bool, opts=None):
     counters = ws[:nl * B * c.w.num_kv_heads * 4].view(torch.int32)
     assert int(torch.count_nonzero(counters)) == 0, "split counters not returned to zero"
     return out
+
+
+# ------------------------------------------------------------------------------------
+# Prefill cases: each sequence's context history already in the pool, its chunk's K/V
+# appended by kv_append at the chunk's slots, then causal attention of the chunk's rows.
+# ------------------------------------------------------------------------------------
+@dataclasses.dataclass
+class PrefillCase:
+    w: "workloads.PrefillWorkload"
+    d: "workloads.PrefillDraw"
+    tables: np.ndarray
+    slots: np.ndarray            # int64 [T] chunk slots (oracle's addressing)
+    pool: "pkv.Pool"
+    key_cache: torch.Tensor
+    value_cache: torch.Tensor
+    key_host: np.ndarray
+    value_host: np.ndarray
+
+
+def build_prefill(name: str, device="cuda", overrides=None) -> PrefillCase:
+    w = workloads.PREFILL_WORKLOADS[name]
+    if overrides:
+        w = dataclasses.replace(w, **overrides)
+    d = workloads.draw_prefill(w, device)
+    alloc = oracle.BlockAllocator(d.num_blocks, d.free_order)
+    tables = oracle.build_block_tables(alloc, d.seq_lens, d.max_blocks, 16)
+    slots = np.array([oracle.slot_of(tables[b], pos, 16)[3]
+                      for b in range(w.batch)
+                      for pos in range(int(d.seq_lens[b] - d.chunk_lens[b]), int(d.seq_lens[b]))],
+                     dtype=np.int64)
+    live = torch.from_numpy(oracle.live_positions(tables, d.seq_lens, d.num_blocks)).to(device)
+    kc, vc = d.key_cache, d.value_cache
+    nan = torch.tensor(NAN16, dtype=torch.int16, device=device).view(torch.bfloat16)
+    dead = ~live
+    kc[dead[:, None, :, None].expand_as(kc)] = nan
+    vc[dead[:, None, :, None].expand_as(vc)] = nan
+    sd = torch.from_numpy(slots).to(device)                    # the chunk's slots start as NaN
+    kc[sd // 16, :, sd % 16, :] = nan
+    vc[sd // 16, :, sd % 16, :] = nan
+    pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim, free_order=d.free_order)
+    pool.attach_device(torch.cuda.current_device())
+    return PrefillCase(w, d, tables, slots, pool, kc, vc, workloads.bf16_bits(kc), workloads.bf16_bits(vc))
+
+
+def prefill_append(c: PrefillCase):
+    """The chunk's K/V into the pools: the library on the GPU, the oracle on its host copy."""
+    slots = pkv.slot_mapping_chunks(c.tables, c.d.seq_lens, c.d.cu_q)
+    np.testing.assert_array_equal(slots, c.slots)
+    pkv.kv_append(c.pool, c.d.k_chunk, c.d.v_chunk, torch.from_numpy(slots).cuda(), c.key_cache, c.value_cache)
+    assert oracle.kv_append(workloads.bf16_bits(c.d.k_chunk), workloads.bf16_bits(c.d.v_chunk), c.slots,
+                            c.key_host, c.value_host) == 0
+
+
+def gpu_prefill(c: PrefillCase):
+    plan, grid = pkv.prefill_plan(c.pool, c.d.cu_q, c.d.seq_lens, c.w.num_q_heads, c.tables.shape[1])
+    out = torch.full_like(c.d.q, float("nan"))
+    pkv.paged_prefill(c.pool, c.d.q, c.key_cache, c.value_cache, torch.from_numpy(c.tables).cuda(),
+                      c.w.scale, torch.from_numpy(plan).cuda(), grid, out)
+    st, bits = c.pool.get_device_error()
+    assert st == pkv.OK and bits == 0, (st, bits)
+    return out
+
+
+def oracle_prefill_rows(c: PrefillCase, rows=None, threads=None):
+    """The oracle's causal attention for packed rows (all rows by default): row cu_q[b] + i
+    is position L_b - P_b + i, i.e. a decode query of length position + 1."""
+    if rows is None:
+        st, out = oracle.paged_prefill(workloads.bf16_bits(c.d.q), c.key_host, c.value_host, c.tables,
+                                       c.d.seq_lens, c.d.cu_q, c.w.scale, c.w.num_kv_heads,
+                                       num_threads=threads or oracle.max_threads())
+        assert st == 0
+        return out
+    rows = np.asarray(rows, dtype=np.int64)
+    seq = np.searchsorted(c.d.cu_q, rows, side="right") - 1
+    lens = (c.d.seq_lens[seq] - c.d.chunk_lens[seq] + (rows - c.d.cu_q[seq]) + 1).astype(np.int32)
+    st, out = oracle.paged_decode(workloads.bf16_bits(c.d.q)[rows], c.key_host, c.value_host,
+                                  np.ascontiguousarray(c.tables[seq]), lens, c.w.scale, c.w.num_kv_heads,
+                                  num_threads=threads or oracle.max_threads())
+    assert st == 0
+    return out

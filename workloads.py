@@ -188,3 +188,80 @@ def draw(w: Workload, device="cpu", seq_lens=None) -> Draw:
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Host uint16 view of a bf16 tensor's bit patterns."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------------------------------
+# Prefill workloads: per sequence a context of C_b cached positions and a chunk of P_b new
+# positions (C_b = 0: a whole prompt).  The pages' prefill example is a prompt of about
+# 2000 tokens ("理解 KV Cache" §2.1); shapes are the Llama-3-8B layer's.
+# ------------------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class PrefillWorkload:
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    chunk: int                   # P_b for every sequence, or the upper end of U{1..chunk}
+    context: int = 0             # C_b = context for every sequence, or U{0..context}
+    ragged: bool = False         # draw P_b and C_b uniformly instead
+    seed: int = 159100
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.head_dim)))
+
+
+PREFILL_WORKLOADS = {
+    "prefill_tiny": PrefillWorkload("prefill_tiny", 3, 8, 2, 64, chunk=40, context=37,
+                                    ragged=True, seed=159100),
+    "prefill_llama3_8b": PrefillWorkload("prefill_llama3_8b", 8, 32, 8, 128, chunk=2048,
+                                         seed=159101),
+    "chunked_prefill_llama3_8b": PrefillWorkload("chunked_prefill_llama3_8b", 16, 32, 8, 128,
+                                                 chunk=512, context=8192, ragged=False,
+                                                 seed=159102),
+}
+
+
+@dataclasses.dataclass
+class PrefillDraw:
+    w: PrefillWorkload
+    chunk_lens: np.ndarray       # int32 [B]  P_b
+    seq_lens: np.ndarray         # int32 [B]  C_b + P_b
+    cu_q: np.ndarray             # int32 [B+1]
+    num_blocks: int
+    max_blocks: int
+    free_order: np.ndarray
+    q: torch.Tensor              # bf16 [T, Hq, D]
+    key_cache: torch.Tensor      # bf16 [NB, Hkv, 16, D]  (the context's history)
+    value_cache: torch.Tensor
+    k_chunk: torch.Tensor        # bf16 [T, Hkv, D]  (the chunk's rows, appended before attention)
+    v_chunk: torch.Tensor
+
+
+def draw_prefill(w: PrefillWorkload, device="cpu") -> PrefillDraw:
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    if w.ragged:
+        P = rng.integers(1, w.chunk, size=w.batch, endpoint=True)
+        C = rng.integers(0, w.context, size=w.batch, endpoint=True)
+    else:
+        P = np.full(w.batch, w.chunk)
+        C = (rng.integers(0, w.context, size=w.batch, endpoint=True) if w.context
+             else np.zeros(w.batch, dtype=np.int64))
+    P, C = P.astype(np.int32), C.astype(np.int32)
+    L = (C + P).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum(P)]).astype(np.int32)
+    nb = int(sum(_blocks(int(x)) for x in L))
+    mb = int(max(_blocks(int(x)) for x in L))
+    T, Hq, Hkv, D = int(cu[-1]), w.num_q_heads, w.num_kv_heads, w.head_dim
+    s = w.seed * 16
+    rows = max(1, (1 << 24) // (Hkv * BLOCK_SIZE * D))
+    return PrefillDraw(
+        w=w, chunk_lens=P, seq_lens=L, cu_q=cu, num_blocks=nb, max_blocks=mb,
+        free_order=draw_free_order(Workload(w.name, 1, 1, 1, D, "fixed", seed=w.seed), nb),
+        q=randn_bf16((T, Hq, D), s + 1, device),
+        key_cache=randn_bf16((nb, Hkv, BLOCK_SIZE, D), s + 2, device, chunk_rows=rows),
+        value_cache=randn_bf16((nb, Hkv, BLOCK_SIZE, D), s + 3, device, chunk_rows=rows),
+        k_chunk=randn_bf16((T, Hkv, D), s + 4, device),
+        v_chunk=randn_bf16((T, Hkv, D), s + 5, device),
+    )
