@@ -492,12 +492,216 @@ def run_reference(args):
     }
 
 
+# ------------------------------------------------------------------ prefill workloads
+PREFILL_METRIC = "prefill attention TFLOP/s (causal, visible keys only), Llama-3-8B layer shape"
+
+
+def _prefill_flops(d, Hq, D):
+    """Algorithmic FLOPs: every packed row sees positions 0 .. its own, and each visible key
+    costs 2*D for q.K and 2*D for p.V per query head."""
+    vis = 0
+    for b in range(len(d.seq_lens)):
+        P, L = int(d.chunk_lens[b]), int(d.seq_lens[b])
+        C = L - P
+        vis += P * C + P * (P + 1) // 2
+    return 4 * Hq * D * vis
+
+
+def _tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def _prefill_oracle_sample(w, nrows=48, threads=None):
+    """The oracle on a bounded sample: the last nrows rows of the first sequence (the rows
+    with the most visible keys), timed once.  Returns (TFLOP/s, seconds, rows)."""
+    import oracle
+    d = workloads.draw_prefill(w, "cpu")
+    a = oracle.BlockAllocator(d.num_blocks, d.free_order)
+    t = oracle.build_block_tables(a, d.seq_lens, d.max_blocks)
+    kb, vb = workloads.bf16_bits(d.key_cache), workloads.bf16_bits(d.value_cache)
+    P, L = int(d.chunk_lens[0]), int(d.seq_lens[0])
+    nrows = min(nrows, P)
+    pos = np.arange(L - nrows, L)
+    rows = pos - (L - P)
+    q = workloads.bf16_bits(d.q)[rows]
+    threads = threads or os.cpu_count() or 1
+    t0 = time.perf_counter()
+    st, _ = oracle.paged_decode(q, kb, vb, np.repeat(t[:1], nrows, 0), (pos + 1).astype(np.int32), w.scale,
+                                w.num_kv_heads, num_threads=threads)
+    sec = time.perf_counter() - t0
+    flops = 4 * w.num_q_heads * w.head_dim * int((pos + 1).sum())
+    return flops / sec / 1e12, sec, nrows, threads
+
+
+def run_prefill(args, world, rank, local_rank):
+    import torch
+    import paged_kv_cache_159_gb300 as pkv
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workloads.PREFILL_WORKLOADS[args.workload]
+    d = workloads.draw_prefill(w, dev)
+    Hq, Hkv, D = w.num_q_heads, w.num_kv_heads, w.head_dim
+    T = int(d.cu_q[-1])
+    pool = pkv.Pool(d.num_blocks, Hkv, D, free_order=d.free_order)
+    pool.attach_device(local_rank)
+    tables = pool.build_block_tables(d.seq_lens, d.max_blocks)
+    slots = pkv.slot_mapping_chunks(tables, d.seq_lens, d.cu_q)
+    plan_h, grid = pkv.prefill_plan(pool, d.cu_q, d.seq_lens, Hq, d.max_blocks)
+    plan = torch.from_numpy(plan_h).to(dev)
+    bt = torch.from_numpy(tables).to(dev)
+    sm = torch.from_numpy(slots).to(dev)
+    kc, vc = d.key_cache, d.value_cache
+    out = torch.empty_like(d.q)
+    flops = _prefill_flops(d, Hq, D)
+    stream = torch.cuda.Stream(device=dev)
+    flush_buf = torch.ones(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4,
+                           dtype=torch.int32, device=dev)
+    flush_out = torch.empty((), dtype=torch.int64, device=dev)
+
+    def step(s=None):
+        pkv.kv_append(pool, d.k_chunk, d.v_chunk, sm, kc, vc, stream=s)
+        mids_rec(s)
+        pkv.paged_prefill(pool, d.q, kc, vc, bt, w.scale, plan, grid, out, stream=s)
+
+    K, W = args.steps, args.warmup
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    cur = [0]
+
+    def mids_rec(s):
+        mids[cur[0]].record(s)
+
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            cur[0] = i % K
+            torch.sum(flush_buf, dim=0, out=flush_out)
+            step(stream)
+    stream.synchronize()
+    st, bits = pool.get_device_error(stream)
+    if st != pkv.OK:
+        raise RuntimeError("device error in warm-up: %d bits %#x" % (st, bits))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                cur[0] = i
+                torch.sum(flush_buf, dim=0, out=flush_out)
+                starts[i].record(stream)
+                step(stream)
+                ends[i].record(stream)
+        stream.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    total = float(sum(starts[i].elapsed_time(ends[i]) * 1e-3 for i in range(K)))
+    pre_mean = float(sum(mids[i].elapsed_time(ends[i]) * 1e-3 for i in range(K)) / K)
+    st, bits = pool.get_device_error(stream)
+    if st != pkv.OK:
+        raise RuntimeError("device error in the timed region: %d bits %#x" % (st, bits))
+
+    # end to end: the step's inputs from pinned host memory, the output back, every step
+    pin = lambda t: t.detach().cpu().pin_memory()
+    hq, hk, hv, hout = pin(d.q), pin(d.k_chunk), pin(d.v_chunk), torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hbt, hsm, hplan = pin(bt), pin(sm), pin(plan)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hbt, hsm, hplan))
+    d2h = hout.numel() * hout.element_size()
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    e2e_t = []
+    for i in range(max(5, min(K, 100)) + 3):
+        torch.sum(flush_buf, dim=0, out=flush_out)
+        torch.cuda.synchronize()
+        ee[0].record()
+        for dst, src in ((d.q, hq), (d.k_chunk, hk), (d.v_chunk, hv), (bt, hbt), (sm, hsm), (plan, hplan)):
+            dst.copy_(src, non_blocking=True)
+        pkv.kv_append(pool, d.k_chunk, d.v_chunk, sm, kc, vc)
+        pkv.paged_prefill(pool, d.q, kc, vc, bt, w.scale, plan, grid, out)
+        hout.copy_(out, non_blocking=True)
+        ee[1].record()
+        ee[1].synchronize()
+        if i >= 3:
+            e2e_t.append(ee[0].elapsed_time(ee[1]) * 1e-3)
+    e2e_step = float(statistics.median(e2e_t))
+    if world > 1:
+        total, pre_mean, e2e_step = reduce_max_over_ranks([total, pre_mean, e2e_step], dev)
+    peak, peak_src = _tensor_peak()
+    value = world * flops * K / total / 1e12
+    achieved = flops / pre_mean / 1e12
+    res = {
+        "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(total / K * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": "%s: %d sequences, chunk %s, context %s, q heads %d / kv heads %d, head_dim %d, "
+                        "block 16 (%d rows, %d causal key visits)" % (
+                            w.name, w.batch, "U{1..%d}" % w.chunk if w.ragged else w.chunk,
+                            ("U{0..%d}" % w.context) if w.context else "0", Hq, Hkv, D, T,
+                            flops // (4 * Hq * D)),
+            "step": "kv_append of the chunks + paged_prefill (tcgen05), plan made once on the host",
+            "grid": grid, "parallelism": "replicas",
+            "l2": "flushed between steps (read of a 2x L2 buffer)",
+            "timing": "CUDA events around each step on the launch stream; flush outside them",
+        },
+        "query_tokens_per_s": round(world * T * K / total, 1),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_kernel<%d>" % D,
+                     "flops_per_launch": flops, "peak_source": peak_src},
+        "e2e": {"value": round(world * flops / e2e_step / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_step * 1e3, 4)},
+        "gpu_launches": 2 * K,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, sec, nrows, threads = _prefill_oracle_sample(w)
+        res["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": int(threads), "kind": "oracle",
+                               "sample": "the last %d rows of sequence 0, fp64, %.2f s" % (nrows, sec)}
+    return res
+
+
+def run_prefill_reference(args):
+    w = workloads.PREFILL_WORKLOADS[args.workload]
+    t = []
+    for i in range(args.warmup + args.steps):
+        tf, sec, nrows, threads = _prefill_oracle_sample(w, nrows=8)
+        if i >= args.warmup:
+            t.append(sec)
+    total = float(sum(t))
+    d = workloads.draw_prefill(w, "cpu")
+    L = int(d.seq_lens[0])
+    flops = 4 * w.num_q_heads * w.head_dim * sum(range(L - 8 + 1, L + 1))
+    value = flops * args.steps / total / 1e12
+    return {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "parallelism": "host threads",
+                   "sample": "the last 8 rows of sequence 0 per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": "the last 8 rows of sequence 0 per step, %d steps" % args.steps},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.PREFILL_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=64)
@@ -510,7 +714,8 @@ def main():
     world, rank, local_rank = _dist_env()
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            ref = run_prefill_reference if args.workload in workloads.PREFILL_WORKLOADS else run_reference
+            print(json.dumps(ref(args)), flush=True)
         return
     if world > 1:
         import torch
@@ -518,7 +723,8 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        res = run_ours(args, world, rank, local_rank)
+        run = run_prefill if args.workload in workloads.PREFILL_WORKLOADS else run_ours
+        res = run(args, world, rank, local_rank)
         if rank == 0:
             print(json.dumps(res), flush=True)
     finally:

@@ -15,25 +15,27 @@
 //   prefill; C_b > 0 a chunk of a longer prompt (chunked prefill).
 //
 // GB300 design:
-//   * Work unit = (sequence, KV head, query tile).  A tile is 128 rows: TP = 128 / g query
-//     positions times the g query heads of the KV head, so each K/V tile read serves the
-//     whole GQA group.  Rows r = position * g + head; for g that does not divide 128 the last
-//     rows are padding.
+//   * Work unit = (sequence, KV head, 256 query rows): TP = 256 / g query positions times the
+//     g query heads of the KV head, so every K/V tile read serves the whole GQA group and two
+//     128-row q-tiles.  Rows r = position * g + head; for g that does not divide 256 the last
+//     rows are padding.  Two q-tiles per K/V tile halve the K/V bytes per FLOP: with one,
+//     the kernel waited on K/V loads.
 //   * A host plan (pkv_prefill_plan) lists the units and assigns them, heaviest first, to
 //     the CTAs of a persistent one-wave grid (longest-processing-time first).  The same plan
 //     serves every layer of a batch.
-//   * One CTA per SM, 6 warps: warp 0 issues the tiled bulk-tensor (TMA) loads, warp 1
-//     issues the tcgen05.mma instructions, warps 2-5 (one per tensor-memory lane quarter)
-//     run the softmax and the epilogue with one query row per thread.
-//   * Per KV tile of 128 keys (8 paged blocks): S = Q.K^T (M 128, N 128, K D) into tensor
-//     memory; the softmax warps read their row of S, mask (causal, by select), update the
-//     running max and sum (exp2 domain, rescaling the output accumulator only when the max
-//     rises by more than 2^8), write P as bf16 into shared memory; then O += P.V (M 128,
-//     N D, K 128) accumulates in tensor memory.  S of the next tile is issued as soon as
-//     the softmax has read S, so it overlaps the softmax; P.V overlaps the next softmax.
-//   * K and V tiles stream through a 2-stage ring.  Each 16-token block of one KV head is a
+//   * One CTA per SM, 10 warps: warp 0 issues the tiled bulk-tensor (TMA) loads, warp 1 the
+//     tcgen05.mma instructions; warps 2-5 run the softmax and epilogue of q-tile 0, warps 6-9
+//     of q-tile 1, one query row per thread.
+//   * Per K/V tile of 64 keys (4 paged blocks): S = Q.K^T (M 128, N 64, K D) per q-tile into
+//     tensor memory (double-buffered, so the next S is computed while the softmax reads
+//     this one); the softmax masks (causal, by select), updates the running max and sum
+//     (exp2 domain, rescaling the output accumulator only when the max rises by more than
+//     2^8) and writes P as bf16 to shared memory; O += P.V (M 128, N D, K 64) accumulates
+//     in tensor memory.  The MMA warp polls its inputs and issues each S and P.V as soon as
+//     they are ready, so no load ever waits behind another tile's product.
+//   * K and V tiles stream through a 3-stage ring.  Each 16-token block of one KV head is a
 //     contiguous [16, D] tile of the cache, loaded by TMA with a 128-byte swizzle as rows
-//     of the [128 keys, D] operand.  V rows past the last key any query of the unit may see
+//     of the [64 keys, D] operand.  V rows past the last key any query of the unit may see
 //     are zeroed in shared memory before P.V, so whatever the cache holds there (unused
 //     tail slots, NaN included) never meets the tensor core: P is 0 there, but 0 x NaN is
 //     not.
@@ -55,14 +57,15 @@
 namespace pkv {
 namespace prefill {
 
-constexpr int BM = 128;            // query rows per tile
-constexpr int BN = 128;            // keys per KV tile
+constexpr int BM = 128;            // query rows per q-tile (two q-tiles per unit)
+constexpr int BN = 64;             // keys per KV tile (4 blocks)
+constexpr int NSTAGE = 3;          // K/V ring depth
 constexpr int BS = 16;             // tokens per block
-constexpr int NTHREADS = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 softmax + epilogue
+constexpr int NTHREADS = 320;      // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + epilogue
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float TAU = 8.0f;        // raise the running max only beyond 2^8
 constexpr uint32_t PLAN_MAGIC = 0x504b5650u;   // "PVKP"
-constexpr uint32_t TMEM_COLS = 256;            // S: 128 columns, O: D columns
+constexpr uint32_t TMEM_COLS = 512;            // S: 2 buffers x 2 q-tiles x 64, O: 2 x D
 
 // A plan: header, per-CTA unit ranges, units.
 struct PlanHeader { uint32_t magic; int32_t num_units, grid, group, tp, hq, hkv, pad; };
@@ -85,13 +88,15 @@ struct Params {
 template <int D>
 struct Smem {
     static constexpr int H = D / 64;                  // 64-column atom columns per row
-    static constexpr int Q = 0;                       // H x [128][64]
-    static constexpr int P = Q + H * 16384;           // 2 x [128][64] (128 keys)
-    static constexpr int KV = P + 2 * 16384;          // 2 stages x (K, V) x H x [128][64]
-    static constexpr int V_OFF = H * 16384;
-    static constexpr int STAGE = 2 * H * 16384;
-    static constexpr int BAR = KV + 2 * STAGE;
-    static constexpr int TOTAL = BAR + 128;
+    static constexpr int Q = 0;                       // H x [256 rows][64]
+    static constexpr int QHALF = BM * 2 * 128;        // bytes of one atom column of Q (256 rows)
+    static constexpr int P = Q + H * QHALF;           // 2 q-tiles x [128 rows][64 keys]
+    static constexpr int KV = P + 2 * 16384;          // NSTAGE x (K, V) x H x [64 keys][64]
+    static constexpr int KHALF = BN * 128;            // bytes of one atom column of a K or V tile
+    static constexpr int V_OFF = H * KHALF;
+    static constexpr int STAGE = 2 * H * KHALF;
+    static constexpr int BAR = KV + NSTAGE * STAGE;
+    static constexpr int TOTAL = BAR + 256;
     static constexpr int ALLOC = TOTAL + 1024;        // alignment slack
 };
 
@@ -106,12 +111,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint8_t *sm = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = dev::smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // barriers: q_full, kv_full[NSTAGE], s_full[2], s_free[2], p_full[2 q-tiles],
+    // o_done[2 q-tiles][NSTAGE], o_free[2 q-tiles]
     const uint32_t bars = base + L::BAR;
-    const uint32_t q_full = bars, s_full = bars + 24, s_free = bars + 32, p_full = bars + 40,
-                   o_free = bars + 64;
-    auto kv_full = [&](int s) { return bars + 8 + 8 * s; };
-    auto o_done = [&](int s) { return bars + 48 + 8 * s; };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 72);
+    const uint32_t q_full = bars;
+    auto kv_full = [&](int s) { return bars + 8 * (1 + s); };
+    auto s_full = [&](int b) { return bars + 8 * (1 + NSTAGE + b); };
+    auto s_free = [&](int b) { return bars + 8 * (3 + NSTAGE + b); };
+    auto p_full = [&](int w) { return bars + 8 * (5 + NSTAGE + w); };
+    auto o_done = [&](int w, int s) { return bars + 8 * (7 + NSTAGE + w * NSTAGE + s); };
+    auto o_free = [&](int w) { return bars + 8 * (7 + 3 * NSTAGE + w); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (9 + 3 * NSTAGE));
 
     const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(p.plan);
     const int32_t *cta_off = reinterpret_cast<const int32_t *>(p.plan + sizeof(PlanHeader));
@@ -125,50 +135,57 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     if (tid == 0) {
         dev::mbar_init(q_full, 1);
-        dev::mbar_init(kv_full(0), 1);
-        dev::mbar_init(kv_full(1), 1);
-        dev::mbar_init(s_full, 1);
-        dev::mbar_init(s_free, 4);
-        dev::mbar_init(p_full, 4);
-        dev::mbar_init(o_done(0), 1);
-        dev::mbar_init(o_done(1), 1);
-        dev::mbar_init(o_free, 4);
+        for (int s = 0; s < NSTAGE; ++s) dev::mbar_init(kv_full(s), 1);
+        for (int b = 0; b < 2; ++b) {
+            dev::mbar_init(s_full(b), 1);
+            dev::mbar_init(s_free(b), 8);             // every softmax warp has read its S
+            dev::mbar_init(p_full(b), 4);             // the q-tile's four warps wrote P
+            dev::mbar_init(o_free(b), 4);
+            for (int s = 0; s < NSTAGE; ++s) dev::mbar_init(o_done(b, s), 1);
+        }
         dev::fence_barrier_init();
     }
     if (warp == 1) tc::tmem_alloc(dev::smem_u32(tmem_slot), TMEM_COLS);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tS = *tmem_slot, tO = tS + 128;
+    const uint32_t tmem = *tmem_slot;
+    // tensor memory: S[buffer][q-tile] at columns (2*buffer + q-tile)*64, O[q-tile] at 256 + q-tile*D
+    auto tS = [&](int b, int w) { return tmem + (uint32_t)((2 * b + w) * BN); };
+    auto tO = [&](int w) { return tmem + 256u + (uint32_t)(w * D); };
 
     if (warp == 0) {
         // ============================ TMA producer ============================
         if (lane == 0) {
-            int J = 0, uq = 0, q_arms = 0, kv_arms[2] = {0, 0};
+            int J = 0, uq = 0, q_arms = 0, kv_arms[NSTAGE] = {};
             bool ok = true;
             for (int u = u0; u < u1 && ok; ++u, ++uq) {
                 const Unit un = units[u];
-                // the previous unit's MMAs are done with Q once its last P.V completed
-                if (uq > 0 && !dev::mbar_wait_bounded(o_done((J - 1) & 1), ((J - 1) >> 1) & 1)) {
-                    ok = false;
-                    break;
+                // the previous unit's MMAs are done with Q once both of its last P.V completed
+                if (uq > 0) {
+                    const int Jl = J - 1;
+                    ok = dev::mbar_wait_bounded(o_done(0, Jl % NSTAGE), (Jl / NSTAGE) & 1) &&
+                         dev::mbar_wait_bounded(o_done(1, Jl % NSTAGE), (Jl / NSTAGE) & 1);
+                    if (!ok) break;
                 }
                 dev::mbar_arrive_expect_tx(q_full, (uint32_t)(H * 64 * p.group * p.TP * 2));
                 ++q_arms;
                 for (int hf = 0; hf < H; ++hf)
-                    tc::tma_load_3d(base + L::Q + hf * 16384, &qmap, hf * 64, un.h * p.group, un.row0, q_full);
+                    tc::tma_load_3d(base + L::Q + hf * L::QHALF, &qmap, hf * 64, un.h * p.group, un.row0, q_full);
                 const int nblk = un.kmax / BS + 1;               // blocks holding keys 0..kmax
                 for (int j = 0; j < un.nkv; ++j, ++J) {
-                    const int s = J & 1;
-                    if (J >= 2 && !dev::mbar_wait_bounded(o_done(s), ((J - 2) >> 1) & 1)) {
-                        ok = false;
-                        break;
+                    const int s = J % NSTAGE;
+                    if (J >= NSTAGE) {                           // both P.V of the stage's last tile
+                        const int Jo = J - NSTAGE;
+                        ok = dev::mbar_wait_bounded(o_done(0, s), (Jo / NSTAGE) & 1) &&
+                             dev::mbar_wait_bounded(o_done(1, s), (Jo / NSTAGE) & 1);
+                        if (!ok) break;
                     }
                     const uint32_t kst = base + L::KV + s * L::STAGE, vst = kst + L::V_OFF;
-                    int ids[8], n = 0;
+                    int ids[BN / BS], n = 0;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int blk = j * 8 + i;
+                    for (int i = 0; i < BN / BS; ++i) {
+                        const int blk = j * (BN / BS) + i;
                         int id = -1;
                         if (blk < nblk && blk < p.MB) {
                             id = __ldg(p.tables + (size_t)un.b * p.MB + blk);
@@ -180,15 +197,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         ids[i] = id;
                         n += id >= 0;
                     }
-                    dev::mbar_arrive_expect_tx(kv_full(s), (uint32_t)(n * 2 * H * 2048));
+                    dev::mbar_arrive_expect_tx(kv_full(s), (uint32_t)(n * 2 * H * BS * 128));
                     ++kv_arms[s];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int i = 0; i < BN / BS; ++i) {
                         if (ids[i] < 0) continue;
                         const int z = ids[i] * p.Hkv + un.h;
                         for (int hf = 0; hf < H; ++hf) {
-                            tc::tma_load_3d(kst + hf * 16384 + i * 2048, &kmap, hf * 64, 0, z, kv_full(s));
-                            tc::tma_load_3d(vst + hf * 16384 + i * 2048, &vmap, hf * 64, 0, z, kv_full(s));
+                            tc::tma_load_3d(kst + hf * L::KHALF + i * BS * 128, &kmap, hf * 64, 0, z, kv_full(s));
+                            tc::tma_load_3d(vst + hf * L::KHALF + i * BS * 128, &vmap, hf * 64, 0, z, kv_full(s));
                         }
                     }
                 }
@@ -196,56 +213,83 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             if (!ok) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
             // no copy may land after the CTA has left: wait (bounded) for the last of each
             if (q_arms) (void)dev::mbar_wait_bounded(q_full, (q_arms - 1) & 1);
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < NSTAGE; ++s)
                 if (kv_arms[s]) (void)dev::mbar_wait_bounded(kv_full(s), (kv_arms[s] - 1) & 1);
         }
     } else if (warp == 1) {
         // ============================ MMA issuer ============================
         if (lane == 0) {
-            constexpr uint32_t IDS = tc::idesc_bf16(BM, BN, 0);   // S = Q K^T
-            constexpr uint32_t IDO = tc::idesc_bf16(BM, D, 1);    // O += P V, V MN-major
+            constexpr uint32_t IDS = tc::idesc_bf16(BM, BN, 0);   // S = Q K^T: M 128, N 64 keys
+            constexpr uint32_t IDO = tc::idesc_bf16(BM, D, 1);    // O += P V: M 128, N D, V MN-major
             int J = 0, uq = 0;
             bool ok = true;
-            auto issue_s = [&](int Jn) -> bool {
-                if (!dev::mbar_wait_bounded(kv_full(Jn & 1), (Jn >> 1) & 1)) return false;
-                if (Jn >= 1 && !dev::mbar_wait_bounded(s_free, (Jn - 1) & 1)) return false;
+            auto issue_s = [&](int Jn) {                          // both q-tiles, one commit
                 tc::fence_after_sync();
-                const uint32_t kst = base + L::KV + (Jn & 1) * L::STAGE;
+                const uint32_t kst = base + L::KV + (Jn % NSTAGE) * L::STAGE;
 #pragma unroll
-                for (int k = 0; k < 4 * H; ++k) {
-                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                    tc::mma_bf16(tS, tc::smem_desc_sw128(base + L::Q + off, 16, 1024),
-                                 tc::smem_desc_sw128(kst + off, 16, 1024), IDS, k > 0);
-                }
-                tc::commit(s_full);
-                return true;
+                for (int w = 0; w < 2; ++w)
+#pragma unroll
+                    for (int k = 0; k < 4 * H; ++k) {
+                        const uint32_t hf = k >> 2, kk = (k & 3) * 32;
+                        tc::mma_bf16(tS(Jn & 1, w), tc::smem_desc_sw128(base + L::Q + hf * L::QHALF + w * 16384 + kk, 16, 1024),
+                                     tc::smem_desc_sw128(kst + hf * L::KHALF + kk, 16, 1024), IDS, k > 0);
+                    }
+                tc::commit(s_full(Jn & 1));
+            };
+            auto issue_pv = [&](int Jc, int w, bool first) {
+                tc::fence_after_sync();
+                const uint32_t vst = base + L::KV + (Jc % NSTAGE) * L::STAGE + L::V_OFF;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k)
+                    tc::mma_bf16(tO(w), tc::smem_desc_sw128(base + L::P + w * 16384 + k * 32, 16, 1024),
+                                 tc::smem_desc_sw128(vst + k * 16 * 128, L::KHALF, 1024), IDO, !first || (k > 0));
+                tc::commit(o_done(w, Jc % NSTAGE));
             };
             for (int u = u0; u < u1 && ok; ++u, ++uq) {
                 const Unit un = units[u];
-                if (!dev::mbar_wait_bounded(q_full, uq & 1) || !issue_s(J)) {
+                if (!dev::mbar_wait_bounded(q_full, uq & 1)) {
                     ok = false;
                     break;
                 }
-                for (int j = 0; j < un.nkv; ++j) {
-                    const int Jc = J + j;
-                    if (j + 1 < un.nkv && !issue_s(Jc + 1)) {
-                        ok = false;
-                        break;
+                // S of tile js (both q-tiles; up to two tiles ahead, one per S buffer) and P.V of
+                // tile jp[w] for each q-tile, issued in whichever order their inputs arrive: S
+                // waits for its K tile and for both softmax groups to have read the S buffer's
+                // previous contents; P.V for its group's P (and, first in a unit, for that
+                // group to have read the previous unit's output).  About 1 s without any
+                // progress ends the launch.
+                int js = 0, jp[2] = {0, 0};
+                unsigned long long t_last = dev::globaltimer();
+                unsigned polls = 0;
+                while (jp[0] < un.nkv || jp[1] < un.nkv) {
+                    bool prog = false;
+                    if (js < un.nkv && js < min(jp[0], jp[1]) + 2) {
+                        const int Jn = J + js;
+                        if (dev::mbar_test_wait(kv_full(Jn % NSTAGE), (Jn / NSTAGE) & 1) &&
+                            (Jn < 2 || dev::mbar_test_wait(s_free(Jn & 1), ((Jn - 2) >> 1) & 1))) {
+                            issue_s(Jn);
+                            ++js;
+                            prog = true;
+                        }
                     }
-                    if (!dev::mbar_wait_bounded(p_full, Jc & 1) ||
-                        (j == 0 && uq > 0 && !dev::mbar_wait_bounded(o_free, (uq - 1) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
-                    const uint32_t vst = base + L::KV + (Jc & 1) * L::STAGE + L::V_OFF;
 #pragma unroll
-                    for (int k = 0; k < BN / 16; ++k) {
-                        const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
-                        tc::mma_bf16(tO, tc::smem_desc_sw128(base + L::P + aoff, 16, 1024),
-                                     tc::smem_desc_sw128(vst + k * 2048, 16384, 1024), IDO, (j > 0) || (k > 0));
+                    for (int w = 0; w < 2; ++w) {
+                        if (jp[w] < js) {
+                            const int Jc = J + jp[w];
+                            if (dev::mbar_test_wait(p_full(w), Jc & 1) &&
+                                (jp[w] > 0 || uq == 0 || dev::mbar_test_wait(o_free(w), (uq - 1) & 1))) {
+                                issue_pv(Jc, w, jp[w] == 0);
+                                ++jp[w];
+                                prog = true;
+                            }
+                        }
                     }
-                    tc::commit(o_done(Jc & 1));
+                    if (prog) {
+                        t_last = dev::globaltimer();
+                        polls = 0;
+                    } else if ((++polls & 63u) == 0 && dev::globaltimer() - t_last > dev::WAIT_NS) {
+                        ok = false;
+                        break;
+                    }
                 }
                 J += un.nkv;
             }
@@ -253,143 +297,139 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
     } else {
         // ============================ softmax + epilogue ============================
-        const int q4 = warp & 3;                           // this warp's tensor-memory lane quarter
-        const int r = 32 * q4 + lane;                      // its row of the tile
+        // Warps 2-5 handle q-tile 0 (rows 0-127 of the unit), warps 6-9 q-tile 1 (rows
+        // 128-255).  Warp w % 4 owns tensor-memory lane quarter w % 4: one row per thread,
+        // all 64 keys of every tile, all D output columns.
+        const int w = (warp - 2) >> 2;
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;                      // row within the q-tile
+        const int rg = w * BM + r;                         // row within the unit
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-        const int st = tid - 64;                           // 0..127 over the four warps
+        const int st = (tid - 64) & 127;                   // 0..127 within the group
         int J = 0;
         bool ok = true;
         for (int u = u0; u < u1 && ok; ++u) {
             const Unit un = units[u];
-            const int pl = r / p.group, hh = r - pl * p.group;
-            const bool valid = r < p.TP * p.group && pl < un.npos;
+            const int pl = rg / p.group, hh = rg - pl * p.group;
+            const bool valid = rg < p.TP * p.group && pl < un.npos;
             const int qpos = un.pos0 + pl;                 // keys 0..qpos are visible
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < un.nkv; ++j, ++J) {
-                if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(s_full, J & 1))) {
-                    ok = false;
-                    break;
-                }
+                ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(s_full(J & 1), (J >> 1) & 1));
+                if (!ok) break;
                 tc::fence_after_sync();
                 float x[BN];
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t v[32];
-                    tc::tmem_ld32(tS + lane_off + 32 * c, v);
+                {
+                    uint32_t v0[32], v1[32];
+                    tc::tmem_ld32(tS(J & 1, w) + lane_off, v0);
+                    tc::tmem_ld32(tS(J & 1, w) + lane_off + 32, v1);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(v[i]);
+                    for (int i = 0; i < 32; ++i) {
+                        x[i] = __uint_as_float(v0[i]);
+                        x[32 + i] = __uint_as_float(v1[i]);
+                    }
                 }
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) dev::mbar_arrive(s_free);     // S may be overwritten now
+                if (lane == 0) dev::mbar_arrive(s_free(J & 1));   // the buffer may be reused
                 const int kb = j * BN;
-                float mx = -INFINITY;
+                if (kb + BN - 1 > un.pos0) {                  // the causal diagonal crosses the tile
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const bool vis = valid && kb + c <= qpos;
-                    x[c] = vis ? x[c] * p.score_scale : -INFINITY;
-                    mx = fmaxf(mx, x[c]);
+                    for (int c = 0; c < BN; ++c) x[c] = (valid && kb + c <= qpos) ? x[c] : -INFINITY;
                 }
-                // raise the running max (and rescale O, which holds earlier tiles) only when
-                // it grows by more than 2^TAU; warp-uniform because tensor-memory access is
+                float mx0 = x[0], mx1 = x[1];
+#pragma unroll
+                for (int c = 2; c < BN; c += 2) {
+                    mx0 = fmaxf(mx0, x[c]);
+                    mx1 = fmaxf(mx1, x[c + 1]);
+                }
+                const float mx = fmaxf(mx0, mx1) * p.score_scale;   // scale > 0: max commutes
                 const bool raise = mx > m + TAU;
                 const bool rescale = raise && m != -INFINITY;
-                bool waited = false;
-                if (__any_sync(dev::FULL, rescale)) {
-                    if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(o_done((J - 1) & 1), ((J - 1) >> 1) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    waited = true;
-                    tc::fence_after_sync();
-                    const float f = rescale ? dev::fast_exp2(m - mx) : 1.f;
+                const float f = rescale ? dev::fast_exp2(m - mx) : 1.f;
+                if (raise) m = mx;
+                // P = exp2(x * scale - m) as packed bf16 in registers, before waiting for the
+                // previous tile's P.V, so that the exponentials overlap it
+                const float nm = m == -INFINITY ? 0.f : -m;
+                uint32_t pw[BN / 2];
+                float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
+                for (int e = 0; e < BN / 2; ++e) {
+                    const float a = dev::fast_exp2(fmaf(x[2 * e], p.score_scale, nm));
+                    const float b2 = dev::fast_exp2(fmaf(x[2 * e + 1], p.score_scale, nm));
+                    ps[e & 3] += a + b2;
+                    pw[e] = dev::pack_bf16x2(a, b2);
+                }
+                l = l * f + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+                // this group's previous P.V must be done before P is overwritten or O rescaled
+                if (J >= 1)
+                    ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(o_done(w, (J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1));
+                if (!ok) break;
+#pragma unroll
+                for (int cc = 0; cc < BN / 8; ++cc)
+                    *reinterpret_cast<uint4 *>(sm + L::P + w * 16384 + tc::sw128_offset(r, cc * 8)) =
+                        make_uint4(pw[4 * cc], pw[4 * cc + 1], pw[4 * cc + 2], pw[4 * cc + 3]);
+                if (__any_sync(dev::FULL, rescale)) {
+                    tc::fence_after_sync();
+#pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
-                        tc::tmem_ld32(tO + lane_off + 32 * c, v);
+                        tc::tmem_ld32(tO(w) + lane_off + 32 * c, v);
                         tc::tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-                        tc::tmem_st32(tO + lane_off + 32 * c, v);
+                        for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * f);
+                        tc::tmem_st32(tO(w) + lane_off + 32 * c, v);
                     }
                     tc::tmem_wait_st();
-                    l *= f;
                 }
-                if (raise) m = mx;
-                // P = exp2(x - m) as bf16 into row r of the P tile (once P.V of the previous
-                // tile has finished reading it)
-                if (!waited && J >= 1 &&
-                    !__all_sync(dev::FULL, dev::mbar_wait_bounded(o_done((J - 1) & 1), ((J - 1) >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                const float mm = m == -INFINITY ? 0.f : m;
-                float psum = 0.f;
-#pragma unroll
-                for (int cc = 0; cc < BN / 8; ++cc) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float a = dev::fast_exp2(x[8 * cc + 2 * e] - mm);
-                        const float b2 = dev::fast_exp2(x[8 * cc + 2 * e + 1] - mm);
-                        psum += a + b2;
-                        w[e] = dev::pack_bf16x2(a, b2);
-                    }
-                    *reinterpret_cast<uint4 *>(sm + L::P + (cc >> 3) * 16384 + tc::sw128_offset(r, (cc & 7) * 8)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
-                l += psum;
-                // last tile: zero the V rows past the unit's last visible key
+                // last tile: zero the V rows past the unit's last visible key (both groups do,
+                // each before its own P.V; the stores write the same zeros)
                 if (j == un.nkv - 1) {
                     const int first = un.kmax + 1 - kb;
                     if (first < BN) {
-                        if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(kv_full(J & 1), (J >> 1) & 1))) {
-                            ok = false;
-                            break;
-                        }
-                        uint8_t *vst = sm + L::KV + (J & 1) * L::STAGE + L::V_OFF;
-                        const int chunks = (BN - first) * 8;     // 16-byte chunks per atom column
+                        ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(kv_full(J % NSTAGE), (J / NSTAGE) & 1));
+                        if (!ok) break;
+                        uint8_t *vst = sm + L::KV + (J % NSTAGE) * L::STAGE + L::V_OFF;
+                        const int chunks = (BN - first) * 8;      // 16-byte chunks per atom column
                         for (int hf = 0; hf < H; ++hf)
                             for (int c = st; c < chunks; c += 128)
-                                *reinterpret_cast<uint4 *>(vst + hf * 16384 + first * 128 + c * 16) =
+                                *reinterpret_cast<uint4 *>(vst + hf * L::KHALF + first * 128 + c * 16) =
                                     make_uint4(0, 0, 0, 0);
                     }
                 }
-                dev::fence_proxy_async_smem();               // P and zeroed rows -> tensor core
+                dev::fence_proxy_async_smem();                   // P and zeroed rows -> tensor core
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) dev::mbar_arrive(p_full);
+                if (lane == 0) dev::mbar_arrive(p_full(w));
             }
             if (!ok) break;
             // epilogue: O / l of this row, bf16, to out[row0 + pl][h*g + hh]
-            if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(o_done((J - 1) & 1), ((J - 1) >> 1) & 1))) {
-                ok = false;
-                break;
-            }
+            ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(o_done(w, (J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1));
+            if (!ok) break;
             tc::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint16_t *dst = p.out + ((size_t)(un.row0 + pl) * p.Hq + (size_t)un.h * p.group + hh) * D;
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
-                tc::tmem_ld32(tO + lane_off + 32 * c, v);
+                tc::tmem_ld32(tO(w) + lane_off + 32 * c, v);
                 tc::tmem_wait_ld();
                 if (valid) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        uint32_t w[4];
+                        uint32_t o4[4];
 #pragma unroll
                         for (int t = 0; t < 4; ++t)
-                            w[t] = dev::pack_bf16x2(__uint_as_float(v[8 * e + 2 * t]) * inv,
-                                                    __uint_as_float(v[8 * e + 2 * t + 1]) * inv);
-                        *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * e) = make_uint4(w[0], w[1], w[2], w[3]);
+                            o4[t] = dev::pack_bf16x2(__uint_as_float(v[8 * e + 2 * t]) * inv,
+                                                     __uint_as_float(v[8 * e + 2 * t + 1]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * e) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
                     }
                 }
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) dev::mbar_arrive(o_free);
+            if (lane == 0) dev::mbar_arrive(o_free(w));
         }
         if (!ok && lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
     }
@@ -397,7 +437,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tS, TMEM_COLS);
+        tc::tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -452,7 +492,7 @@ cudaError_t launch(const CUtensorMap &qm, const CUtensorMap &km, const CUtensorM
     return cudaGetLastError();
 }
 
-int tile_positions(int group) { return BM / group; }
+int tile_positions(int group) { return 2 * BM / group; }
 
 }  // namespace prefill
 }  // namespace pkv
