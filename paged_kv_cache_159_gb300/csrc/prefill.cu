@@ -23,18 +23,21 @@
 //   * A host plan (pkv_prefill_plan) lists the units and assigns them, heaviest first, to
 //     the CTAs of a persistent one-wave grid (longest-processing-time first).  The same plan
 //     serves every layer of a batch.
-//   * One CTA per SM, 10 warps: warp 0 issues the tiled bulk-tensor (TMA) loads, warp 1 the
-//     tcgen05.mma instructions; warps 2-5 run the softmax and epilogue of q-tile 0, warps 6-9
-//     of q-tile 1, one query row per thread.
+//   * One CTA per SM, 11 warps: warp 0 issues the tiled bulk-tensor (TMA) loads of Q and K,
+//     warp 10 those of V, warp 1 the tcgen05.mma instructions; warps 2-5 run the softmax and
+//     epilogue of q-tile 0, warps 6-9 of q-tile 1, one query row per thread.
 //   * Per K/V tile of 64 keys (4 paged blocks): S = Q.K^T (M 128, N 64, K D) per q-tile into
 //     tensor memory (double-buffered, so the next S is computed while the softmax reads
 //     this one); the softmax masks (causal, by select), updates the running max and sum
 //     (exp2 domain, rescaling the output accumulator only when the max rises by more than
 //     2^8) and writes P as bf16 to shared memory; O += P.V (M 128, N D, K 64) accumulates
-//     in tensor memory.  The MMA warp polls its inputs and issues each S and P.V as soon as
-//     they are ready, so no load ever waits behind another tile's product.
-//   * K and V tiles stream through a 3-stage ring.  Each 16-token block of one KV head is a
-//     contiguous [16, D] tile of the cache, loaded by TMA with a 128-byte swizzle as rows
+//     in tensor memory.  The MMA warp polls its inputs and issues each P.V and S as soon as
+//     they are ready, P.V first.
+//   * K and V stream through two separate 4-stage rings.  A K tile is free again once S is
+//     computed, a V tile only after P.V: sharing one stage would hold K for a whole tile's
+//     pipeline, and with loads of scattered 4 KiB blocks taking microseconds under load, the
+//     ring, not the tensor core, would set the pace.  Each 16-token block of one KV head is
+//     a contiguous [16, D] tile of the cache, loaded by TMA with a 128-byte swizzle as rows
 //     of the [64 keys, D] operand.  V rows past the last key any query of the unit may see
 //     are zeroed in shared memory before P.V, so whatever the cache holds there (unused
 //     tail slots, NaN included) never meets the tensor core: P is 0 there, but 0 x NaN is
@@ -59,9 +62,9 @@ namespace prefill {
 
 constexpr int BM = 128;            // query rows per q-tile (two q-tiles per unit)
 constexpr int BN = 64;             // keys per KV tile (4 blocks)
-constexpr int NSTAGE = 3;          // K/V ring depth
+constexpr int NSTAGE = 4;          // K/V ring depth
 constexpr int BS = 16;             // tokens per block
-constexpr int NTHREADS = 320;      // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + epilogue
+constexpr int NTHREADS = 352;      // warp 0 Q+K loads, 1 MMA, 2-9 softmax + epilogue, 10 V loads
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float TAU = 8.0f;        // raise the running max only beyond 2^8
 constexpr uint32_t PLAN_MAGIC = 0x504b5650u;   // "PVKP"
@@ -91,11 +94,11 @@ struct Smem {
     static constexpr int Q = 0;                       // H x [256 rows][64]
     static constexpr int QHALF = BM * 2 * 128;        // bytes of one atom column of Q (256 rows)
     static constexpr int P = Q + H * QHALF;           // 2 q-tiles x [128 rows][64 keys]
-    static constexpr int KV = P + 2 * 16384;          // NSTAGE x (K, V) x H x [64 keys][64]
     static constexpr int KHALF = BN * 128;            // bytes of one atom column of a K or V tile
-    static constexpr int V_OFF = H * KHALF;
-    static constexpr int STAGE = 2 * H * KHALF;
-    static constexpr int BAR = KV + NSTAGE * STAGE;
+    static constexpr int KSTAGE = H * KHALF;          // one K (or V) tile
+    static constexpr int K = P + 2 * 16384;           // NSTAGE K tiles
+    static constexpr int V = K + NSTAGE * KSTAGE;     // NSTAGE V tiles
+    static constexpr int BAR = V + NSTAGE * KSTAGE;
     static constexpr int TOTAL = BAR + 256;
     static constexpr int ALLOC = TOTAL + 1024;        // alignment slack
 };
@@ -111,17 +114,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint8_t *sm = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = dev::smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // barriers: q_full, kv_full[NSTAGE], s_full[2], s_free[2], p_full[2 q-tiles],
-    // o_done[2 q-tiles][NSTAGE], o_free[2 q-tiles]
+    // barriers: q_full; k_full, v_full, k_free [NSTAGE]; s_full, s_free [2 S buffers];
+    // p_full [2 q-tiles]; o_done [2 q-tiles][NSTAGE]; o_free [2 q-tiles]
     const uint32_t bars = base + L::BAR;
     const uint32_t q_full = bars;
-    auto kv_full = [&](int s) { return bars + 8 * (1 + s); };
-    auto s_full = [&](int b) { return bars + 8 * (1 + NSTAGE + b); };
-    auto s_free = [&](int b) { return bars + 8 * (3 + NSTAGE + b); };
-    auto p_full = [&](int w) { return bars + 8 * (5 + NSTAGE + w); };
-    auto o_done = [&](int w, int s) { return bars + 8 * (7 + NSTAGE + w * NSTAGE + s); };
-    auto o_free = [&](int w) { return bars + 8 * (7 + 3 * NSTAGE + w); };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (9 + 3 * NSTAGE));
+    auto k_full = [&](int s) { return bars + 8 * (1 + s); };
+    auto v_full = [&](int s) { return bars + 8 * (1 + NSTAGE + s); };
+    auto k_free = [&](int s) { return bars + 8 * (1 + 2 * NSTAGE + s); };
+    auto s_full = [&](int b) { return bars + 8 * (1 + 3 * NSTAGE + b); };
+    auto s_free = [&](int b) { return bars + 8 * (3 + 3 * NSTAGE + b); };
+    auto p_full = [&](int w) { return bars + 8 * (5 + 3 * NSTAGE + w); };
+    auto o_done = [&](int w, int s) { return bars + 8 * (7 + 3 * NSTAGE + w * NSTAGE + s); };
+    auto o_free = [&](int w) { return bars + 8 * (7 + 5 * NSTAGE + w); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (9 + 5 * NSTAGE));
 
     const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(p.plan);
     const int32_t *cta_off = reinterpret_cast<const int32_t *>(p.plan + sizeof(PlanHeader));
@@ -135,7 +140,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     if (tid == 0) {
         dev::mbar_init(q_full, 1);
-        for (int s = 0; s < NSTAGE; ++s) dev::mbar_init(kv_full(s), 1);
+        for (int s = 0; s < NSTAGE; ++s) {
+            dev::mbar_init(k_full(s), 1);
+            dev::mbar_init(v_full(s), 1);
+            dev::mbar_init(k_free(s), 1);
+        }
         for (int b = 0; b < 2; ++b) {
             dev::mbar_init(s_full(b), 1);
             dev::mbar_init(s_free(b), 8);             // every softmax warp has read its S
@@ -154,59 +163,71 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     auto tS = [&](int b, int w) { return tmem + (uint32_t)((2 * b + w) * BN); };
     auto tO = [&](int w) { return tmem + 256u + (uint32_t)(w * D); };
 
-    if (warp == 0) {
-        // ============================ TMA producer ============================
+    // Physical block ids of K/V tile j of a unit (-1: past the unit's last needed block, or
+    // flagged as outside the pool) and how many are valid.
+    auto tile_ids = [&](const Unit &un, int j, int (&ids)[BN / BS]) {
+        const int nblk = un.kmax / BS + 1;                   // blocks holding keys 0..kmax
+        int n = 0;
+#pragma unroll
+        for (int i = 0; i < BN / BS; ++i) {
+            const int blk = j * (BN / BS) + i;
+            int id = -1;
+            if (blk < nblk && blk < p.MB) {
+                id = __ldg(p.tables + (size_t)un.b * p.MB + blk);
+                if (id < 0 || id >= p.num_blocks) {
+                    dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+                    id = -1;
+                }
+            }
+            ids[i] = id;
+            n += id >= 0;
+        }
+        return n;
+    };
+
+    if (warp == 0 || warp == 10) {
+        // ============ TMA producers: warp 0 loads Q and K, warp 10 loads V ============
+        // The two rings are separate because K is free again once S is computed, while V
+        // is needed until P.V: a K stage is held for about a load plus S, not for a whole
+        // tile's pipeline.
         if (lane == 0) {
-            int J = 0, uq = 0, q_arms = 0, kv_arms[NSTAGE] = {};
+            const bool isk = warp == 0;
+            const CUtensorMap *map = isk ? &kmap : &vmap;
+            int J = 0, uq = 0, q_arms = 0, arms[NSTAGE] = {};
             bool ok = true;
             for (int u = u0; u < u1 && ok; ++u, ++uq) {
                 const Unit un = units[u];
-                // the previous unit's MMAs are done with Q once both of its last P.V completed
-                if (uq > 0) {
-                    const int Jl = J - 1;
-                    ok = dev::mbar_wait_bounded(o_done(0, Jl % NSTAGE), (Jl / NSTAGE) & 1) &&
-                         dev::mbar_wait_bounded(o_done(1, Jl % NSTAGE), (Jl / NSTAGE) & 1);
-                    if (!ok) break;
+                if (isk) {
+                    // the previous unit's S products are done with Q once its last S completed
+                    if (uq > 0 && !dev::mbar_wait_bounded(k_free((J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    dev::mbar_arrive_expect_tx(q_full, (uint32_t)(H * 64 * p.group * p.TP * 2));
+                    ++q_arms;
+                    for (int hf = 0; hf < H; ++hf)
+                        tc::tma_load_3d(base + L::Q + hf * L::QHALF, &qmap, hf * 64, un.h * p.group, un.row0, q_full);
                 }
-                dev::mbar_arrive_expect_tx(q_full, (uint32_t)(H * 64 * p.group * p.TP * 2));
-                ++q_arms;
-                for (int hf = 0; hf < H; ++hf)
-                    tc::tma_load_3d(base + L::Q + hf * L::QHALF, &qmap, hf * 64, un.h * p.group, un.row0, q_full);
-                const int nblk = un.kmax / BS + 1;               // blocks holding keys 0..kmax
                 for (int j = 0; j < un.nkv; ++j, ++J) {
                     const int s = J % NSTAGE;
-                    if (J >= NSTAGE) {                           // both P.V of the stage's last tile
-                        const int Jo = J - NSTAGE;
-                        ok = dev::mbar_wait_bounded(o_done(0, s), (Jo / NSTAGE) & 1) &&
-                             dev::mbar_wait_bounded(o_done(1, s), (Jo / NSTAGE) & 1);
+                    if (J >= NSTAGE) {            // the stage's previous tile: S done (K), P.V done (V)
+                        const uint32_t par = ((J - NSTAGE) / NSTAGE) & 1;
+                        ok = isk ? dev::mbar_wait_bounded(k_free(s), par)
+                                 : dev::mbar_wait_bounded(o_done(0, s), par) && dev::mbar_wait_bounded(o_done(1, s), par);
                         if (!ok) break;
                     }
-                    const uint32_t kst = base + L::KV + s * L::STAGE, vst = kst + L::V_OFF;
-                    int ids[BN / BS], n = 0;
-#pragma unroll
-                    for (int i = 0; i < BN / BS; ++i) {
-                        const int blk = j * (BN / BS) + i;
-                        int id = -1;
-                        if (blk < nblk && blk < p.MB) {
-                            id = __ldg(p.tables + (size_t)un.b * p.MB + blk);
-                            if (id < 0 || id >= p.num_blocks) {
-                                dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-                                id = -1;
-                            }
-                        }
-                        ids[i] = id;
-                        n += id >= 0;
-                    }
-                    dev::mbar_arrive_expect_tx(kv_full(s), (uint32_t)(n * 2 * H * BS * 128));
-                    ++kv_arms[s];
+                    int ids[BN / BS];
+                    const int n = tile_ids(un, j, ids);
+                    const uint32_t full = isk ? k_full(s) : v_full(s);
+                    const uint32_t dst = base + (isk ? L::K : L::V) + s * L::KSTAGE;
+                    dev::mbar_arrive_expect_tx(full, (uint32_t)(n * H * BS * 128));
+                    ++arms[s];
 #pragma unroll
                     for (int i = 0; i < BN / BS; ++i) {
                         if (ids[i] < 0) continue;
                         const int z = ids[i] * p.Hkv + un.h;
-                        for (int hf = 0; hf < H; ++hf) {
-                            tc::tma_load_3d(kst + hf * L::KHALF + i * BS * 128, &kmap, hf * 64, 0, z, kv_full(s));
-                            tc::tma_load_3d(vst + hf * L::KHALF + i * BS * 128, &vmap, hf * 64, 0, z, kv_full(s));
-                        }
+                        for (int hf = 0; hf < H; ++hf)
+                            tc::tma_load_3d(dst + hf * L::KHALF + i * BS * 128, map, hf * 64, 0, z, full);
                     }
                 }
             }
@@ -214,7 +235,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             // no copy may land after the CTA has left: wait (bounded) for the last of each
             if (q_arms) (void)dev::mbar_wait_bounded(q_full, (q_arms - 1) & 1);
             for (int s = 0; s < NSTAGE; ++s)
-                if (kv_arms[s]) (void)dev::mbar_wait_bounded(kv_full(s), (kv_arms[s] - 1) & 1);
+                if (arms[s]) (void)dev::mbar_wait_bounded(isk ? k_full(s) : v_full(s), (arms[s] - 1) & 1);
         }
     } else if (warp == 1) {
         // ============================ MMA issuer ============================
@@ -223,9 +244,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             constexpr uint32_t IDO = tc::idesc_bf16(BM, D, 1);    // O += P V: M 128, N D, V MN-major
             int J = 0, uq = 0;
             bool ok = true;
-            auto issue_s = [&](int Jn) {                          // both q-tiles, one commit
+            auto issue_s = [&](int Jn) {                          // both q-tiles
                 tc::fence_after_sync();
-                const uint32_t kst = base + L::KV + (Jn % NSTAGE) * L::STAGE;
+                const uint32_t kst = base + L::K + (Jn % NSTAGE) * L::KSTAGE;
 #pragma unroll
                 for (int w = 0; w < 2; ++w)
 #pragma unroll
@@ -235,10 +256,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                      tc::smem_desc_sw128(kst + hf * L::KHALF + kk, 16, 1024), IDS, k > 0);
                     }
                 tc::commit(s_full(Jn & 1));
+                tc::commit(k_free(Jn % NSTAGE));                 // the K tile may be reloaded
             };
             auto issue_pv = [&](int Jc, int w, bool first) {
                 tc::fence_after_sync();
-                const uint32_t vst = base + L::KV + (Jc % NSTAGE) * L::STAGE + L::V_OFF;
+                const uint32_t vst = base + L::V + (Jc % NSTAGE) * L::KSTAGE;
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
                     tc::mma_bf16(tO(w), tc::smem_desc_sw128(base + L::P + w * 16384 + k * 32, 16, 1024),
@@ -251,36 +273,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     ok = false;
                     break;
                 }
-                // S of tile js (both q-tiles; up to two tiles ahead, one per S buffer) and P.V of
-                // tile jp[w] for each q-tile, issued in whichever order their inputs arrive: S
-                // waits for its K tile and for both softmax groups to have read the S buffer's
-                // previous contents; P.V for its group's P (and, first in a unit, for that
-                // group to have read the previous unit's output).  About 1 s without any
-                // progress ends the launch.
+                // P.V of tile jp[w] for each q-tile and S of tile js (both q-tiles), issued in
+                // whichever order their inputs arrive.  P.V waits for its group's P, its V
+                // tile and, first in a unit, for the group to have read the previous unit's
+                // output; it goes first, because it frees the P buffer and a V stage.  S waits
+                // for its K tile and for the S buffer's previous readers, and runs at most one
+                // tile ahead of P.V so that no P.V queues behind two S products.  About 1 s
+                // without any progress ends the launch.
                 int js = 0, jp[2] = {0, 0};
                 unsigned long long t_last = dev::globaltimer();
                 unsigned polls = 0;
                 while (jp[0] < un.nkv || jp[1] < un.nkv) {
                     bool prog = false;
-                    if (js < un.nkv && js < min(jp[0], jp[1]) + 2) {
-                        const int Jn = J + js;
-                        if (dev::mbar_test_wait(kv_full(Jn % NSTAGE), (Jn / NSTAGE) & 1) &&
-                            (Jn < 2 || dev::mbar_test_wait(s_free(Jn & 1), ((Jn - 2) >> 1) & 1))) {
-                            issue_s(Jn);
-                            ++js;
-                            prog = true;
-                        }
-                    }
 #pragma unroll
                     for (int w = 0; w < 2; ++w) {
                         if (jp[w] < js) {
                             const int Jc = J + jp[w];
                             if (dev::mbar_test_wait(p_full(w), Jc & 1) &&
+                                dev::mbar_test_wait(v_full(Jc % NSTAGE), (Jc / NSTAGE) & 1) &&
                                 (jp[w] > 0 || uq == 0 || dev::mbar_test_wait(o_free(w), (uq - 1) & 1))) {
                                 issue_pv(Jc, w, jp[w] == 0);
                                 ++jp[w];
                                 prog = true;
                             }
+                        }
+                    }
+                    if (js < un.nkv && js <= min(jp[0], jp[1]) + 1) {
+                        const int Jn = J + js;
+                        if (dev::mbar_test_wait(k_full(Jn % NSTAGE), (Jn / NSTAGE) & 1) &&
+                            (Jn < 2 || dev::mbar_test_wait(s_free(Jn & 1), ((Jn - 2) >> 1) & 1))) {
+                            issue_s(Jn);
+                            ++js;
+                            prog = true;
                         }
                     }
                     if (prog) {
@@ -388,9 +412,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (j == un.nkv - 1) {
                     const int first = un.kmax + 1 - kb;
                     if (first < BN) {
-                        ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(kv_full(J % NSTAGE), (J / NSTAGE) & 1));
+                        ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(v_full(J % NSTAGE), (J / NSTAGE) & 1));
                         if (!ok) break;
-                        uint8_t *vst = sm + L::KV + (J % NSTAGE) * L::STAGE + L::V_OFF;
+                        uint8_t *vst = sm + L::V + (J % NSTAGE) * L::KSTAGE;
                         const int chunks = (BN - first) * 8;      // 16-byte chunks per atom column
                         for (int hf = 0; hf < H; ++hf)
                             for (int c = st; c < chunks; c += 128)
