@@ -538,6 +538,27 @@ def _prefill_oracle_sample(w, nrows=48, threads=None):
     return flops / sec / 1e12, sec, nrows, threads
 
 
+PREFILL_SOURCES = ("prefill.cu", "tc_device.cuh")
+
+
+def _prefill_traffic(workload: str):
+    """DRAM bytes per prefill launch from the committed ncu summary, if it was taken on the
+    current prefill sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "prefill_%s.md" % workload.replace("prefill_", "", 1))
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    s = re.search(r"prefill_source_sha256_16:\s*([0-9a-f]+)", text)
+    h = hashlib.sha256()
+    for name in PREFILL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_159_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if not m or not s or s.group(1) != h.hexdigest()[:16]:
+        return None
+    return int(m.group(1))
+
+
 def run_prefill(args, world, rank, local_rank):
     import torch
     import paged_kv_cache_159_gb300 as pkv
@@ -655,7 +676,8 @@ def run_prefill(args, world, rank, local_rank):
         },
         "query_tokens_per_s": round(world * T * K / total, 1),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_kernel<%d>" % D,
+                     "frac": round(achieved / peak, 4), "traffic": _prefill_traffic(w.name),
+                     "kernel": "prefill_kernel<%d>" % D,
                      "flops_per_launch": flops, "peak_source": peak_src},
         "e2e": {"value": round(world * flops / e2e_step / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
