@@ -355,6 +355,45 @@ int pkv_paged_prefill(pkv_pool *pool, const void *q, const void *key_cache, cons
                       const int32_t *block_tables, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
                       int32_t total_q, float scale, const void *plan, int32_t grid, void *out, void *stream);
 
+/* Host side of one decode step, for pkv_decode_step_host: host memory, page-locked (pinned)
+ * for the copies to be asynchronous.  block_tables and seq_lens may be NULL when the device
+ * copies are already current (tables change only when a sequence gains a block).  With
+ * k_new and v_new both NULL the step only decodes (pkv_paged_attention_decode_ex). */
+typedef struct {
+    const void *q;                  /* bf16 [batch, num_q_heads, D] */
+    const void *k_new;              /* bf16 [batch, Hkv, D] */
+    const void *v_new;              /* bf16 [batch, Hkv, D] */
+    const int32_t *block_tables;    /* int32 [batch, max_blocks], or NULL */
+    const int32_t *seq_lens;        /* int32 [batch], or NULL */
+    void *out;                      /* bf16 [batch, num_q_heads, D], written */
+    int32_t contiguous;             /* nonzero: the inputs lie back to back (see below) */
+} pkv_host_step;
+
+/* The device buffers of the same step (device memory, shapes as in pkv_host_step). */
+typedef struct {
+    void *q;
+    void *k_new;
+    void *v_new;
+    int32_t *block_tables;
+    int32_t *seq_lens;
+    void *out;
+} pkv_device_step;
+
+/* One whole decode step from host memory in one call [Decode][Slot][Attn]: asynchronous
+ * copies of the step's inputs host -> device on `stream`, pkv_decode_step on the device
+ * buffers, and the copy of out back to host -- every operation issued by this call, in
+ * stream order.  With host->contiguous set, the caller promises that the inputs present lie
+ * back to back, in the order q, k_new, v_new, block_tables, seq_lens, within one host
+ * allocation and likewise within one device allocation (dev->q first); they then travel in
+ * one copy (INVALID if the pointers are not so laid out).  Otherwise each travels in its
+ * own copy.  It returns once everything is issued: synchronise the stream before reading
+ * host->out or reusing the host inputs.  Caches, workspace, opts and errors as
+ * pkv_decode_step; INVALID if a needed pointer is NULL. */
+int pkv_decode_step_host(pkv_pool *pool, const pkv_host_step *host, const pkv_device_step *dev,
+                         void *key_cache, void *value_cache, int32_t batch, int32_t num_q_heads,
+                         int32_t max_blocks, float scale, void *workspace, size_t workspace_bytes,
+                         const pkv_decode_opts *opts, void *stream);
+
 /* Bytes of the fixed device scratch behind pkv_paged_attention_decode_noalloc. */
 #define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
 

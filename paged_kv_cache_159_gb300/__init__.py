@@ -46,7 +46,7 @@ EXPORTED = (
     "pkv_decode_step_layers", "pkv_cow_prepare", "pkv_copy_blocks",
     "pkv_block_hashes", "pkv_prefix_lookup", "pkv_prefix_insert", "pkv_prefix_evict",
     "pkv_prefix_clear", "pkv_prefix_cached_blocks", "pkv_slot_mapping_chunks",
-    "pkv_prefill_plan_bytes", "pkv_prefill_plan", "pkv_paged_prefill",
+    "pkv_prefill_plan_bytes", "pkv_prefill_plan", "pkv_paged_prefill", "pkv_decode_step_host",
     "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
     "pkv_paged_attention_decode_ex", "pkv_decode_step", "pkv_paged_attention_decode_noalloc",
     "pkv_get_device_error", "pkv_probe_copy",
@@ -65,6 +65,17 @@ class pool_desc(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
                 ("v_scale", ctypes.c_float), ("num_layers", ctypes.c_int32)]
+
+
+class host_step(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("block_tables", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("contiguous", ctypes.c_int32)]
+
+
+class device_step(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("block_tables", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p), ("out", ctypes.c_void_p)]
 
 
 class decode_opts(ctypes.Structure):
@@ -116,6 +127,9 @@ def lib():
                                                 ctypes.POINTER(_I32)]),
             "pkv_paged_prefill": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
                                                  ctypes.c_float, _P, _I32, _P, _P]),
+            "pkv_decode_step_host": (ctypes.c_int, [_P, ctypes.POINTER(host_step), ctypes.POINTER(device_step),
+                                                    _P, _P, _I32, _I32, _I32, ctypes.c_float, _P,
+                                                    ctypes.c_size_t, ctypes.POINTER(decode_opts), _P]),
             "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32, _I32, ctypes.POINTER(decode_opts)]),
             "pkv_paged_attention_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
                                                           ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
@@ -465,6 +479,35 @@ def decode_step_layers(pool: Pool, q, k_new, v_new, key_cache, value_cache, bloc
         int(block_tables.shape[1]), float(scale), _dev_ptr(out, "out"),
         _dev_ptr(workspace, "workspace"), int(ws_bytes), ctypes.byref(o) if o else None,
         _stream_ptr(stream)), "decode_step_layers")
+
+
+def _host_ptr(t, what: str):
+    if t is None:
+        return None
+    if getattr(t, "is_cuda", False) or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous host tensor" % what)
+    return t.data_ptr()
+
+
+def decode_step_host(pool: Pool, host: dict, dev: dict, key_cache, value_cache, scale: float, workspace,
+                     opts=None, stream=None):
+    """One decode step from host memory in one call (pkv_decode_step_host).  host: dict of
+    pinned CPU tensors q, k_new, v_new, block_tables (or None), seq_lens (or None), out, and
+    optionally contiguous=True when the inputs are views laid back to back in one host and
+    one device buffer; dev: dict of the matching CUDA tensors.  Returns once everything is
+    issued."""
+    B, Hq, _ = dev["q"].shape
+    h = host_step(_host_ptr(host["q"], "q"), _host_ptr(host.get("k_new"), "k_new"), _host_ptr(host.get("v_new"), "v_new"),
+                  _host_ptr(host.get("block_tables"), "block_tables"), _host_ptr(host.get("seq_lens"), "seq_lens"),
+                  _host_ptr(host["out"], "out"), int(bool(host.get("contiguous", False))))
+    d = device_step(*[(_dev_ptr(dev.get(k), k).value if dev.get(k) is not None else None)
+                      for k in ("q", "k_new", "v_new", "block_tables", "seq_lens", "out")])
+    o = _opts(opts)
+    _check(lib().pkv_decode_step_host(pool.handle, ctypes.byref(h), ctypes.byref(d), _dev_ptr(key_cache, "key_cache"),
+                                      _dev_ptr(value_cache, "value_cache"), int(B), int(Hq),
+                                      int(dev["block_tables"].shape[1]), float(scale), _dev_ptr(workspace, "workspace"),
+                                      int(workspace.numel() * workspace.element_size()),
+                                      ctypes.byref(o) if o else None, _stream_ptr(stream)), "decode_step_host")
 
 
 def paged_attention_decode_noalloc(pool: Pool, q, key_cache, value_cache, block_tables,

@@ -210,3 +210,55 @@ extern "C" int pkv_decode_step_layers(pkv_pool *pool, const void *q, const void 
                                     value_cache, block_tables, seq_lens, batch, num_q_heads,
                                     max_blocks, scale, out, workspace, workspace_bytes, opts, stream);
 }
+
+extern "C" int pkv_decode_step_host(pkv_pool *pool, const pkv_host_step *host, const pkv_device_step *dev,
+                                    void *key_cache, void *value_cache, int32_t batch, int32_t num_q_heads,
+                                    int32_t max_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                    const pkv_decode_opts *opts, void *stream)
+{
+    int st = pkv::check_attached(pool);
+    if (st != PKV_OK) return st;
+    if (!host || !dev || batch < 0 || num_q_heads < 1 || max_blocks < 1) return PKV_ERR_INVALID;
+    if (batch == 0) return PKV_OK;
+    const bool append = host->k_new || host->v_new;
+    if (!host->q || !host->out || !dev->q || !dev->block_tables || !dev->seq_lens || !dev->out)
+        return PKV_ERR_INVALID;
+    if (append && (!host->k_new || !host->v_new || !dev->k_new || !dev->v_new)) return PKV_ERR_INVALID;
+    const pkv_pool_desc &d = pool->desc;
+    const size_t qb = (size_t)batch * num_q_heads * d.head_dim * 2;
+    const size_t kb = (size_t)batch * d.num_kv_heads * d.head_dim * 2;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const struct { void *dst; const void *src; size_t n; } in[] = {
+        {dev->q, host->q, qb},
+        {dev->k_new, host->k_new, append ? kb : 0},
+        {dev->v_new, host->v_new, append ? kb : 0},
+        {dev->block_tables, host->block_tables, (size_t)batch * max_blocks * 4},
+        {dev->seq_lens, host->seq_lens, (size_t)batch * 4},
+    };
+    if (host->contiguous) {
+        // the caller lays the inputs out back to back in one host and one device allocation:
+        // one copy (a copy may not span two allocations, so this is never inferred)
+        const char *hs = static_cast<const char *>(host->q);
+        char *ds = static_cast<char *>(dev->q);
+        size_t n = 0;
+        for (const auto &c : in) {
+            if (!c.n) continue;
+            if (c.src != hs + n || c.dst != ds + n) return PKV_ERR_INVALID;
+            n += c.n;
+        }
+        if (cudaMemcpyAsync(ds, hs, n, cudaMemcpyHostToDevice, s) != cudaSuccess) return PKV_ERR_CUDA;
+    } else {
+        for (const auto &c : in)
+            if (c.src && c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s) != cudaSuccess)
+                return PKV_ERR_CUDA;
+    }
+    st = append ? pkv_decode_step(pool, dev->q, dev->k_new, dev->v_new, key_cache, value_cache, dev->block_tables,
+                                  dev->seq_lens, batch, num_q_heads, max_blocks, scale, dev->out, workspace,
+                                  workspace_bytes, opts, stream)
+                : pkv_paged_attention_decode_ex(pool, dev->q, key_cache, value_cache, dev->block_tables,
+                                                dev->seq_lens, batch, num_q_heads, max_blocks, scale, dev->out,
+                                                workspace, workspace_bytes, opts, stream);
+    if (st != PKV_OK) return st;
+    return cudaMemcpyAsync(host->out, dev->out, qb, cudaMemcpyDeviceToHost, s) == cudaSuccess ? PKV_OK
+                                                                                              : PKV_ERR_CUDA;
+}

@@ -279,3 +279,51 @@ def test_probe_copy():
     pkv.probe_copy(dst, src)
     torch.cuda.synchronize()
     assert torch.equal(src, dst)
+
+
+@pytest.mark.parametrize("contiguous", [False, True])
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b", "qwen25_7b_prefix"])
+def test_decode_step_from_host_memory_equals_the_device_step(name, contiguous):
+    """pkv_decode_step_host (copies in, one-launch step, copy out, all from one call) gives
+    the same bits as pkv_decode_step on device buffers: output and pool."""
+    a = C.build(name)
+    b = C.build(name)
+    bt, sl, _ = C.device_tables(a)
+    B, Hq, _ = a.q.shape
+    ws_a = torch.zeros(pkv.decode_workspace_bytes(a.pool, B, Hq, bt.shape[1]), dtype=torch.uint8, device="cuda")
+    ws_b = torch.zeros_like(ws_a)
+    out_a = torch.empty_like(a.q)
+    if a.w.append:
+        pkv.decode_step(a.pool, a.q, a.k_new, a.v_new, a.key_cache, a.value_cache, bt, sl, a.w.scale, out_a, ws_a)
+    else:
+        pkv.paged_attention_decode(a.pool, a.q, a.key_cache, a.value_cache, bt, sl, a.w.scale, out_a, ws_a)
+    pin = lambda t: t.detach().cpu().pin_memory()
+    host = {"q": pin(b.q), "block_tables": pin(bt), "seq_lens": pin(sl),
+            "out": torch.empty(b.q.shape, dtype=b.q.dtype).pin_memory()}
+    dev = {"q": torch.empty_like(b.q), "block_tables": torch.empty_like(bt), "seq_lens": torch.empty_like(sl),
+           "out": torch.empty_like(b.q)}
+    if b.w.append:
+        host.update(k_new=pin(b.k_new), v_new=pin(b.v_new))
+        dev.update(k_new=torch.empty_like(b.k_new), v_new=torch.empty_like(b.v_new))
+    if contiguous:                  # the inputs as views of one host and one device buffer
+        names = [k for k in ("q", "k_new", "v_new", "block_tables", "seq_lens") if k in host]
+        sizes = [host[k].numel() * host[k].element_size() for k in names]
+        hbuf = torch.empty(sum(sizes), dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(sum(sizes), dtype=torch.uint8, device="cuda")
+        off = 0
+        for k, n in zip(names, sizes):
+            t = host[k]
+            host[k] = hbuf[off:off + n].view(t.dtype).view(t.shape)
+            host[k].copy_(t)
+            dev[k] = dbuf[off:off + n].view(t.dtype).view(t.shape)
+            off += n
+        host["contiguous"] = True
+    stream = torch.cuda.current_stream()
+    pkv.decode_step_host(b.pool, host, dev, b.key_cache, b.value_cache, b.w.scale, ws_b, stream=stream)
+    stream.synchronize()
+    for c in (a, b):
+        st, bits = c.pool.get_device_error()
+        assert st == pkv.OK and bits == 0
+    assert torch.equal(host["out"].view(torch.int16), out_a.cpu().view(torch.int16))
+    assert torch.equal(a.key_cache.view(torch.int16), b.key_cache.view(torch.int16))
+    assert torch.equal(a.value_cache.view(torch.int16), b.value_cache.view(torch.int16))
