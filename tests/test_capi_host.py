@@ -348,3 +348,21 @@ def test_prefix_insert_errors_change_nothing(lib):
         p.prefix_insert(list(range(300, 316)), 0, [7])                    # a free block
     assert p.prefix_cached_blocks() == 2 and p.refcount(int(other[0])) == 1
     assert p.prefix_lookup(toks + [5] * 3).tolist() == row.tolist()
+
+
+def test_prefill_plan_argument_errors(lib):
+    p = pkv.Pool(64, 8, 128)
+    bad = [
+        (np.array([0, 5, 3], np.int32), np.array([5, 9], np.int32), 32, 4),    # negative chunk
+        (np.array([1, 5], np.int32), np.array([5], np.int32), 32, 4),          # cu_q[0] != 0
+        (np.array([0, 6], np.int32), np.array([5], np.int32), 32, 4),          # chunk longer than the sequence
+        (np.array([0, 5], np.int32), np.array([100], np.int32), 32, 4),        # needs 7 table entries
+        (np.array([0, 5], np.int32), np.array([5], np.int32), 12, 4),          # Hq not a multiple of Hkv
+    ]
+    for cu, lens, hq, mb in bad:
+        out = np.zeros(1 << 16, np.uint8)
+        grid = pkv.ctypes.c_int32()
+        st = lib.pkv_prefill_plan(p.handle, pkv._np_ptr(cu), pkv._np_ptr(lens), lens.size, hq, mb,
+                                  pkv._np_ptr(out), out.size, pkv.ctypes.byref(grid))
+        assert st == pkv.ERR_INVALID, (cu, lens, hq)
+    assert lib.pkv_prefill_plan_bytes(p.handle, 2, 8 * 17, 100) == 0          # group > 16

@@ -68,3 +68,63 @@ def test_chunked_prefill_llama3_8b_full_size_sampled():
     pos = np.array([0, 1, 31, 32, 255, 256, 510, 511])
     rows = np.concatenate([b * 512 + pos for b in range(w.batch)])
     _run("chunked_prefill_llama3_8b", rows=rows)
+
+
+def _plan_units(buf, grid):
+    """Decode a plan (layout of pkv_prefill_plan): header, per-CTA ranges, units."""
+    hdr = np.frombuffer(buf[:32].tobytes(), dtype=np.int32)
+    off = np.frombuffer(buf[32:32 + 4 * (grid + 1)].tobytes(), dtype=np.int32)
+    start = (32 + 4 * (grid + 1) + 31) // 32 * 32
+    n = int(hdr[1])
+    units = np.frombuffer(buf[start:start + 32 * n].tobytes(), dtype=np.int32).reshape(n, 8)
+    return hdr, off, units
+
+
+@pytest.mark.parametrize("name", ["prefill_tiny", "chunked_prefill_llama3_8b"])
+def test_prefill_plan_covers_every_row_once_and_balances(name):
+    """Every (sequence, KV head, query row) is in exactly one unit; each unit's key range is
+    its rows' causal range; longest-first assignment keeps every CTA within one unit (plus
+    its overhead) of the ideal share."""
+    w = workloads.PREFILL_WORKLOADS[name]
+    d = workloads.draw_prefill(w, "cpu")
+    pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim)
+    plan, grid = pkv.prefill_plan(pool, d.cu_q, d.seq_lens, w.num_q_heads, d.max_blocks)
+    hdr, off, units = _plan_units(plan, grid)
+    g = w.num_q_heads // w.num_kv_heads
+    assert hdr[2] == grid and hdr[3] == g and hdr[4] == 256 // g
+    assert off[0] == 0 and off[-1] == len(units) and np.all(np.diff(off) >= 1)
+    seen = np.zeros((int(d.cu_q[-1]), w.num_kv_heads), np.int32)
+    for b, h, row0, pos0, npos, nkv, kmax, _ in units:
+        assert 1 <= npos <= 256 // g
+        C = int(d.seq_lens[b] - d.chunk_lens[b])
+        assert pos0 == C + (row0 - d.cu_q[b]) and kmax == pos0 + npos - 1 and nkv == kmax // 64 + 1
+        seen[row0:row0 + npos, h] += 1
+    assert np.all(seen == 1)
+    load = np.array([sum(int(units[i, 5]) + 2 for i in range(off[c], off[c + 1])) for c in range(grid)])
+    assert load.max() <= load.sum() / grid + units[:, 5].max() + 2
+
+
+def test_prefill_flags_a_mismatched_plan_and_a_bad_table_entry():
+    c = C.build_prefill("prefill_tiny")
+    C.prefill_append(c)
+    torch.cuda.synchronize()
+    plan, grid = pkv.prefill_plan(c.pool, c.d.cu_q, c.d.seq_lens, c.w.num_q_heads, c.tables.shape[1])
+    out = torch.full_like(c.d.q, 7.0)
+    bt = torch.from_numpy(c.tables).cuda()
+    # a plan made for another head count: nothing runs, the plan bit is set
+    other, g2 = pkv.prefill_plan(c.pool, c.d.cu_q, c.d.seq_lens, 2 * c.w.num_q_heads, c.tables.shape[1])
+    q2 = torch.zeros((c.d.q.shape[0], 2 * c.w.num_q_heads, c.w.head_dim), dtype=torch.bfloat16, device="cuda")
+    o2 = torch.full_like(q2, 7.0)
+    pkv.paged_prefill(c.pool, q2, c.key_cache, c.value_cache, bt, c.w.scale, torch.from_numpy(plan).cuda(), grid, o2)
+    st, bits = c.pool.get_device_error()
+    assert st == pkv.ERR_DEVICE and bits == pkv.DEVERR_PLAN
+    assert bool((o2 == 7.0).all())
+    # a table entry outside the pool is flagged (the kernel skips that block and finishes)
+    bad = bt.clone()
+    bad[0, 0] = c.d.num_blocks + 3
+    pkv.paged_prefill(c.pool, c.d.q, c.key_cache, c.value_cache, bad, c.w.scale, torch.from_numpy(plan).cuda(), grid, out)
+    st, bits = c.pool.get_device_error()
+    assert st == pkv.ERR_DEVICE and bits & pkv.DEVERR_BLOCK_ID and not bits & pkv.DEVERR_TIMEOUT
+    # the context is still usable: a correct run afterwards matches the oracle
+    out = C.gpu_prefill(c)
+    C.tol_check(C.bf16_to_f64(out), C.oracle_prefill_rows(c, threads=1))
