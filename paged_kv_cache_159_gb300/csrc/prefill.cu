@@ -23,17 +23,27 @@
 //   * A host plan (pkv_prefill_plan) lists the units and assigns them, heaviest first, to
 //     the CTAs of a persistent one-wave grid (longest-processing-time first).  The same plan
 //     serves every layer of a batch.
-//   * One CTA per SM, 11 warps: warp 0 issues the tiled bulk-tensor (TMA) loads of Q and K,
-//     warp 10 those of V, warp 1 the tcgen05.mma instructions; warps 2-5 run the softmax and
-//     epilogue of q-tile 0, warps 6-9 of q-tile 1, one query row per thread.
+//   * One CTA per SM, 13 warps: warps 0, 10 and 11 issue the tiled bulk-tensor (TMA) loads of
+//     K, V and Q, warp 1 the tcgen05.mma instructions of S and warp 12 those of P.V; warps
+//     2-5 run the softmax and epilogue of q-tile 0, warps 6-9 of q-tile 1, one query row per
+//     thread.
 //   * Per K/V tile of 64 keys (4 paged blocks): S = Q.K^T (M 128, N 64, K D) per q-tile into
 //     tensor memory (double-buffered, so the next S is computed while the softmax reads
 //     this one); the softmax masks (causal, by select), updates the running max and sum
 //     (exp2 domain, rescaling the output accumulator only when the max rises by more than
-//     2^8) and writes P as bf16 to shared memory; O += P.V (M 128, N D, K 64) accumulates
-//     in tensor memory.  The MMA warp polls its inputs and issues each P.V and S as soon as
-//     they are ready, P.V first.
-//   * K and V stream through two separate 4-stage rings.  A K tile is free again once S is
+//     2^8) and writes P as bf16 back into the tensor-memory columns its S came from; O +=
+//     P.V (M 128, N D, K 64) reads P from tensor memory and V from shared memory and
+//     accumulates in tensor memory.  The S that next overwrites a P waits until that P's
+//     P.V is complete.
+//   * Feeding the tensor pipe sets the pace: it accepts only a few instructions ahead, a
+//     128 x 64 x 16 MMA takes about 36 ns and a 128 x 128 x 16 one about 56 ns, and each
+//     satisfied mbarrier wait of the issuing thread costs about 70 ns.  One thread that
+//     waited for its inputs between batches left the pipe idle about 40 % of each tile; two
+//     issuing threads (S and P.V) overlap one's waits with the other's products.
+//   * Keeping P out of shared memory leaves the room for deeper rings and takes P's stores
+//     and the tensor core's reads of it off the shared-memory port, and the softmax no
+//     longer waits for the previous P.V before writing P (only a rescale of O does).
+//   * K and V stream through two separate rings (5 stages each at D = 128).  A K tile is free again once S is
 //     computed, a V tile only after P.V: sharing one stage would hold K for a whole tile's
 //     pipeline, and with loads of scattered 4 KiB blocks taking microseconds under load, the
 //     ring, not the tensor core, would set the pace.  Each 16-token block of one KV head is
@@ -62,13 +72,12 @@ namespace prefill {
 
 constexpr int BM = 128;            // query rows per q-tile (two q-tiles per unit)
 constexpr int BN = 64;             // keys per KV tile (4 blocks)
-constexpr int NSTAGE = 4;          // K/V ring depth
 constexpr int BS = 16;             // tokens per block
-constexpr int NTHREADS = 352;      // warp 0 Q+K loads, 1 MMA, 2-9 softmax + epilogue, 10 V loads
+constexpr int NTHREADS = 416;      // warp 0 K loads, 1 S MMAs, 2-9 softmax + epilogue, 10 V, 11 Q loads, 12 P.V MMAs
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float TAU = 8.0f;        // raise the running max only beyond 2^8
 constexpr uint32_t PLAN_MAGIC = 0x504b5650u;   // "PVKP"
-constexpr uint32_t TMEM_COLS = 512;            // S: 2 buffers x 2 q-tiles x 64, O: 2 x D
+constexpr uint32_t TMEM_COLS = 512;            // S (and P over it): 2 buffers x 2 q-tiles x 64, O: 2 x D
 
 // A plan: header, per-CTA unit ranges, units.
 struct PlanHeader { uint32_t magic; int32_t num_units, grid, group, tp, hq, hkv, pad; };
@@ -91,16 +100,18 @@ struct Params {
 template <int D>
 struct Smem {
     static constexpr int H = D / 64;                  // 64-column atom columns per row
+    static constexpr int NS = D == 128 ? 5 : 8;       // K/V ring depth (what the room allows)
     static constexpr int Q = 0;                       // H x [256 rows][64]
     static constexpr int QHALF = BM * 2 * 128;        // bytes of one atom column of Q (256 rows)
-    static constexpr int P = Q + H * QHALF;           // 2 q-tiles x [128 rows][64 keys]
     static constexpr int KHALF = BN * 128;            // bytes of one atom column of a K or V tile
     static constexpr int KSTAGE = H * KHALF;          // one K (or V) tile
-    static constexpr int K = P + 2 * 16384;           // NSTAGE K tiles
-    static constexpr int V = K + NSTAGE * KSTAGE;     // NSTAGE V tiles
-    static constexpr int BAR = V + NSTAGE * KSTAGE;
-    static constexpr int TOTAL = BAR + 256;
+    static constexpr int K = Q + H * QHALF;           // NS K tiles
+    static constexpr int V = K + NS * KSTAGE;         // NS V tiles
+    static constexpr int BAR = V + NS * KSTAGE;       // 12 + 5 NS mbarriers, then the TMEM slot
+    static constexpr int TOTAL = BAR + 512;
     static constexpr int ALLOC = TOTAL + 1024;        // alignment slack
+    static_assert(8 * (12 + 5 * NS) + 4 <= 512, "barrier area");
+    static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
 template <int D>
@@ -110,12 +121,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 {
     using L = Smem<D>;
     constexpr int H = L::H;
+    constexpr int NSTAGE = L::NS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = dev::smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // barriers: q_full; k_full, v_full, k_free [NSTAGE]; s_full, s_free [2 S buffers];
-    // p_full [2 q-tiles]; o_done [2 q-tiles][NSTAGE]; o_free [2 q-tiles]
+    // p_full [2 q-tiles][2 tile parities]; o_done [2 q-tiles][NSTAGE]; o_free [2 q-tiles];
+    // q_free (a unit's last S is done with Q).
+    // p_full alternates by tile: the softmax does not wait for the previous P.V, so it can
+    // finish tile J+1 before the MMA warp has seen tile J's P, and a single barrier would
+    // then run two phases ahead of its waiter.
     const uint32_t bars = base + L::BAR;
     const uint32_t q_full = bars;
     auto k_full = [&](int s) { return bars + 8 * (1 + s); };
@@ -123,10 +139,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     auto k_free = [&](int s) { return bars + 8 * (1 + 2 * NSTAGE + s); };
     auto s_full = [&](int b) { return bars + 8 * (1 + 3 * NSTAGE + b); };
     auto s_free = [&](int b) { return bars + 8 * (3 + 3 * NSTAGE + b); };
-    auto p_full = [&](int w) { return bars + 8 * (5 + 3 * NSTAGE + w); };
-    auto o_done = [&](int w, int s) { return bars + 8 * (7 + 3 * NSTAGE + w * NSTAGE + s); };
-    auto o_free = [&](int w) { return bars + 8 * (7 + 5 * NSTAGE + w); };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (9 + 5 * NSTAGE));
+    auto p_full = [&](int w, int J) { return bars + 8 * (5 + 3 * NSTAGE + 2 * w + (J & 1)); };
+    auto o_done = [&](int w, int s) { return bars + 8 * (9 + 3 * NSTAGE + w * NSTAGE + s); };
+    auto o_free = [&](int w) { return bars + 8 * (9 + 5 * NSTAGE + w); };
+    const uint32_t q_free = bars + 8 * (11 + 5 * NSTAGE);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (12 + 5 * NSTAGE));
 
     const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(p.plan);
     const int32_t *cta_off = reinterpret_cast<const int32_t *>(p.plan + sizeof(PlanHeader));
@@ -140,6 +157,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     if (tid == 0) {
         dev::mbar_init(q_full, 1);
+        dev::mbar_init(q_free, 1);
         for (int s = 0; s < NSTAGE; ++s) {
             dev::mbar_init(k_full(s), 1);
             dev::mbar_init(v_full(s), 1);
@@ -148,7 +166,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (int b = 0; b < 2; ++b) {
             dev::mbar_init(s_full(b), 1);
             dev::mbar_init(s_free(b), 8);             // every softmax warp has read its S
-            dev::mbar_init(p_full(b), 4);             // the q-tile's four warps wrote P
+            dev::mbar_init(p_full(b, 0), 4);          // the q-tile's four warps wrote P
+            dev::mbar_init(p_full(b, 1), 4);
             dev::mbar_init(o_free(b), 4);
             for (int s = 0; s < NSTAGE; ++s) dev::mbar_init(o_done(b, s), 1);
         }
@@ -185,29 +204,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         return n;
     };
 
-    if (warp == 0 || warp == 10) {
-        // ============ TMA producers: warp 0 loads Q and K, warp 10 loads V ============
+    if (warp == 11) {
+        // ============ TMA producer of Q: a unit's rows once the previous unit's last S is done
+        if (lane == 0) {
+            int uq = 0;
+            bool ok = true;
+            for (int u = u0; u < u1; ++u, ++uq) {
+                const Unit un = units[u];
+                if (uq > 0 && !dev::mbar_wait_bounded(q_free, (uq - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                dev::mbar_arrive_expect_tx(q_full, (uint32_t)(H * 64 * p.group * p.TP * 2));
+                for (int hf = 0; hf < H; ++hf)
+                    tc::tma_load_3d(base + L::Q + hf * L::QHALF, &qmap, hf * 64, un.h * p.group, un.row0, q_full);
+            }
+            if (!ok) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+            // no copy may land after the CTA has left: wait (bounded) for the last one
+            if (uq > 0) (void)dev::mbar_wait_bounded(q_full, (uq - 1) & 1);
+        }
+    } else if (warp == 0 || warp == 10) {
+        // ============ TMA producers: warp 0 loads K, warp 10 loads V ============
         // The two rings are separate because K is free again once S is computed, while V
         // is needed until P.V: a K stage is held for about a load plus S, not for a whole
-        // tile's pipeline.
+        // tile's pipeline.  Q has a producer of its own so that the K ring runs ahead into
+        // the next unit while the current one finishes.
         if (lane == 0) {
             const bool isk = warp == 0;
             const CUtensorMap *map = isk ? &kmap : &vmap;
-            int J = 0, uq = 0, q_arms = 0, arms[NSTAGE] = {};
+            int J = 0, arms[NSTAGE] = {};
             bool ok = true;
-            for (int u = u0; u < u1 && ok; ++u, ++uq) {
+            for (int u = u0; u < u1 && ok; ++u) {
                 const Unit un = units[u];
-                if (isk) {
-                    // the previous unit's S products are done with Q once its last S completed
-                    if (uq > 0 && !dev::mbar_wait_bounded(k_free((J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    dev::mbar_arrive_expect_tx(q_full, (uint32_t)(H * 64 * p.group * p.TP * 2));
-                    ++q_arms;
-                    for (int hf = 0; hf < H; ++hf)
-                        tc::tma_load_3d(base + L::Q + hf * L::QHALF, &qmap, hf * 64, un.h * p.group, un.row0, q_full);
-                }
                 for (int j = 0; j < un.nkv; ++j, ++J) {
                     const int s = J % NSTAGE;
                     if (J >= NSTAGE) {            // the stage's previous tile: S done (K), P.V done (V)
@@ -233,89 +261,82 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
             if (!ok) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
             // no copy may land after the CTA has left: wait (bounded) for the last of each
-            if (q_arms) (void)dev::mbar_wait_bounded(q_full, (q_arms - 1) & 1);
             for (int s = 0; s < NSTAGE; ++s)
                 if (arms[s]) (void)dev::mbar_wait_bounded(isk ? k_full(s) : v_full(s), (arms[s] - 1) & 1);
         }
-    } else if (warp == 1) {
-        // ============================ MMA issuer ============================
+    } else if (warp == 1 || warp == 12) {
+        // ============ MMA issuers: warp 1 the S products, warp 12 the P.V products ============
+        // Two issuing threads, so that one waits for its next inputs while the other's
+        // products keep the tensor pipe busy: the pipe accepts only a few instructions ahead,
+        // and a single thread that waited between batches left it idle.  The S of tile J
+        // overwrites the tensor memory that P(J-2) was read from, so it waits for P.V(J-2)
+        // to be complete.  Every wait is on work issued before it (no cycle); about 1 s
+        // without progress ends the launch.
         if (lane == 0) {
-            constexpr uint32_t IDS = tc::idesc_bf16(BM, BN, 0);   // S = Q K^T: M 128, N 64 keys
-            constexpr uint32_t IDO = tc::idesc_bf16(BM, D, 1);    // O += P V: M 128, N D, V MN-major
             int J = 0, uq = 0;
             bool ok = true;
-            auto issue_s = [&](int Jn) {                          // both q-tiles
-                tc::fence_after_sync();
-                const uint32_t kst = base + L::K + (Jn % NSTAGE) * L::KSTAGE;
-#pragma unroll
-                for (int w = 0; w < 2; ++w)
-#pragma unroll
-                    for (int k = 0; k < 4 * H; ++k) {
-                        const uint32_t hf = k >> 2, kk = (k & 3) * 32;
-                        tc::mma_bf16(tS(Jn & 1, w), tc::smem_desc_sw128(base + L::Q + hf * L::QHALF + w * 16384 + kk, 16, 1024),
-                                     tc::smem_desc_sw128(kst + hf * L::KHALF + kk, 16, 1024), IDS, k > 0);
-                    }
-                tc::commit(s_full(Jn & 1));
-                tc::commit(k_free(Jn % NSTAGE));                 // the K tile may be reloaded
+            auto wait = [&](uint32_t bar, uint32_t par) {
+                if (ok && !dev::mbar_wait_bounded(bar, par)) ok = false;
+                return ok;
             };
-            auto issue_pv = [&](int Jc, int w, bool first) {
-                tc::fence_after_sync();
-                const uint32_t vst = base + L::V + (Jc % NSTAGE) * L::KSTAGE;
+            if (warp == 1) {
+                constexpr uint32_t IDS = tc::idesc_bf16(BM, BN, 0);   // S = Q K^T: M 128, N 64 keys
+                // The operand descriptors are built once; each MMA adds its offset.
+                const uint64_t dQ = tc::smem_desc_sw128(base + L::Q, 16, 1024);
+                const uint64_t dK = tc::smem_desc_sw128(base + L::K, 16, 1024);
+                for (int u = u0; u < u1 && ok; ++u, ++uq) {
+                    const Unit un = units[u];
+                    if (!wait(q_full, uq & 1)) break;
+                    for (int j = 0; j < un.nkv; ++j, ++J) {
+                        const int st = J % NSTAGE;
+                        if (!wait(k_full(st), (J / NSTAGE) & 1)) break;
+                        if (J >= 2) {
+                            // the softmax has read S(J-2) and P.V(J-2) has read P(J-2)
+                            const int s2 = (J - 2) % NSTAGE;
+                            const uint32_t p2 = ((J - 2) / NSTAGE) & 1;
+                            if (!wait(s_free(J & 1), ((J - 2) >> 1) & 1) || !wait(o_done(0, s2), p2) ||
+                                !wait(o_done(1, s2), p2))
+                                break;
+                        }
+                        tc::fence_after_sync();
+                        const uint64_t dk = tc::desc_add(dK, (uint32_t)st * L::KSTAGE);
+                        const uint32_t ts = tS(J & 1, 0);
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k)
-                    tc::mma_bf16(tO(w), tc::smem_desc_sw128(base + L::P + w * 16384 + k * 32, 16, 1024),
-                                 tc::smem_desc_sw128(vst + k * 16 * 128, L::KHALF, 1024), IDO, !first || (k > 0));
-                tc::commit(o_done(w, Jc % NSTAGE));
-            };
-            for (int u = u0; u < u1 && ok; ++u, ++uq) {
-                const Unit un = units[u];
-                if (!dev::mbar_wait_bounded(q_full, uq & 1)) {
-                    ok = false;
-                    break;
-                }
-                // P.V of tile jp[w] for each q-tile and S of tile js (both q-tiles), issued in
-                // whichever order their inputs arrive.  P.V waits for its group's P, its V
-                // tile and, first in a unit, for the group to have read the previous unit's
-                // output; it goes first, because it frees the P buffer and a V stage.  S waits
-                // for its K tile and for the S buffer's previous readers, and runs at most one
-                // tile ahead of P.V so that no P.V queues behind two S products.  About 1 s
-                // without any progress ends the launch.
-                int js = 0, jp[2] = {0, 0};
-                unsigned long long t_last = dev::globaltimer();
-                unsigned polls = 0;
-                while (jp[0] < un.nkv || jp[1] < un.nkv) {
-                    bool prog = false;
+                        for (int w = 0; w < 2; ++w)
 #pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        if (jp[w] < js) {
-                            const int Jc = J + jp[w];
-                            if (dev::mbar_test_wait(p_full(w), Jc & 1) &&
-                                dev::mbar_test_wait(v_full(Jc % NSTAGE), (Jc / NSTAGE) & 1) &&
-                                (jp[w] > 0 || uq == 0 || dev::mbar_test_wait(o_free(w), (uq - 1) & 1))) {
-                                issue_pv(Jc, w, jp[w] == 0);
-                                ++jp[w];
-                                prog = true;
+                            for (int k = 0; k < 4 * H; ++k) {
+                                const uint32_t hf = k >> 2, kk = (k & 3) * 32;
+                                tc::mma_bf16(ts + (uint32_t)(w * BN), tc::desc_add(dQ, hf * L::QHALF + w * 16384 + kk),
+                                             tc::desc_add(dk, hf * L::KHALF + kk), IDS, k > 0);
                             }
-                        }
-                    }
-                    if (js < un.nkv && js <= min(jp[0], jp[1]) + 1) {
-                        const int Jn = J + js;
-                        if (dev::mbar_test_wait(k_full(Jn % NSTAGE), (Jn / NSTAGE) & 1) &&
-                            (Jn < 2 || dev::mbar_test_wait(s_free(Jn & 1), ((Jn - 2) >> 1) & 1))) {
-                            issue_s(Jn);
-                            ++js;
-                            prog = true;
-                        }
-                    }
-                    if (prog) {
-                        t_last = dev::globaltimer();
-                        polls = 0;
-                    } else if ((++polls & 63u) == 0 && dev::globaltimer() - t_last > dev::WAIT_NS) {
-                        ok = false;
-                        break;
+                        tc::commit(s_full(J & 1));
+                        tc::commit(k_free(st));                      // the K tile may be reloaded
+                        if (j == un.nkv - 1) tc::commit(q_free);     // the unit is done with Q
                     }
                 }
-                J += un.nkv;
+            } else {
+                constexpr uint32_t IDO = tc::idesc_bf16(BM, D, 1);    // O += P V: M 128, N D, V MN-major
+                const uint64_t dV = tc::smem_desc_sw128(base + L::V, L::KHALF, 1024);
+                for (int u = u0; u < u1 && ok; ++u, ++uq) {
+                    const Unit un = units[u];
+                    for (int j = 0; j < un.nkv && ok; ++j, ++J) {
+                        const int st = J % NSTAGE;
+                        if (!wait(v_full(st), (J / NSTAGE) & 1)) break;
+                        const uint64_t dv = tc::desc_add(dV, (uint32_t)st * L::KSTAGE);
+                        for (int w = 0; w < 2; ++w) {
+                            // P(J) of the q-tile; first in a unit, its previous output was read
+                            if (!wait(p_full(w, J), (J >> 1) & 1)) break;
+                            if (j == 0 && uq > 0 && !wait(o_free(w), (uq - 1) & 1)) break;
+                            tc::fence_after_sync();
+                            const uint32_t tp = tS(J & 1, w), to = tO(w);
+#pragma unroll
+                            for (int k = 0; k < BN / 16; ++k)
+                                tc::mma_bf16_ts(to, tp + (uint32_t)(k * 8), tc::desc_add(dv, k * 16 * 128), IDO,
+                                                j > 0 || k > 0);
+                            tc::commit(o_done(w, st));
+                        }
+                    }
+                }
             }
             if (!ok) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
         }
@@ -373,8 +394,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 const bool rescale = raise && m != -INFINITY;
                 const float f = rescale ? dev::fast_exp2(m - mx) : 1.f;
                 if (raise) m = mx;
-                // P = exp2(x * scale - m) as packed bf16 in registers, before waiting for the
-                // previous tile's P.V, so that the exponentials overlap it
+                // P = exp2(x * scale - m) as packed bf16 (the lower key in the low half)
                 const float nm = m == -INFINITY ? 0.f : -m;
                 uint32_t pw[BN / 2];
                 float ps[4] = {0.f, 0.f, 0.f, 0.f};
@@ -386,15 +406,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     pw[e] = dev::pack_bf16x2(a, b2);
                 }
                 l = l * f + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-                // this group's previous P.V must be done before P is overwritten or O rescaled
-                if (J >= 1)
-                    ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(o_done(w, (J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1));
-                if (!ok) break;
-#pragma unroll
-                for (int cc = 0; cc < BN / 8; ++cc)
-                    *reinterpret_cast<uint4 *>(sm + L::P + w * 16384 + tc::sw128_offset(r, cc * 8)) =
-                        make_uint4(pw[4 * cc], pw[4 * cc + 1], pw[4 * cc + 2], pw[4 * cc + 3]);
+                // P over this tile's S columns (already read): the A operand of this tile's
+                // P.V.  No wait: the previous P.V reads the other S buffer.
+                tc::tmem_st32(tS(J & 1, w) + lane_off, pw);
                 if (__any_sync(dev::FULL, rescale)) {
+                    // O may be rescaled only once the previous P.V has accumulated into it
+                    ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(o_done(w, (J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1));
+                    if (!ok) break;
                     tc::fence_after_sync();
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
@@ -405,8 +423,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * f);
                         tc::tmem_st32(tO(w) + lane_off + 32 * c, v);
                     }
-                    tc::tmem_wait_st();
                 }
+                tc::tmem_wait_st();
                 // last tile: zero the V rows past the unit's last visible key (both groups do,
                 // each before its own P.V; the stores write the same zeros)
                 if (j == un.nkv - 1) {
@@ -420,12 +438,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                             for (int c = st; c < chunks; c += 128)
                                 *reinterpret_cast<uint4 *>(vst + hf * L::KHALF + first * 128 + c * 16) =
                                     make_uint4(0, 0, 0, 0);
+                        dev::fence_proxy_async_smem();           // zeroed rows -> tensor core
                     }
                 }
-                dev::fence_proxy_async_smem();                   // P and zeroed rows -> tensor core
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) dev::mbar_arrive(p_full(w));
+                if (lane == 0) dev::mbar_arrive(p_full(w, J));
             }
             if (!ok) break;
             // epilogue: O / l of this row, bf16, to out[row0 + pl][h*g + hh]

@@ -5,7 +5,7 @@
 //
 // Operand layout used throughout: 128-byte swizzle, tiles built from [rows][64] bf16 "atom
 // columns" of 128 bytes per row, each atom column starting 1024-byte aligned.  A K-major
-// operand (Q, K, P) keeps the contraction index within a row; an MN-major operand (V as
+// operand (Q, K) keeps the contraction index within a row; an MN-major operand (V as
 // the B operand of P.V) keeps the output column index within a row.
 #pragma once
 
@@ -27,6 +27,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
            ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The descriptor of the operand `bytes` further on (a multiple of 16) in shared memory: the
+// start-address field holds addr / 16 in 14 bits and shared addresses stay below 256 KiB, so
+// the addition never carries out of the field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D, A K-major, B
 // K-major (b_mn = 0) or MN-major (b_mn = 1), M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn)
@@ -43,6 +48,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] . B[smem]^T, issued by one thread.  A is read from tensor memory:
+// row i of the M = 128 rows in lane i, two bf16 of consecutive k per 32-bit column (the
+// lower k in the low half), so one k-step of 16 spans 8 columns from a_tmem.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
