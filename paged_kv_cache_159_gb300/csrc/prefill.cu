@@ -107,10 +107,10 @@ struct Smem {
     static constexpr int KSTAGE = H * KHALF;          // one K (or V) tile
     static constexpr int K = Q + H * QHALF;           // NS K tiles
     static constexpr int V = K + NS * KSTAGE;         // NS V tiles
-    static constexpr int BAR = V + NS * KSTAGE;       // 12 + 5 NS mbarriers, then the TMEM slot
+    static constexpr int BAR = V + NS * KSTAGE;       // 8 + 4 NS mbarriers, then the TMEM slot
     static constexpr int TOTAL = BAR + 512;
     static constexpr int ALLOC = TOTAL + 1024;        // alignment slack
-    static_assert(8 * (12 + 5 * NS) + 4 <= 512, "barrier area");
+    static_assert(8 * (8 + 4 * NS) + 4 <= 512, "barrier area");
     static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
@@ -126,24 +126,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint8_t *sm = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = dev::smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // barriers: q_full; k_full, v_full, k_free [NSTAGE]; s_full, s_free [2 S buffers];
-    // p_full [2 q-tiles][2 tile parities]; o_done [2 q-tiles][NSTAGE]; o_free [2 q-tiles];
-    // q_free (a unit's last S is done with Q).
+    // mbarriers: q_full, q_free (a unit's last S is done with Q); k_full, v_full, k_free
+    // [NSTAGE]; s_full [2 S buffers]; p_full [2 tile parities] (all eight softmax warps wrote
+    // P); o_done [NSTAGE] (both q-tiles' P.V of the stage's tile are complete); o_free [2
+    // q-tiles] (the epilogue has read O).
     // p_full alternates by tile: the softmax does not wait for the previous P.V, so it can
-    // finish tile J+1 before the MMA warp has seen tile J's P, and a single barrier would
-    // then run two phases ahead of its waiter.
+    // finish tile J+1 before the P.V issuer has seen tile J's P, and a single barrier would
+    // then run two phases ahead of its waiter.  S(J) waits for o_done of tile J-2, which
+    // also covers the softmax's reads of S(J-2): each softmax warp reads its S before it
+    // writes P, and P.V(J-2) waits for that P.
     const uint32_t bars = base + L::BAR;
-    const uint32_t q_full = bars;
-    auto k_full = [&](int s) { return bars + 8 * (1 + s); };
-    auto v_full = [&](int s) { return bars + 8 * (1 + NSTAGE + s); };
-    auto k_free = [&](int s) { return bars + 8 * (1 + 2 * NSTAGE + s); };
-    auto s_full = [&](int b) { return bars + 8 * (1 + 3 * NSTAGE + b); };
-    auto s_free = [&](int b) { return bars + 8 * (3 + 3 * NSTAGE + b); };
-    auto p_full = [&](int w, int J) { return bars + 8 * (5 + 3 * NSTAGE + 2 * w + (J & 1)); };
-    auto o_done = [&](int w, int s) { return bars + 8 * (9 + 3 * NSTAGE + w * NSTAGE + s); };
-    auto o_free = [&](int w) { return bars + 8 * (9 + 5 * NSTAGE + w); };
-    const uint32_t q_free = bars + 8 * (11 + 5 * NSTAGE);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (12 + 5 * NSTAGE));
+    const uint32_t q_full = bars, q_free = bars + 8;
+    auto k_full = [&](int s) { return bars + 8 * (2 + s); };
+    auto v_full = [&](int s) { return bars + 8 * (2 + NSTAGE + s); };
+    auto k_free = [&](int s) { return bars + 8 * (2 + 2 * NSTAGE + s); };
+    auto s_full = [&](int b) { return bars + 8 * (2 + 3 * NSTAGE + b); };
+    auto p_full = [&](int J) { return bars + 8 * (4 + 3 * NSTAGE + (J & 1)); };
+    auto o_done = [&](int s) { return bars + 8 * (6 + 3 * NSTAGE + s); };
+    auto o_free = [&](int w) { return bars + 8 * (6 + 4 * NSTAGE + w); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (8 + 4 * NSTAGE));
 
     const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(p.plan);
     const int32_t *cta_off = reinterpret_cast<const int32_t *>(p.plan + sizeof(PlanHeader));
@@ -162,14 +163,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             dev::mbar_init(k_full(s), 1);
             dev::mbar_init(v_full(s), 1);
             dev::mbar_init(k_free(s), 1);
+            dev::mbar_init(o_done(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             dev::mbar_init(s_full(b), 1);
-            dev::mbar_init(s_free(b), 8);             // every softmax warp has read its S
-            dev::mbar_init(p_full(b, 0), 4);          // the q-tile's four warps wrote P
-            dev::mbar_init(p_full(b, 1), 4);
-            dev::mbar_init(o_free(b), 4);
-            for (int s = 0; s < NSTAGE; ++s) dev::mbar_init(o_done(b, s), 1);
+            dev::mbar_init(p_full(b), 8);             // every softmax warp wrote its P rows
+            dev::mbar_init(o_free(b), 4);             // the q-tile's four warps read O
         }
         dev::fence_barrier_init();
     }
@@ -182,26 +181,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     auto tS = [&](int b, int w) { return tmem + (uint32_t)((2 * b + w) * BN); };
     auto tO = [&](int w) { return tmem + 256u + (uint32_t)(w * D); };
 
-    // Physical block ids of K/V tile j of a unit (-1: past the unit's last needed block, or
-    // flagged as outside the pool) and how many are valid.
-    auto tile_ids = [&](const Unit &un, int j, int (&ids)[BN / BS]) {
+    // Block-table entries of K/V tile j of a unit, fetched a tile ahead of their use so that
+    // the table's load latency stays off the producers' path (INT_MIN: past the unit's last
+    // needed block).  resolve() checks them: -1 for a block not loaded, which an entry
+    // outside the pool also flags.
+    auto fetch_ids = [&](const Unit &un, int j, int (&raw)[BN / BS]) {
         const int nblk = un.kmax / BS + 1;                   // blocks holding keys 0..kmax
-        int n = 0;
 #pragma unroll
         for (int i = 0; i < BN / BS; ++i) {
             const int blk = j * (BN / BS) + i;
-            int id = -1;
-            if (blk < nblk && blk < p.MB) {
-                id = __ldg(p.tables + (size_t)un.b * p.MB + blk);
-                if (id < 0 || id >= p.num_blocks) {
-                    dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-                    id = -1;
-                }
-            }
-            ids[i] = id;
-            n += id >= 0;
+            raw[i] = (blk < nblk && blk < p.MB) ? __ldg(p.tables + (size_t)un.b * p.MB + blk) : INT_MIN;
         }
-        return n;
+    };
+    auto resolve = [&](int id) {
+        if (id == INT_MIN) return -1;
+        if (id < 0 || id >= p.num_blocks) {
+            dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+            return -1;
+        }
+        return id;
     };
 
     if (warp == 11) {
@@ -229,35 +227,57 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // is needed until P.V: a K stage is held for about a load plus S, not for a whole
         // tile's pipeline.  Q has a producer of its own so that the K ring runs ahead into
         // the next unit while the current one finishes.
-        if (lane == 0) {
+        if (lane == 0 && u0 < u1) {
             const bool isk = warp == 0;
             const CUtensorMap *map = isk ? &kmap : &vmap;
             int J = 0, arms[NSTAGE] = {};
             bool ok = true;
-            for (int u = u0; u < u1 && ok; ++u) {
-                const Unit un = units[u];
-                for (int j = 0; j < un.nkv; ++j, ++J) {
-                    const int s = J % NSTAGE;
-                    if (J >= NSTAGE) {            // the stage's previous tile: S done (K), P.V done (V)
-                        const uint32_t par = ((J - NSTAGE) / NSTAGE) & 1;
-                        ok = isk ? dev::mbar_wait_bounded(k_free(s), par)
-                                 : dev::mbar_wait_bounded(o_done(0, s), par) && dev::mbar_wait_bounded(o_done(1, s), par);
-                        if (!ok) break;
-                    }
-                    int ids[BN / BS];
-                    const int n = tile_ids(un, j, ids);
-                    const uint32_t full = isk ? k_full(s) : v_full(s);
-                    const uint32_t dst = base + (isk ? L::K : L::V) + s * L::KSTAGE;
-                    dev::mbar_arrive_expect_tx(full, (uint32_t)(n * H * BS * 128));
-                    ++arms[s];
-#pragma unroll
-                    for (int i = 0; i < BN / BS; ++i) {
-                        if (ids[i] < 0) continue;
-                        const int z = ids[i] * p.Hkv + un.h;
-                        for (int hf = 0; hf < H; ++hf)
-                            tc::tma_load_3d(dst + hf * L::KHALF + i * BS * 128, map, hf * 64, 0, z, full);
-                    }
+            // cursor (u, j) over this CTA's tiles; the next tile's entries are in flight while
+            // the current one waits for its stage
+            int u = u0, j = 0;
+            Unit un = units[u];
+            int raw[BN / BS];
+            fetch_ids(un, 0, raw);
+            while (ok) {
+                int un_idx = u, jn = j + 1;
+                Unit nx = un;
+                if (jn == un.nkv) {
+                    ++un_idx;
+                    jn = 0;
+                    if (un_idx < u1) nx = units[un_idx];
                 }
+                int rawn[BN / BS];
+                if (un_idx < u1) fetch_ids(nx, jn, rawn);
+                const int s = J % NSTAGE;
+                if (J >= NSTAGE) {            // the stage's previous tile: S done (K), P.V done (V)
+                    const uint32_t par = ((J - NSTAGE) / NSTAGE) & 1;
+                    ok = isk ? dev::mbar_wait_bounded(k_free(s), par) : dev::mbar_wait_bounded(o_done(s), par);
+                    if (!ok) break;
+                }
+                int ids[BN / BS], n = 0;
+#pragma unroll
+                for (int i = 0; i < BN / BS; ++i) {
+                    ids[i] = resolve(raw[i]);
+                    n += ids[i] >= 0;
+                }
+                const uint32_t full = isk ? k_full(s) : v_full(s);
+                const uint32_t dst = base + (isk ? L::K : L::V) + s * L::KSTAGE;
+                dev::mbar_arrive_expect_tx(full, (uint32_t)(n * H * BS * 128));
+                ++arms[s];
+#pragma unroll
+                for (int i = 0; i < BN / BS; ++i) {
+                    if (ids[i] < 0) continue;
+                    const int z = ids[i] * p.Hkv + un.h;
+                    for (int hf = 0; hf < H; ++hf)
+                        tc::tma_load_3d(dst + hf * L::KHALF + i * BS * 128, map, hf * 64, 0, z, full);
+                }
+                ++J;
+                if (un_idx >= u1) break;
+                u = un_idx;
+                j = jn;
+                un = nx;
+#pragma unroll
+                for (int i = 0; i < BN / BS; ++i) raw[i] = rawn[i];
             }
             if (!ok) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
             // no copy may land after the CTA has left: wait (bounded) for the last of each
@@ -290,14 +310,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     for (int j = 0; j < un.nkv; ++j, ++J) {
                         const int st = J % NSTAGE;
                         if (!wait(k_full(st), (J / NSTAGE) & 1)) break;
-                        if (J >= 2) {
-                            // the softmax has read S(J-2) and P.V(J-2) has read P(J-2)
-                            const int s2 = (J - 2) % NSTAGE;
-                            const uint32_t p2 = ((J - 2) / NSTAGE) & 1;
-                            if (!wait(s_free(J & 1), ((J - 2) >> 1) & 1) || !wait(o_done(0, s2), p2) ||
-                                !wait(o_done(1, s2), p2))
-                                break;
-                        }
+                        // P.V(J-2) has read P(J-2), so the softmax is done with S(J-2) as well
+                        if (J >= 2 && !wait(o_done((J - 2) % NSTAGE), ((J - 2) / NSTAGE) & 1)) break;
                         tc::fence_after_sync();
                         const uint64_t dk = tc::desc_add(dK, (uint32_t)st * L::KSTAGE);
                         const uint32_t ts = tS(J & 1, 0);
@@ -323,9 +337,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         const int st = J % NSTAGE;
                         if (!wait(v_full(st), (J / NSTAGE) & 1)) break;
                         const uint64_t dv = tc::desc_add(dV, (uint32_t)st * L::KSTAGE);
+                        if (!wait(p_full(J), (J >> 1) & 1)) break;          // P(J) of both q-tiles
                         for (int w = 0; w < 2; ++w) {
-                            // P(J) of the q-tile; first in a unit, its previous output was read
-                            if (!wait(p_full(w, J), (J >> 1) & 1)) break;
+                            // first in a unit: the q-tile's previous output has been read
                             if (j == 0 && uq > 0 && !wait(o_free(w), (uq - 1) & 1)) break;
                             tc::fence_after_sync();
                             const uint32_t tp = tS(J & 1, w), to = tO(w);
@@ -333,8 +347,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                             for (int k = 0; k < BN / 16; ++k)
                                 tc::mma_bf16_ts(to, tp + (uint32_t)(k * 8), tc::desc_add(dv, k * 16 * 128), IDO,
                                                 j > 0 || k > 0);
-                            tc::commit(o_done(w, st));
                         }
+                        tc::commit(o_done(st));
                     }
                 }
             }
@@ -375,9 +389,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         x[32 + i] = __uint_as_float(v1[i]);
                     }
                 }
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) dev::mbar_arrive(s_free(J & 1));   // the buffer may be reused
                 const int kb = j * BN;
                 if (kb + BN - 1 > un.pos0) {                  // the causal diagonal crosses the tile
 #pragma unroll
@@ -411,7 +422,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 tc::tmem_st32(tS(J & 1, w) + lane_off, pw);
                 if (__any_sync(dev::FULL, rescale)) {
                     // O may be rescaled only once the previous P.V has accumulated into it
-                    ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(o_done(w, (J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1));
+                    ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(o_done((J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1));
                     if (!ok) break;
                     tc::fence_after_sync();
 #pragma unroll 1
@@ -443,11 +454,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) dev::mbar_arrive(p_full(w, J));
+                if (lane == 0) dev::mbar_arrive(p_full(J));
             }
             if (!ok) break;
             // epilogue: O / l of this row, bf16, to out[row0 + pl][h*g + hh]
-            ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(o_done(w, (J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1));
+            ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(o_done((J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1));
             if (!ok) break;
             tc::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
