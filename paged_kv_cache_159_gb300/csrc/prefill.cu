@@ -73,7 +73,7 @@ namespace prefill {
 constexpr int BM = 128;            // query rows per q-tile (two q-tiles per unit)
 constexpr int BN = 64;             // keys per KV tile (4 blocks)
 constexpr int BS = 16;             // tokens per block
-constexpr int NTHREADS = 416;      // warp 0 K loads, 1 S MMAs, 2-9 softmax + epilogue, 10 V, 11 Q loads, 12 P.V MMAs
+constexpr int NTHREADS = 480;      // warp 0 K loads, 1 and 12 S MMAs, 2-9 softmax + epilogue, 10 V, 11 Q loads, 13-14 P.V MMAs
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float TAU = 8.0f;        // raise the running max only beyond 2^8
 constexpr uint32_t PLAN_MAGIC = 0x504b5650u;   // "PVKP"
@@ -107,10 +107,10 @@ struct Smem {
     static constexpr int KSTAGE = H * KHALF;          // one K (or V) tile
     static constexpr int K = Q + H * QHALF;           // NS K tiles
     static constexpr int V = K + NS * KSTAGE;         // NS V tiles
-    static constexpr int BAR = V + NS * KSTAGE;       // 8 + 4 NS mbarriers, then the TMEM slot
+    static constexpr int BAR = V + NS * KSTAGE;       // 12 + 4 NS mbarriers, then the TMEM slot
     static constexpr int TOTAL = BAR + 512;
     static constexpr int ALLOC = TOTAL + 1024;        // alignment slack
-    static_assert(8 * (8 + 4 * NS) + 4 <= 512, "barrier area");
+    static_assert(8 * (12 + 4 * NS) + 4 <= 512, "barrier area");
     static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
@@ -127,9 +127,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const uint32_t base = dev::smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // mbarriers: q_full, q_free (a unit's last S is done with Q); k_full, v_full, k_free
-    // [NSTAGE]; s_full [2 S buffers]; p_full [2 tile parities] (all eight softmax warps wrote
-    // P); o_done [NSTAGE] (both q-tiles' P.V of the stage's tile are complete); o_free [2
-    // q-tiles] (the epilogue has read O).
+    // [NSTAGE]; s_full [2 q-tiles][2 tile parities]; p_full [2 q-tiles][2 tile parities]
+    // (the q-tile's four softmax warps wrote P); o_done [NSTAGE] (both q-tiles' P.V of the
+    // stage's tile are complete); o_free [2 q-tiles] (the epilogue has read O).
     // p_full alternates by tile: the softmax does not wait for the previous P.V, so it can
     // finish tile J+1 before the P.V issuer has seen tile J's P, and a single barrier would
     // then run two phases ahead of its waiter.  S(J) waits for o_done of tile J-2, which
@@ -140,11 +140,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     auto k_full = [&](int s) { return bars + 8 * (2 + s); };
     auto v_full = [&](int s) { return bars + 8 * (2 + NSTAGE + s); };
     auto k_free = [&](int s) { return bars + 8 * (2 + 2 * NSTAGE + s); };
-    auto s_full = [&](int b) { return bars + 8 * (2 + 3 * NSTAGE + b); };
-    auto p_full = [&](int J) { return bars + 8 * (4 + 3 * NSTAGE + (J & 1)); };
-    auto o_done = [&](int s) { return bars + 8 * (6 + 3 * NSTAGE + s); };
-    auto o_free = [&](int w) { return bars + 8 * (6 + 4 * NSTAGE + w); };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (8 + 4 * NSTAGE));
+    auto s_full = [&](int w, int J) { return bars + 8 * (2 + 3 * NSTAGE + 2 * w + (J & 1)); };
+    auto p_full = [&](int w, int J) { return bars + 8 * (6 + 3 * NSTAGE + 2 * w + (J & 1)); };
+    auto o_done = [&](int s) { return bars + 8 * (10 + 3 * NSTAGE + s); };
+    auto o_free = [&](int w) { return bars + 8 * (10 + 4 * NSTAGE + w); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (12 + 4 * NSTAGE));
 
     const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(p.plan);
     const int32_t *cta_off = reinterpret_cast<const int32_t *>(p.plan + sizeof(PlanHeader));
@@ -158,16 +158,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     if (tid == 0) {
         dev::mbar_init(q_full, 1);
-        dev::mbar_init(q_free, 1);
+        dev::mbar_init(q_free, 2);                    // both S issuers' last S of a unit
         for (int s = 0; s < NSTAGE; ++s) {
             dev::mbar_init(k_full(s), 1);
             dev::mbar_init(v_full(s), 1);
-            dev::mbar_init(k_free(s), 1);
-            dev::mbar_init(o_done(s), 1);
+            dev::mbar_init(k_free(s), 2);             // both q-tiles' S of the stage's tile
+            dev::mbar_init(o_done(s), 2);             // both q-tiles' P.V of the stage's tile
         }
         for (int b = 0; b < 2; ++b) {
-            dev::mbar_init(s_full(b), 1);
-            dev::mbar_init(p_full(b), 8);             // every softmax warp wrote its P rows
+            dev::mbar_init(s_full(b, 0), 1);
+            dev::mbar_init(s_full(b, 1), 1);
+            dev::mbar_init(p_full(b, 0), 4);          // the q-tile's four softmax warps wrote P
+            dev::mbar_init(p_full(b, 1), 4);
             dev::mbar_init(o_free(b), 4);             // the q-tile's four warps read O
         }
         dev::fence_barrier_init();
@@ -284,25 +286,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             for (int s = 0; s < NSTAGE; ++s)
                 if (arms[s]) (void)dev::mbar_wait_bounded(isk ? k_full(s) : v_full(s), (arms[s] - 1) & 1);
         }
-    } else if (warp == 1 || warp == 12) {
-        // ============ MMA issuers: warp 1 the S products, warp 12 the P.V products ============
-        // Two issuing threads, so that one waits for its next inputs while the other's
-        // products keep the tensor pipe busy: the pipe accepts only a few instructions ahead,
-        // and a single thread that waited between batches left it idle.  The S of tile J
-        // overwrites the tensor memory that P(J-2) was read from, so it waits for P.V(J-2)
-        // to be complete.  Every wait is on work issued before it (no cycle); about 1 s
-        // without progress ends the launch.
+    } else if (warp == 1 || warp >= 12) {
+        // ============ MMA issuers: per q-tile w, one thread issues S and one P.V ============
+        // Warps 1 and 12 issue S of q-tiles 0 and 1, warps 13 and 14 their P.V.  One thread
+        // issues a tcgen05.mma only about every 36 ns whatever its shape, longer than the pipe
+        // needs for a 128 x 64 x 16 product, so four threads share the issue.  The S of tile J
+        // overwrites the tensor memory that P(J-2) was read from, so it waits for the P.V of
+        // tile J-2 to be complete.  Every wait is on work issued before it (no cycle); about
+        // 1 s without progress ends the launch.
         if (lane == 0) {
+            const bool is_s = warp == 1 || warp == 12;
+            const int w = (warp == 1 || warp == 13) ? 0 : 1;
             int J = 0, uq = 0;
             bool ok = true;
             auto wait = [&](uint32_t bar, uint32_t par) {
                 if (ok && !dev::mbar_wait_bounded(bar, par)) ok = false;
                 return ok;
             };
-            if (warp == 1) {
+            if (is_s) {
                 constexpr uint32_t IDS = tc::idesc_bf16(BM, BN, 0);   // S = Q K^T: M 128, N 64 keys
                 // The operand descriptors are built once; each MMA adds its offset.
-                const uint64_t dQ = tc::smem_desc_sw128(base + L::Q, 16, 1024);
+                const uint64_t dQ = tc::desc_add(tc::smem_desc_sw128(base + L::Q, 16, 1024), (uint32_t)w * 16384);
                 const uint64_t dK = tc::smem_desc_sw128(base + L::K, 16, 1024);
                 for (int u = u0; u < u1 && ok; ++u, ++uq) {
                     const Unit un = units[u];
@@ -314,41 +318,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         if (J >= 2 && !wait(o_done((J - 2) % NSTAGE), ((J - 2) / NSTAGE) & 1)) break;
                         tc::fence_after_sync();
                         const uint64_t dk = tc::desc_add(dK, (uint32_t)st * L::KSTAGE);
-                        const uint32_t ts = tS(J & 1, 0);
+                        const uint32_t ts = tS(J & 1, w);
 #pragma unroll
-                        for (int w = 0; w < 2; ++w)
-#pragma unroll
-                            for (int k = 0; k < 4 * H; ++k) {
-                                const uint32_t hf = k >> 2, kk = (k & 3) * 32;
-                                tc::mma_bf16(ts + (uint32_t)(w * BN), tc::desc_add(dQ, hf * L::QHALF + w * 16384 + kk),
-                                             tc::desc_add(dk, hf * L::KHALF + kk), IDS, k > 0);
-                            }
-                        tc::commit(s_full(J & 1));
-                        tc::commit(k_free(st));                      // the K tile may be reloaded
-                        if (j == un.nkv - 1) tc::commit(q_free);     // the unit is done with Q
+                        for (int k = 0; k < 4 * H; ++k) {
+                            const uint32_t hf = k >> 2, kk = (k & 3) * 32;
+                            tc::mma_bf16(ts, tc::desc_add(dQ, hf * L::QHALF + kk), tc::desc_add(dk, hf * L::KHALF + kk),
+                                         IDS, k > 0);
+                        }
+                        tc::commit(s_full(w, J));
+                        tc::commit(k_free(st));                      // (both q-tiles) the K tile may be reloaded
+                        if (j == un.nkv - 1) tc::commit(q_free);     // (both q-tiles) the unit is done with Q
                     }
                 }
             } else {
                 constexpr uint32_t IDO = tc::idesc_bf16(BM, D, 1);    // O += P V: M 128, N D, V MN-major
                 const uint64_t dV = tc::smem_desc_sw128(base + L::V, L::KHALF, 1024);
+                const uint32_t to = tO(w);
                 for (int u = u0; u < u1 && ok; ++u, ++uq) {
                     const Unit un = units[u];
-                    for (int j = 0; j < un.nkv && ok; ++j, ++J) {
+                    for (int j = 0; j < un.nkv; ++j, ++J) {
                         const int st = J % NSTAGE;
-                        if (!wait(v_full(st), (J / NSTAGE) & 1)) break;
+                        if (!wait(v_full(st), (J / NSTAGE) & 1) || !wait(p_full(w, J), (J >> 1) & 1)) break;
+                        // first in a unit: the q-tile's previous output has been read
+                        if (j == 0 && uq > 0 && !wait(o_free(w), (uq - 1) & 1)) break;
+                        tc::fence_after_sync();
                         const uint64_t dv = tc::desc_add(dV, (uint32_t)st * L::KSTAGE);
-                        if (!wait(p_full(J), (J >> 1) & 1)) break;          // P(J) of both q-tiles
-                        for (int w = 0; w < 2; ++w) {
-                            // first in a unit: the q-tile's previous output has been read
-                            if (j == 0 && uq > 0 && !wait(o_free(w), (uq - 1) & 1)) break;
-                            tc::fence_after_sync();
-                            const uint32_t tp = tS(J & 1, w), to = tO(w);
+                        const uint32_t tp = tS(J & 1, w);
 #pragma unroll
-                            for (int k = 0; k < BN / 16; ++k)
-                                tc::mma_bf16_ts(to, tp + (uint32_t)(k * 8), tc::desc_add(dv, k * 16 * 128), IDO,
-                                                j > 0 || k > 0);
-                        }
-                        tc::commit(o_done(st));
+                        for (int k = 0; k < BN / 16; ++k)
+                            tc::mma_bf16_ts(to, tp + (uint32_t)(k * 8), tc::desc_add(dv, k * 16 * 128), IDO, j > 0 || k > 0);
+                        tc::commit(o_done(st));                      // (both q-tiles)
                     }
                 }
             }
@@ -374,7 +373,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const int qpos = un.pos0 + pl;                 // keys 0..qpos are visible
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < un.nkv; ++j, ++J) {
-                ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(s_full(J & 1), (J >> 1) & 1));
+                ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(s_full(w, J), (J >> 1) & 1));
                 if (!ok) break;
                 tc::fence_after_sync();
                 float x[BN];
@@ -454,7 +453,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) dev::mbar_arrive(p_full(J));
+                if (lane == 0) dev::mbar_arrive(p_full(w, J));
             }
             if (!ok) break;
             // epilogue: O / l of this row, bf16, to out[row0 + pl][h*g + hh]
