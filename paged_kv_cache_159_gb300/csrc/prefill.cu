@@ -38,8 +38,9 @@
 //   * Feeding the tensor pipe sets the pace: it accepts only a few instructions ahead, a
 //     128 x 64 x 16 MMA takes about 36 ns and a 128 x 128 x 16 one about 56 ns, and each
 //     satisfied mbarrier wait of the issuing thread costs about 70 ns.  One thread that
-//     waited for its inputs between batches left the pipe idle about 40 % of each tile; two
-//     issuing threads (S and P.V) overlap one's waits with the other's products.
+//     waited for its inputs between batches left the pipe idle about 40 % of each tile; four
+//     issuing threads (S and P.V for each q-tile) overlap one's waits with the others'
+//     products.
 //   * Keeping P out of shared memory leaves the room for deeper rings and takes P's stores
 //     and the tensor core's reads of it off the shared-memory port, and the softmax no
 //     longer waits for the previous P.V before writing P (only a rescale of O does).
