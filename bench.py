@@ -51,12 +51,21 @@ def _hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_source_hash() -> str:
+def code_hash(names) -> str:
+    """sha256 (16 hex digits) of the named csrc files' code: // comments, trailing blanks and
+    empty lines are dropped, so an edit to comments alone keeps a profile's counters valid."""
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_159_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    for name in names:
+        with open(os.path.join(ROOT, "paged_kv_cache_159_gb300", "csrc", name)) as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
+
+
+def decode_source_hash() -> str:
+    return code_hash(DECODE_SOURCES)
 
 
 def _profiled_traffic(workload: str):
@@ -577,11 +586,7 @@ def _prefill_traffic(workload: str):
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
     s = re.search(r"prefill_source_sha256_16:\s*([0-9a-f]+)", text)
-    h = hashlib.sha256()
-    for name in PREFILL_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_159_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    if not m or not s or s.group(1) != h.hexdigest()[:16]:
+    if not m or not s or s.group(1) != code_hash(PREFILL_SOURCES):
         return None
     return int(m.group(1))
 
