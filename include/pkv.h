@@ -332,7 +332,7 @@ int pkv_decode_step_layers(pkv_pool *pool, const void *q, const void *k_new, con
  * plan's size for batch sequences and total_q packed rows (0 if the shape is invalid).
  * pkv_prefill_plan: cu_q (host int32 [batch+1], cu_q[0] = 0) and seq_lens (host int32
  * [batch], each >= its P_b, >= 1, needing at most max_blocks table entries) give the units
- * (sequence, KV head, tile of 128 / g query positions) and their assignment to a one-wave
+ * (sequence, KV head, tile of 256 / g query positions) and their assignment to a one-wave
  * persistent grid, heaviest unit first to the least-loaded CTA; plan_out (host,
  * plan_bytes) receives it and *grid_out the grid.  The caller copies the plan to device
  * memory (32-byte aligned) for pkv_paged_prefill.  Requires Hq a multiple of Hkv with
@@ -350,7 +350,8 @@ int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const int32_t *s
  * tensor memory, P in bf16.  Positions a row may not see are never used, whatever the
  * cache holds there.  A plan that does not match the call sets PKV_DEVERR_PLAN and
  * computes nothing; a table entry outside the pool sets PKV_DEVERR_BLOCK_ID (that
- * sequence's rows are then unspecified). */
+ * sequence's rows are then unspecified); a wait inside the kernel that runs out (about 1 s)
+ * sets PKV_DEVERR_TIMEOUT and the launch ends. */
 int pkv_paged_prefill(pkv_pool *pool, const void *q, const void *key_cache, const void *value_cache,
                       const int32_t *block_tables, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
                       int32_t total_q, float scale, const void *plan, int32_t grid, void *out, void *stream);
