@@ -601,6 +601,10 @@ extern "C" int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const
     const int grid = std::max(1, std::min<int>(sms, (int)units.size()));
     const size_t need = plan_units_offset(grid) + units.size() * sizeof(Unit);
     if (need > plan_bytes) return PKV_ERR_INVALID;
+    // A unit costs its K/V tiles plus about three tile-times of its own: waiting for its Q
+    // rows, the S -> softmax -> P.V chain filling and draining, and writing its output
+    // (per-CTA end times fit 2.5 to 4 tiles per unit).
+    auto cost = [&](int i) { return (int64_t)units[(size_t)i].nkv + 3; };
     // longest processing time first: heaviest unit to the least-loaded CTA
     std::vector<int> order(units.size());
     for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
@@ -610,13 +614,49 @@ extern "C" int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const
     std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
     for (int c = 0; c < grid; ++c) heap.push({0, c});
     std::vector<std::vector<int>> per(grid);
+    std::vector<int64_t> load(grid, 0);
     for (int i : order) {
         Load top = heap.top();
         heap.pop();
         per[(size_t)top.second].push_back(i);
-        top.first += units[(size_t)i].nkv + 2;            // + Q load and epilogue
+        top.first += cost(i);
+        load[(size_t)top.second] = top.first;
         heap.push(top);
     }
+    // Then move a unit, or swap two, between the most and the least loaded CTA while that
+    // lowers the larger of their two loads (each step lowers the multiset of loads, so it
+    // ends).
+    for (int it = 0; it < 16 * grid; ++it) {
+        const int ca = (int)(std::max_element(load.begin(), load.end()) - load.begin());
+        const int cb = (int)(std::min_element(load.begin(), load.end()) - load.begin());
+        const int64_t la = load[(size_t)ca], lb = load[(size_t)cb];
+        int64_t best = la;
+        int bi = -1, bj = -1;                                   // unit of ca, unit of cb (-1: none)
+        for (size_t x = 0; x < per[(size_t)ca].size(); ++x) {
+            const int i = per[(size_t)ca][x];
+            const int64_t d = cost(i);
+            if (std::max(la - d, lb + d) < best) { best = std::max(la - d, lb + d); bi = (int)x; bj = -1; }
+            for (size_t y = 0; y < per[(size_t)cb].size(); ++y) {
+                const int64_t e2 = d - cost(per[(size_t)cb][y]);
+                if (e2 > 0 && std::max(la - e2, lb + e2) < best) { best = std::max(la - e2, lb + e2); bi = (int)x; bj = (int)y; }
+            }
+        }
+        if (bi < 0) break;
+        const int i = per[(size_t)ca][(size_t)bi];
+        per[(size_t)ca].erase(per[(size_t)ca].begin() + bi);
+        load[(size_t)ca] -= cost(i);
+        load[(size_t)cb] += cost(i);
+        if (bj >= 0) {
+            const int j = per[(size_t)cb][(size_t)bj];
+            per[(size_t)cb].erase(per[(size_t)cb].begin() + bj);
+            per[(size_t)ca].push_back(j);
+            load[(size_t)cb] -= cost(j);
+            load[(size_t)ca] += cost(j);
+        }
+        per[(size_t)cb].push_back(i);
+    }
+    for (auto &v : per)                                         // heaviest first within a CTA
+        std::stable_sort(v.begin(), v.end(), [&](int a, int b) { return units[(size_t)a].nkv > units[(size_t)b].nkv; });
     uint8_t *out = static_cast<uint8_t *>(plan_out);
     PlanHeader hdr{PLAN_MAGIC, (int32_t)units.size(), grid, g, tp, num_q_heads, Hkv, 0};
     std::memcpy(out, &hdr, sizeof(hdr));
