@@ -625,7 +625,9 @@ extern "C" int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const
     }
     // Then move a unit, or swap two, between the most and the least loaded CTA while that
     // lowers the larger of their two loads (each step lowers the multiset of loads, so it
-    // ends).
+    // ends).  With many units per CTA the greedy pass is already fine-grained: swaps are
+    // searched only up to 64 units per CTA, which bounds the host time.
+    const bool swaps = units.size() <= (size_t)64 * grid;
     for (int it = 0; it < 16 * grid; ++it) {
         const int ca = (int)(std::max_element(load.begin(), load.end()) - load.begin());
         const int cb = (int)(std::min_element(load.begin(), load.end()) - load.begin());
@@ -636,7 +638,7 @@ extern "C" int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const
             const int i = per[(size_t)ca][x];
             const int64_t d = cost(i);
             if (std::max(la - d, lb + d) < best) { best = std::max(la - d, lb + d); bi = (int)x; bj = -1; }
-            for (size_t y = 0; y < per[(size_t)cb].size(); ++y) {
+            for (size_t y = 0; swaps && y < per[(size_t)cb].size(); ++y) {
                 const int64_t e2 = d - cost(per[(size_t)cb][y]);
                 if (e2 > 0 && std::max(la - e2, lb + e2) < best) { best = std::max(la - e2, lb + e2); bi = (int)x; bj = (int)y; }
             }
