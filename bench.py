@@ -475,11 +475,41 @@ def cpu_baseline(w, sample_seqs=64, threads=None, reps=3):
         t.append(time.perf_counter() - t0)
     sec = min(t)
     kv_read = int(d.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    # the same decode on one core, over the first sequences of the sample (at most 8)
+    n1 = min(8, sample_seqs)
+    pairs = np.array([[b, h] for b in range(n1) for h in range(w.num_q_heads)], dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.paged_decode(q, kb, vb, tables, d.seq_lens, w.scale, w.num_kv_heads, pairs=pairs, num_threads=1)
+    sec1 = time.perf_counter() - t0
+    kv1 = int(d.seq_lens[:n1].astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 2 * 2
     return {"value": round(kv_read / sec / 1e9, 4), "unit": "GB/s", "cores": int(threads),
             "kind": "oracle",
             "sample": "%d of %d sequences (all %d query heads), kv_append + fp64 decode, best of %d: %.3f s"
                       % (sample_seqs, w.batch, w.num_q_heads, reps, sec),
-            "query_tokens_per_s": round(sample_seqs / sec, 2)}
+            "query_tokens_per_s": round(sample_seqs / sec, 2),
+            "value_1core": round(kv1 / sec1 / 1e9, 4),
+            "sample_1core": "%d sequences, fp64 decode on one core: %.3f s" % (n1, sec1),
+            "cpu": _cpu_model()}
+
+
+def _cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, or the Arm implementer and part)."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k, v = k.strip(), v.strip()
+                if k and v and k not in fields:
+                    fields[k] = v
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return "%s, CPU implementer %s, part %s" % (platform.machine(), fields.get("CPU implementer", "?"), fields["CPU part"])
+    return platform.machine()
 
 
 def run_reference(args):
