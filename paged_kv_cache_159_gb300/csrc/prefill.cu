@@ -395,29 +395,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 #pragma unroll
                     for (int c = 0; c < BN; ++c) x[c] = (valid && kb + c <= qpos) ? x[c] : -INFINITY;
                 }
-                float mx0 = x[0], mx1 = x[1];
+                float mx4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-                for (int c = 2; c < BN; c += 2) {
-                    mx0 = fmaxf(mx0, x[c]);
-                    mx1 = fmaxf(mx1, x[c + 1]);
-                }
-                const float mx = fmaxf(mx0, mx1) * p.score_scale;   // scale > 0: max commutes
+                for (int c = 4; c < BN; c += 8)
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) mx4[t] = tc::fmax3(mx4[t], x[c + t], x[c + 4 + t]);
+                const float mx = tc::fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * p.score_scale;   // scale > 0: max commutes
                 const bool raise = mx > m + TAU;
                 const bool rescale = raise && m != -INFINITY;
                 const float f = rescale ? dev::fast_exp2(m - mx) : 1.f;
                 if (raise) m = mx;
                 // P = exp2(x * scale - m) as packed bf16 (the lower key in the low half)
                 const float nm = m == -INFINITY ? 0.f : -m;
+                // (packed pairs: one fma and one add per two keys)
                 uint32_t pw[BN / 2];
-                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                const float2 sc2 = make_float2(p.score_scale, p.score_scale), nm2 = make_float2(nm, nm);
+                float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int e = 0; e < BN / 2; ++e) {
-                    const float a = dev::fast_exp2(fmaf(x[2 * e], p.score_scale, nm));
-                    const float b2 = dev::fast_exp2(fmaf(x[2 * e + 1], p.score_scale, nm));
-                    ps[e & 3] += a + b2;
-                    pw[e] = dev::pack_bf16x2(a, b2);
+                    const float2 t = tc::ffma2(make_float2(x[2 * e], x[2 * e + 1]), sc2, nm2);
+                    const float2 pe = make_float2(dev::fast_exp2(t.x), dev::fast_exp2(t.y));
+                    ps[e & 1] = tc::fadd2(ps[e & 1], pe);
+                    pw[e] = dev::pack_bf16x2(pe.x, pe.y);
                 }
-                l = l * f + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+                const float2 ps2 = tc::fadd2(ps[0], ps[1]);
+                l = l * f + (ps2.x + ps2.y);
                 // P over this tile's S columns (already read): the A operand of this tile's
                 // P.V.  No wait: the previous P.V reads the other S buffer.
                 tc::tmem_st32(tS(J & 1, w) + lane_off, pw);
