@@ -510,6 +510,40 @@ def decode_step_host(pool: Pool, host: dict, dev: dict, key_cache, value_cache, 
                                       ctypes.byref(o) if o else None, _stream_ptr(stream)), "decode_step_host")
 
 
+class DecodeStepHost:
+    """decode_step_host prepared once for a fixed set of buffers (a serving loop reuses the
+    same pinned host and device buffers every step and refills their contents).  The pointer
+    structures are built and checked here; each run() is one pkv_decode_step_host call, which
+    still copies every input in and the output back.  The tensors must stay alive and in
+    place while the object is used."""
+
+    def __init__(self, pool: Pool, host: dict, dev: dict, key_cache, value_cache, scale: float, workspace,
+                 opts=None, stream=None):
+        B, Hq, _ = dev["q"].shape
+        self._keep = (pool, host, dev, key_cache, value_cache, workspace)
+        self._h = host_step(_host_ptr(host["q"], "q"), _host_ptr(host.get("k_new"), "k_new"),
+                            _host_ptr(host.get("v_new"), "v_new"),
+                            _host_ptr(host.get("block_tables"), "block_tables"),
+                            _host_ptr(host.get("seq_lens"), "seq_lens"), _host_ptr(host["out"], "out"),
+                            int(bool(host.get("contiguous", False))))
+        self._d = device_step(*[(_dev_ptr(dev.get(k), k).value if dev.get(k) is not None else None)
+                                for k in ("q", "k_new", "v_new", "block_tables", "seq_lens", "out")])
+        self._o = _opts(opts)
+        self._fn = lib().pkv_decode_step_host
+        self._args = (pool.handle, ctypes.byref(self._h), ctypes.byref(self._d), _dev_ptr(key_cache, "key_cache"),
+                      _dev_ptr(value_cache, "value_cache"), ctypes.c_int32(int(B)), ctypes.c_int32(int(Hq)),
+                      ctypes.c_int32(int(dev["block_tables"].shape[1])), ctypes.c_float(float(scale)),
+                      _dev_ptr(workspace, "workspace"),
+                      ctypes.c_size_t(int(workspace.numel() * workspace.element_size())),
+                      ctypes.byref(self._o) if self._o else None, _stream_ptr(stream))
+
+    def run(self):
+        """Issue one step (copies in, the one-launch decode, copy out) on the prepared stream."""
+        st = self._fn(*self._args)
+        if st:
+            _check(st, "decode_step_host")
+
+
 def paged_attention_decode_noalloc(pool: Pool, q, key_cache, value_cache, block_tables,
                                    seq_lens, scale: float, out, stream=None):
     """Decode without a workspace, for callers that cannot allocate device memory at run

@@ -281,11 +281,12 @@ def test_probe_copy():
     assert torch.equal(src, dst)
 
 
-@pytest.mark.parametrize("contiguous", [False, True])
+@pytest.mark.parametrize("contiguous,prepared", [(False, False), (True, False), (True, True)])
 @pytest.mark.parametrize("name", ["tiny", "llama3_8b", "qwen25_7b_prefix"])
-def test_decode_step_from_host_memory_equals_the_device_step(name, contiguous):
+def test_decode_step_from_host_memory_equals_the_device_step(name, contiguous, prepared):
     """pkv_decode_step_host (copies in, one-launch step, copy out, all from one call) gives
-    the same bits as pkv_decode_step on device buffers: output and pool."""
+    the same bits as pkv_decode_step on device buffers: output and pool.  `prepared` runs it
+    through DecodeStepHost (pointer structures built once, one C call per step)."""
     a = C.build(name)
     b = C.build(name)
     bt, sl, _ = C.device_tables(a)
@@ -319,7 +320,10 @@ def test_decode_step_from_host_memory_equals_the_device_step(name, contiguous):
             off += n
         host["contiguous"] = True
     stream = torch.cuda.current_stream()
-    pkv.decode_step_host(b.pool, host, dev, b.key_cache, b.value_cache, b.w.scale, ws_b, stream=stream)
+    if prepared:
+        pkv.DecodeStepHost(b.pool, host, dev, b.key_cache, b.value_cache, b.w.scale, ws_b, stream=stream).run()
+    else:
+        pkv.decode_step_host(b.pool, host, dev, b.key_cache, b.value_cache, b.w.scale, ws_b, stream=stream)
     stream.synchronize()
     for c in (a, b):
         st, bits = c.pool.get_device_error()
