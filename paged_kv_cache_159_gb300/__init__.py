@@ -21,6 +21,9 @@ Names follow the C ABI without the ``pkv_`` prefix:
   automatic prefix caching on the host.
 * ``slot_mapping_chunks``, ``prefill_plan``, ``paged_prefill`` -- prefill and chunked
   prefill on the tcgen05 tensor cores (plan on the host once per batch, run per layer).
+* ``decode_step_host`` -- one decode step from pinned host memory (upload, one-launch step,
+  download) in one C call; ``DecodeStepHost`` prepares that call once for a set of reused
+  buffers, so each ``run()`` is the C call alone.
 * ``decode_workspace_bytes``, ``probe_copy``, ``device_sm_count``.
 """
 from __future__ import annotations
