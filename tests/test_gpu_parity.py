@@ -281,6 +281,34 @@ def test_probe_copy():
     assert torch.equal(src, dst)
 
 
+def test_prepared_host_step_reads_the_refilled_host_buffers():
+    """A DecodeStepHost is built once for a set of buffers; each run() uploads what the host
+    buffers hold at that time (a serving loop refills them every step).  Two runs with
+    different queries give the device-buffer decode of each, bit for bit."""
+    c = C.build("qwen25_7b_prefix")
+    assert not c.w.append
+    bt, sl, _ = C.device_tables(c)
+    B, Hq, _ = c.q.shape
+    ws = torch.zeros(pkv.decode_workspace_bytes(c.pool, B, Hq, bt.shape[1]), dtype=torch.uint8, device="cuda")
+    pin = lambda t: t.detach().cpu().pin_memory()
+    host = {"q": pin(c.q), "block_tables": pin(bt), "seq_lens": pin(sl),
+            "out": torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()}
+    dev = {"q": torch.empty_like(c.q), "block_tables": torch.empty_like(bt), "seq_lens": torch.empty_like(sl),
+           "out": torch.empty_like(c.q)}
+    stream = torch.cuda.current_stream()
+    step = pkv.DecodeStepHost(c.pool, host, dev, c.key_cache, c.value_cache, c.w.scale, ws, stream=stream)
+    for q in (c.q, (c.q.float() * -0.5).to(torch.bfloat16)):
+        host["q"].copy_(q.cpu())
+        step.run()
+        stream.synchronize()
+        ref = torch.empty_like(c.q)
+        pkv.paged_attention_decode(c.pool, q, c.key_cache, c.value_cache, bt, sl, c.w.scale, ref, ws)
+        torch.cuda.synchronize()
+        st, bits = c.pool.get_device_error()
+        assert st == pkv.OK and bits == 0
+        assert torch.equal(host["out"].view(torch.int16), ref.cpu().view(torch.int16))
+
+
 @pytest.mark.parametrize("contiguous,prepared", [(False, False), (True, False), (True, True)])
 @pytest.mark.parametrize("name", ["tiny", "llama3_8b", "qwen25_7b_prefix"])
 def test_decode_step_from_host_memory_equals_the_device_step(name, contiguous, prepared):
