@@ -221,25 +221,28 @@ def run_ours(args, world, rank, local_rank):
     # the new rows
     launch_bytes = decode_bytes + (new_rows if w.append and not args.separate_append else 0)
 
-    def cow_call(stream=None):
+    # the step's device inputs; the end-to-end leg below passes views of one packed buffer
+    dev_in = {"q": d.q, "k": d.k_new, "v": d.v_new, "bt": bt, "sl": sl, "sm": sm, "cs": cow_src, "cd": cow_dst}
+
+    def cow_call(stream=None, t=dev_in):
         if len(cow_pairs):
-            pkv.copy_blocks(pool, kc, vc, cow_src, cow_dst, stream=stream)
+            pkv.copy_blocks(pool, kc, vc, t["cs"], t["cd"], stream=stream)
 
-    def append_call(stream=None):
+    def append_call(stream=None, t=dev_in):
         if nl > 1:
-            pkv.kv_append_layers(pool, d.k_new, d.v_new, sm, kc, vc, stream=stream)
+            pkv.kv_append_layers(pool, t["k"], t["v"], t["sm"], kc, vc, stream=stream)
         else:
-            pkv.kv_append(pool, d.k_new, d.v_new, sm, kc, vc, stream=stream)
+            pkv.kv_append(pool, t["k"], t["v"], t["sm"], kc, vc, stream=stream)
 
-    def decode_call(fused: bool, stream=None):
+    def decode_call(fused: bool, stream=None, t=dev_in):
         if nl > 1:
-            pkv.decode_step_layers(pool, d.q, d.k_new if fused else None, d.v_new if fused else None,
-                                   kc, vc, bt, sl, w.scale, out, ws, opts=decode_opts, stream=stream)
+            pkv.decode_step_layers(pool, t["q"], t["k"] if fused else None, t["v"] if fused else None,
+                                   kc, vc, t["bt"], t["sl"], w.scale, out, ws, opts=decode_opts, stream=stream)
         elif fused:
-            pkv.decode_step(pool, d.q, d.k_new, d.v_new, kc, vc, bt, sl, w.scale, out, ws,
+            pkv.decode_step(pool, t["q"], t["k"], t["v"], kc, vc, t["bt"], t["sl"], w.scale, out, ws,
                             opts=decode_opts, stream=stream)
         else:
-            pkv.paged_attention_decode(pool, d.q, kc, vc, bt, sl, w.scale, out, ws, opts=decode_opts,
+            pkv.paged_attention_decode(pool, t["q"], kc, vc, t["bt"], t["sl"], w.scale, out, ws, opts=decode_opts,
                                        stream=stream)
 
     # same-process bandwidth denominator: the library's copy probe over 2 x 1 GiB
@@ -353,6 +356,26 @@ def run_ours(args, world, rank, local_rank):
         # still one C call that uploads the inputs, decodes and downloads the output
         prepared = pkv.DecodeStepHost(pool, hstep, dstep, kc, vc, w.scale, ws, opts=decode_opts,
                                       stream=torch.cuda.current_stream())
+    else:
+        # the other steps (copy-on-write, a separate append, several layers): the inputs are
+        # packed the same way, one upload per step, and the library calls take views of the
+        # device copy
+        parts = [("q", host["q"])] + ([("k", host["k"]), ("v", host["v"])] if w.append else []) + \
+                [("bt", bt_h), ("sl", host["sl"])] + \
+                ([("cs", cow_src_h), ("cd", cow_dst_h)] if len(cow_pairs) else []) + \
+                ([("sm", sm_h)] if w.append and args.separate_append else [])
+        spans = [(t.numel() * t.element_size() + 15) // 16 * 16 for _, t in parts]   # 16-byte aligned views
+        hbuf = torch.empty(sum(spans), dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(sum(spans), dtype=torch.uint8, device=dev)
+        hview, dview, off = {}, dict(dev_in), 0
+        for (name, t), n in zip(parts, spans):
+            nb = t.numel() * t.element_size()
+            hview[name] = hbuf[off:off + nb].view(t.dtype).view(t.shape)
+            hview[name].copy_(t)
+            dview[name] = dbuf[off:off + nb].view(t.dtype).view(t.shape)
+            off += n
+        h2d = int(hbuf.numel())                   # the packed buffer is what is uploaded
+    ref_out = out.detach().cpu()                  # the timed steps' output
     for i in range(e2e_steps + 3):
         flush_l2()
         torch.cuda.synchronize()
@@ -364,33 +387,27 @@ def run_ours(args, world, rank, local_rank):
             if i >= 3:
                 e2e_t.append(ee[0].elapsed_time(ee[1]) * 1e-3)
             continue
-        if args.separate_append:
+        if w.append and args.separate_append:
             slots_np = pkv.slot_mapping(tables_host, d.seq_lens)        # host allocator side
-            sm_h[:] = torch.from_numpy(slots_np)
-        d.q.copy_(host["q"], non_blocking=True)
-        if len(cow_pairs):
-            cow_src.copy_(cow_src_h, non_blocking=True)
-            cow_dst.copy_(cow_dst_h, non_blocking=True)
-        bt.copy_(bt_h, non_blocking=True)
-        sl.copy_(host["sl"], non_blocking=True)
+            hview["sm"][:] = torch.from_numpy(slots_np)
+        dbuf.copy_(hbuf, non_blocking=True)                              # one upload
         if w.append:
-            d.k_new.copy_(host["k"], non_blocking=True)
-            d.v_new.copy_(host["v"], non_blocking=True)
-            cow_call()
+            cow_call(t=dview)
             if args.separate_append:
-                sm.copy_(sm_h, non_blocking=True)
-                append_call()
-                decode_call(False)
+                append_call(t=dview)
+                decode_call(False, t=dview)
             else:
-                decode_call(True)
+                decode_call(True, t=dview)
         else:
-            decode_call(False)
+            decode_call(False, t=dview)
         host["out"].copy_(out, non_blocking=True)
         ee[1].record()
         ee[1].synchronize()
         if i >= 3:
             e2e_t.append(ee[0].elapsed_time(ee[1]) * 1e-3)
     e2e_step = float(statistics.median(e2e_t))
+    if not torch.equal(host["out"].view(torch.int16), ref_out.view(torch.int16)):
+        raise RuntimeError("end-to-end decode output differs from the timed steps'")
 
     # ---- reduce over ranks (max time), aggregate bytes over ranks
     if world > 1:
@@ -435,7 +452,7 @@ def run_ours(args, world, rank, local_rank):
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_step * 1e3, 4),
                 "api": "DecodeStepHost.run (one pkv_decode_step_host call)" if one_call
-                       else "torch copies + library calls"},
+                       else "one packed upload + library calls on views of it"},
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 3),
