@@ -55,6 +55,15 @@ def test_prefill_edge_lengths(chunk, context):
                           "head_dim": 128, "seed": 159120 + chunk + context})
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_sequences_without_new_rows(D):
+    """Sequences whose chunk is empty this step (P_b = 0, context only) sit between others:
+    they get no units and no rows, and the rows around them are unchanged."""
+    _run("prefill_tiny", {"batch": 5, "head_dim": D, "num_q_heads": 8, "num_kv_heads": 2,
+                          "chunk_list": (40, 0, 129, 0, 1), "context_list": (37, 50, 0, 300, 16),
+                          "seed": 159130 + D})
+
+
 def test_prefill_llama3_8b_full_size_sampled():
     """8 prompts of 2048 positions, Llama-3-8B layer shape: rows at the edges of blocks, query
     tiles and KV tiles of every sequence, checked against the oracle one by one."""

@@ -206,6 +206,8 @@ class PrefillWorkload:
     context: int = 0             # C_b = context for every sequence, or U{0..context}
     ragged: bool = False         # draw P_b and C_b uniformly instead
     seed: int = 159100
+    chunk_list: tuple = ()       # explicit P_b per sequence (with context_list), overriding the above
+    context_list: tuple = ()
 
     @property
     def scale(self) -> float:
@@ -241,7 +243,10 @@ class PrefillDraw:
 
 def draw_prefill(w: PrefillWorkload, device="cpu") -> PrefillDraw:
     rng = np.random.Generator(np.random.PCG64(w.seed))
-    if w.ragged:
+    if w.chunk_list:
+        assert len(w.chunk_list) == len(w.context_list) == w.batch
+        P, C = np.array(w.chunk_list), np.array(w.context_list)
+    elif w.ragged:
         P = rng.integers(1, w.chunk, size=w.batch, endpoint=True)
         C = rng.integers(0, w.context, size=w.batch, endpoint=True)
     else:
