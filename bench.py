@@ -5,12 +5,18 @@ GQA decode attention) on the Llama-3-8B layer shape, through libpkv's C ABI.
 
 Prints one JSON line (rank 0).  `value` is K/V-cache bytes read per step divided by the
 device time of a step, summed over ranks (replicas: every rank runs its own copy of the
-workload, nothing is exchanged).  Each timed step is bracketed by CUDA events on the launch
-stream; the L2 cache is flushed between steps (outside the events) by reading a buffer twice
-its size (a read, so that no write-back of the flush lands in the next step).
-`e2e` repeats the measurement through the Python/C-ABI calls with pinned host inputs copied
-in and the output copied back every step.  `--impl reference` times the fp64 CPU oracle on
-a bounded sample of the same workload (one sequence per step).
+workload, nothing is exchanged).  Where sequences share prefix blocks, each physical block
+counts once (the bytes that must cross HBM); the logical bytes are given as `effective`.
+Each timed step is bracketed by CUDA events on the launch stream; the L2 cache is flushed
+between steps (outside the events) by reading a buffer twice its size (a read, so that no
+write-back of the flush lands in the next step).  `e2e` repeats the measurement through the
+Python/C-ABI calls with pinned host inputs copied in and the output copied back every step;
+`steady` repeats the step thousands of times with clock samples under load.  The default
+run also times every other workload (`other_configs`: ragged batch, Llama-3-70B long
+context, Qwen2.5-7B prefix sharing with bf16 and FP8 pools and with copy-on-write, the
+32-layer step, prefill and chunked prefill), each with its value, roofline fraction and
+traffic ratio.  `--impl reference` times the fp64 CPU oracle on a bounded sample of the
+same workload (one sequence per step).
 """
 import argparse
 import hashlib
@@ -153,13 +159,48 @@ def aggregate_value(world, kv_bytes_per_step, steps, slowest_total_s):
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args, world, rank, local_rank):
+def _unique_kv_positions(tables, seq_lens, num_blocks):
+    """Positions of K/V read when every physical block is read once: for each distinct block
+    id, the most positions any sequence reads from it.  A block shared by many tables (a
+    common prefix) counts once, as the pages store it once."""
+    most = np.zeros(num_blocks, np.int64)
+    for b, L in enumerate(seq_lens):
+        nb = -(-int(L) // 16)
+        np.maximum.at(most, tables[b, :nb], np.minimum(16, int(L) - 16 * np.arange(nb)))
+    return int(most.sum())
+
+
+def _copy_probe(pkv, torch, dev, stream):
+    """The library's streaming copy over 2 x 1 GiB, best of 10: the same-process bandwidth
+    denominator reported beside the measured peak."""
+    src = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        pkv.probe_copy(dst, src, stream=stream)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    probe = []
+    with torch.cuda.stream(stream):
+        for _ in range(10):
+            ev[0].record(stream)
+            pkv.probe_copy(dst, src, stream=stream)
+            ev[1].record(stream)
+            ev[1].synchronize()
+            probe.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+    copy_gbs = 2 * src.numel() / min(probe) / 1e9
+    del src, dst
+    return copy_gbs
+
+
+def run_decode(args, name, world, rank, local_rank, K, W, full=True):
+    """One decode workload: K timed steps after W warm-up steps.  full: also the end-to-end
+    leg from host memory, the steady repeat with clock samples and the oracle on the host."""
     import torch
     import paged_kv_cache_159_gb300 as pkv
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = workloads.WORKLOADS[args.workload]
+    w = workloads.WORKLOADS[name]
     nl = w.layers
     if nl > 1 and w.kv_dtype == "fp8":
         raise SystemExit("layered workloads are bf16")
@@ -246,22 +287,9 @@ def run_ours(args, world, rank, local_rank):
                                        stream=stream)
 
     # same-process bandwidth denominator: the library's copy probe over 2 x 1 GiB
-    src = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
-    dst = torch.empty_like(src)
-    for _ in range(3):
-        pkv.probe_copy(dst, src, stream=stream)
-    torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    probe = []
-    with torch.cuda.stream(stream):
-        for _ in range(10):
-            ev[0].record(stream)
-            pkv.probe_copy(dst, src, stream=stream)
-            ev[1].record(stream)
-            ev[1].synchronize()
-            probe.append(ev[0].elapsed_time(ev[1]) * 1e-3)
-    copy_gbs = 2 * src.numel() / min(probe) / 1e9
-    del src, dst
+    copy_gbs = None
+    if full:
+        copy_gbs = _copy_probe(pkv, torch, dev, stream)
 
     # L2 flush between steps: a read of a buffer twice the L2 size.  Reading leaves only clean
     # lines behind, so no write-back of the flush lands inside the next timed step.
@@ -272,12 +300,11 @@ def run_ours(args, world, rank, local_rank):
     def flush_l2():
         torch.sum(flush_buf, dim=0, out=flush_out)
 
-    K, W = args.steps, args.warmup
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
 
-    def timed_step(i):
+    def timed_step(i, starts=starts, mids=mids, ends=ends):
         flush_l2()                                # L2 flush (read), outside the timed interval
         starts[i].record(stream)
         cow_call(stream)
@@ -316,107 +343,163 @@ def run_ours(args, world, rank, local_rank):
     if st != pkv.OK:
         raise RuntimeError("device error in the timed region: %d bits %#x" % (st, bits))
 
-    # ---- end to end through the API: pinned host inputs in, output back, every step
-    host = {}
-    pin = lambda t: t.detach().cpu().pin_memory()
-    host["q"], host["k"], host["v"] = pin(d.q), pin(d.k_new), pin(d.v_new)
-    host["sl"] = torch.from_numpy(d.seq_lens.copy()).pin_memory()
-    host["out"] = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    tables_host = tables
-    h2d = (host["q"].numel() * 2 + (host["k"].numel() * 2 * 2 if w.append else 0)
-           + tables_host.nbytes + host["sl"].numel() * 4
-           + (B * 8 if w.append and args.separate_append else 0) + cow_pairs.nbytes)
-    d2h = host["out"].numel() * 2
-    cow_src_h = torch.from_numpy(cow_pairs[:, 0].copy()).pin_memory()
-    cow_dst_h = torch.from_numpy(cow_pairs[:, 1].copy()).pin_memory()
-    e2e_steps = max(5, min(K, 200))
-    bt_h = torch.from_numpy(tables_host).pin_memory()
-    sm_h = torch.empty(B, dtype=torch.int64).pin_memory()
-    ee = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    e2e_t = []
-    # the one-call host-memory step (pkv_decode_step_host) where it covers the step: copies
-    # in, the one-launch step and the copy out issued by one C call
-    one_call = nl == 1 and not args.separate_append and not len(cow_pairs)
-    if one_call:
-        # the step's inputs laid out back to back in one pinned host buffer and one device
-        # buffer (q, k_new, v_new, block_tables, seq_lens): one upload per step
-        parts = [("q", host["q"])] + ([("k_new", host["k"]), ("v_new", host["v"])] if w.append else []) + \
-                [("block_tables", bt_h), ("seq_lens", host["sl"])]
-        sizes = [t.numel() * t.element_size() for _, t in parts]
-        hbuf = torch.empty(sum(sizes), dtype=torch.uint8).pin_memory()
-        dbuf = torch.empty(sum(sizes), dtype=torch.uint8, device=dev)
-        hstep, dstep, off = {"out": host["out"], "contiguous": True}, {"out": out}, 0
-        for (name, t), n in zip(parts, sizes):
-            hv = hbuf[off:off + n].view(t.dtype).view(t.shape)
-            hv.copy_(t)
-            hstep[name] = hv
-            dstep[name] = dbuf[off:off + n].view(t.dtype).view(t.shape)
-            off += n
-        # the call prepared once for these buffers (as a serving loop would); each step is
-        # still one C call that uploads the inputs, decodes and downloads the output
-        prepared = pkv.DecodeStepHost(pool, hstep, dstep, kc, vc, w.scale, ws, opts=decode_opts,
-                                      stream=torch.cuda.current_stream())
-    else:
-        # the other steps (copy-on-write, a separate append, several layers): the inputs are
-        # packed the same way, one upload per step, and the library calls take views of the
-        # device copy
-        parts = [("q", host["q"])] + ([("k", host["k"]), ("v", host["v"])] if w.append else []) + \
-                [("bt", bt_h), ("sl", host["sl"])] + \
-                ([("cs", cow_src_h), ("cd", cow_dst_h)] if len(cow_pairs) else []) + \
-                ([("sm", sm_h)] if w.append and args.separate_append else [])
-        spans = [(t.numel() * t.element_size() + 15) // 16 * 16 for _, t in parts]   # 16-byte aligned views
-        hbuf = torch.empty(sum(spans), dtype=torch.uint8).pin_memory()
-        dbuf = torch.empty(sum(spans), dtype=torch.uint8, device=dev)
-        hview, dview, off = {}, dict(dev_in), 0
-        for (name, t), n in zip(parts, spans):
-            nb = t.numel() * t.element_size()
-            hview[name] = hbuf[off:off + nb].view(t.dtype).view(t.shape)
-            hview[name].copy_(t)
-            dview[name] = dbuf[off:off + nb].view(t.dtype).view(t.shape)
-            off += n
-        h2d = int(hbuf.numel())                   # the packed buffer is what is uploaded
-    ref_out = out.detach().cpu()                  # the timed steps' output
-    for i in range(e2e_steps + 3):
-        flush_l2()
-        torch.cuda.synchronize()
-        ee[0].record()
+    # ---- the steady repeat of the same step: enough steps for clock samples under load
+    steady = None
+    if full and args.steady_steps > 0:
+        S = args.steady_steps
+        st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(S)] for _ in range(3)]
+        with ClockSampler(local_rank) as sclk:
+            with torch.cuda.stream(stream):
+                for i in range(S):
+                    timed_step(i, *st_ev)
+            stream.synchronize()
+        st_step = sorted(st_ev[0][i].elapsed_time(st_ev[2][i]) * 1e-3 for i in range(S))
+        st_dec = sorted(st_ev[1][i].elapsed_time(st_ev[2][i]) * 1e-3 for i in range(S))
+        steady = {"steps": S, "ms_per_step_median": round(st_step[S // 2] * 1e3, 5),
+                  "kernel_us_median": round(st_dec[S // 2] * 1e6, 2),
+                  "clocks": sclk.summary()}
+        st, bits = pool.get_device_error(stream)
+        if st != pkv.OK:
+            raise RuntimeError("device error in the steady repeat: %d bits %#x" % (st, bits))
+
+    def e2e_leg():
+        # ---- end to end through the API: pinned host inputs in, output back, every step
+        host = {}
+        pin = lambda t: t.detach().cpu().pin_memory()
+        host["q"], host["k"], host["v"] = pin(d.q), pin(d.k_new), pin(d.v_new)
+        host["sl"] = torch.from_numpy(d.seq_lens.copy()).pin_memory()
+        host["out"] = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        tables_host = tables
+        h2d = (host["q"].numel() * 2 + (host["k"].numel() * 2 * 2 if w.append else 0)
+               + tables_host.nbytes + host["sl"].numel() * 4
+               + (B * 8 if w.append and args.separate_append else 0) + cow_pairs.nbytes)
+        d2h = host["out"].numel() * 2
+        cow_src_h = torch.from_numpy(cow_pairs[:, 0].copy()).pin_memory()
+        cow_dst_h = torch.from_numpy(cow_pairs[:, 1].copy()).pin_memory()
+        e2e_steps = max(5, min(K, 200))
+        bt_h = torch.from_numpy(tables_host).pin_memory()
+        sm_h = torch.empty(B, dtype=torch.int64).pin_memory()
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e2e_t = []
+        # the one-call host-memory step (pkv_decode_step_host) where it covers the step: copies
+        # in, the one-launch step and the copy out issued by one C call
+        one_call = nl == 1 and not args.separate_append and not len(cow_pairs)
         if one_call:
-            prepared.run()                                                 # one upload, one download
+            # the step's inputs laid out back to back in one pinned host buffer and one device
+            # buffer (q, k_new, v_new, block_tables, seq_lens): one upload per step
+            parts = [("q", host["q"])] + ([("k_new", host["k"]), ("v_new", host["v"])] if w.append else []) + \
+                    [("block_tables", bt_h), ("seq_lens", host["sl"])]
+            sizes = [t.numel() * t.element_size() for _, t in parts]
+            hbuf = torch.empty(sum(sizes), dtype=torch.uint8).pin_memory()
+            dbuf = torch.empty(sum(sizes), dtype=torch.uint8, device=dev)
+            hstep, dstep, off = {"out": host["out"], "contiguous": True}, {"out": out}, 0
+            for (name, t), n in zip(parts, sizes):
+                hv = hbuf[off:off + n].view(t.dtype).view(t.shape)
+                hv.copy_(t)
+                hstep[name] = hv
+                dstep[name] = dbuf[off:off + n].view(t.dtype).view(t.shape)
+                off += n
+            # the call prepared once for these buffers (as a serving loop would); each step is
+            # still one C call that uploads the inputs, decodes and downloads the output
+            prepared = pkv.DecodeStepHost(pool, hstep, dstep, kc, vc, w.scale, ws, opts=decode_opts,
+                                          stream=torch.cuda.current_stream())
+        else:
+            # the other steps (copy-on-write, a separate append, several layers): the inputs are
+            # packed the same way, one upload per step, and the library calls take views of the
+            # device copy
+            parts = [("q", host["q"])] + ([("k", host["k"]), ("v", host["v"])] if w.append else []) + \
+                    [("bt", bt_h), ("sl", host["sl"])] + \
+                    ([("cs", cow_src_h), ("cd", cow_dst_h)] if len(cow_pairs) else []) + \
+                    ([("sm", sm_h)] if w.append and args.separate_append else [])
+            spans = [(t.numel() * t.element_size() + 15) // 16 * 16 for _, t in parts]   # 16-byte aligned views
+            hbuf = torch.empty(sum(spans), dtype=torch.uint8).pin_memory()
+            dbuf = torch.empty(sum(spans), dtype=torch.uint8, device=dev)
+            hview, dview, off = {}, dict(dev_in), 0
+            for (name, t), n in zip(parts, spans):
+                nb = t.numel() * t.element_size()
+                hview[name] = hbuf[off:off + nb].view(t.dtype).view(t.shape)
+                hview[name].copy_(t)
+                dview[name] = dbuf[off:off + nb].view(t.dtype).view(t.shape)
+                off += n
+            h2d = int(hbuf.numel())                   # the packed buffer is what is uploaded
+        ref_out = out.detach().cpu()                  # the timed steps' output
+        for i in range(e2e_steps + 3):
+            flush_l2()
+            torch.cuda.synchronize()
+            ee[0].record()
+            if one_call:
+                prepared.run()                                                 # one upload, one download
+                ee[1].record()
+                ee[1].synchronize()
+                if i >= 3:
+                    e2e_t.append(ee[0].elapsed_time(ee[1]) * 1e-3)
+                continue
+            if w.append and args.separate_append:
+                slots_np = pkv.slot_mapping(tables_host, d.seq_lens)        # host allocator side
+                hview["sm"][:] = torch.from_numpy(slots_np)
+            dbuf.copy_(hbuf, non_blocking=True)                              # one upload
+            if w.append:
+                cow_call(t=dview)
+                if args.separate_append:
+                    append_call(t=dview)
+                    decode_call(False, t=dview)
+                else:
+                    decode_call(True, t=dview)
+            else:
+                decode_call(False, t=dview)
+            host["out"].copy_(out, non_blocking=True)
             ee[1].record()
             ee[1].synchronize()
             if i >= 3:
                 e2e_t.append(ee[0].elapsed_time(ee[1]) * 1e-3)
-            continue
-        if w.append and args.separate_append:
-            slots_np = pkv.slot_mapping(tables_host, d.seq_lens)        # host allocator side
-            hview["sm"][:] = torch.from_numpy(slots_np)
-        dbuf.copy_(hbuf, non_blocking=True)                              # one upload
-        if w.append:
-            cow_call(t=dview)
-            if args.separate_append:
-                append_call(t=dview)
-                decode_call(False, t=dview)
-            else:
-                decode_call(True, t=dview)
-        else:
-            decode_call(False, t=dview)
-        host["out"].copy_(out, non_blocking=True)
-        ee[1].record()
-        ee[1].synchronize()
-        if i >= 3:
-            e2e_t.append(ee[0].elapsed_time(ee[1]) * 1e-3)
-    e2e_step = float(statistics.median(e2e_t))
-    if not torch.equal(host["out"].view(torch.int16), ref_out.view(torch.int16)):
-        raise RuntimeError("end-to-end decode output differs from the timed steps'")
+        e2e_step = float(statistics.median(e2e_t))
+        if not torch.equal(host["out"].view(torch.int16), ref_out.view(torch.int16)):
+            raise RuntimeError("end-to-end decode output differs from the timed steps'")
+        api = ("DecodeStepHost.run (one pkv_decode_step_host call)" if one_call
+               else "one packed upload + library calls on views of it")
+        return e2e_step, h2d, d2h, api
+
+    e2e_step = h2d = d2h = None
+    if full:
+        e2e_step, h2d, d2h, e2e_api = e2e_leg()
 
     # ---- reduce over ranks (max time), aggregate bytes over ranks
     if world > 1:
-        total, dec_mean, e2e_step = reduce_max_over_ranks([total, dec_mean, e2e_step], dev)
+        total, dec_mean = reduce_max_over_ranks([total, dec_mean], dev)
+        if e2e_step is not None:
+            (e2e_step,) = reduce_max_over_ranks([e2e_step], dev)
     peak, peak_src = _hbm_peak()
     ms_per_step = total / K * 1e3
-    value = aggregate_value(world, kv_read, K, total)
-    achieved = launch_bytes / dec_mean / 1e9
-    traffic = _profiled_traffic(args.workload)
+    # Shared prefix blocks are stored once and read by many tables: their bytes cross HBM
+    # once, so the roofline counts unique K/V bytes (each physical block once); the logical
+    # bytes (every table's view) are reported beside them as "effective".
+    shared = w.prefix_blocks > 0
+    kv_unique = (nl * _unique_kv_positions(tables, d.seq_lens, d.num_blocks) * Hkv * D * elem * 2
+                 if shared else kv_read)
+    launch_unique = launch_bytes - kv_read + kv_unique
+    value = aggregate_value(world, kv_unique, K, total)
+    achieved = launch_unique / dec_mean / 1e9
+    traffic = _profiled_traffic(name)
+    kernel = "decode_mma_kernel (%s%s)" % ("decode_step" if w.append and not args.separate_append
+                                           else "paged_attention_decode", ", %d layers" % nl if nl > 1 else "")
+    step = (("copy_blocks + " if len(cow_pairs) else "") +
+            (("kv_append + paged_attention_decode" if args.separate_append else
+              "decode_step (append at L-1 + paged decode, one launch)") if w.append
+             else "paged_attention_decode") + (", all %d layers per launch" % nl if nl > 1 else ""))
+    basis = ("unique K/V bytes (each shared prefix block once)" if shared else "K/V bytes")
+    if not full:
+        r = {"value": round(value, 1), "unit": "GB/s", "basis": basis, "step": step,
+             "ms_per_step": round(ms_per_step, 5), "kernel_us": round(dec_mean * 1e6, 2),
+             "frac": round(achieved / peak, 4), "achieved": round(achieved, 1),
+             "bytes_per_launch": launch_unique,
+             "traffic": traffic, "traffic_ratio": round(traffic / launch_unique, 3) if traffic else None,
+             "kernel": kernel, "steps": K, "warmup": W, "gpu_launches": launches_per_step * K,
+             "query_tokens_per_s": round(world * B * K / total, 1)}
+        if shared:
+            r["effective"] = round(aggregate_value(world, kv_read, K, total), 1)
+            r["effective_basis"] = "logical K/V bytes (every table's blocks counted)"
+            r["effective_frac"] = round(launch_bytes / dec_mean / 1e9 / peak, 4)
+        return r
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_per_step, 5),
@@ -429,34 +512,33 @@ def run_ours(args, world, rank, local_rank):
                                                  else "%s (sum %d)" % (w.lengths, int(d.seq_lens.sum())),
                                                  w.kv_dtype),
             "copy_on_write_pairs": int(len(cow_pairs)),
-            "step": ("copy_blocks + " if len(cow_pairs) else "") +
-                    (("kv_append + paged_attention_decode" if args.separate_append else
-                      "decode_step (append at L-1 + paged decode, one launch)") if w.append
-                     else "paged_attention_decode") + (", all %d layers per launch" % nl if nl > 1 else ""),
+            "step": step,
             "decode_opts": decode_opts,
             "l2": "flushed between steps (read of a 2x L2 buffer); inputs also exceed L2",
             "parallelism": "replicas",
             "timing": "CUDA events around each step on the launch stream; flush outside them",
         },
-        "pct_of_hbm_peak": round(100.0 * (kv_read * K / total / 1e9) / peak, 2),
+        "basis": basis,
+        "pct_of_hbm_peak": round(100.0 * (kv_unique * K / total / 1e9) / peak, 2),
         "query_tokens_per_s": round(world * B * K / total, 1),
         "step_bytes": step_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_mma_kernel (%s%s)" % ("decode_step" if w.append and not args.separate_append
-                                                             else "paged_attention_decode",
-                                                             ", %d layers" % nl if nl > 1 else ""),
-                     "bytes_per_launch": launch_bytes, "peak_source": peak_src + " hbm_gbs",
-                     "same_run_copy_gbs": round(copy_gbs, 1)},
-        "e2e": {"value": round(world * kv_read / e2e_step / 1e9, 1), "unit": "GB/s",
+                     "kernel": kernel, "bytes_per_launch": launch_unique,
+                     "peak_source": peak_src + " hbm_gbs", "same_run_copy_gbs": round(copy_gbs, 1) if copy_gbs else None},
+        "e2e": {"value": round(world * kv_unique / e2e_step / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(e2e_step * 1e3, 4),
-                "api": "DecodeStepHost.run (one pkv_decode_step_host call)" if one_call
-                       else "one packed upload + library calls on views of it"},
+                "ms_per_step": round(e2e_step * 1e3, 4), "api": e2e_api},
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 3),
     }
+    if shared:
+        res["effective"] = round(aggregate_value(world, kv_read, K, total), 1)
+        res["effective_basis"] = "logical K/V bytes (every table's blocks counted)"
+    if steady is not None:
+        steady["value_at_median"] = round(world * kv_unique / (steady["ms_per_step_median"] * 1e-3) / 1e9, 1)
+        res["steady"] = steady
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, sample_seqs=args.cpu_sample_seqs)
     return res
@@ -642,13 +724,15 @@ def _prefill_traffic(workload: str):
     return int(m.group(1))
 
 
-def run_prefill(args, world, rank, local_rank):
+def run_prefill(args, name, world, rank, local_rank, K, W, full=True):
+    """One prefill workload: K timed steps after W warm-up steps.  full: also the end-to-end
+    leg from host memory and the oracle on the host."""
     import torch
     import paged_kv_cache_159_gb300 as pkv
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = workloads.PREFILL_WORKLOADS[args.workload]
+    w = workloads.PREFILL_WORKLOADS[name]
     d = workloads.draw_prefill(w, dev)
     Hq, Hkv, D = w.num_q_heads, w.num_kv_heads, w.head_dim
     T = int(d.cu_q[-1])
@@ -673,7 +757,6 @@ def run_prefill(args, world, rank, local_rank):
         mids_rec(s)
         pkv.paged_prefill(pool, d.q, kc, vc, bt, w.scale, plan, grid, out, stream=s)
 
-    K, W = args.steps, args.warmup
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -715,66 +798,88 @@ def run_prefill(args, world, rank, local_rank):
     if st != pkv.OK:
         raise RuntimeError("device error in the timed region: %d bits %#x" % (st, bits))
 
-    # end to end: the step's inputs from pinned host memory, the output back, every step.
-    # The batch is cut into groups of whole sequences, each with its own host plan; group
-    # i+1's upload overlaps group i's kv_append + prefill and group i-1's download (three
-    # streams).  Rows do not depend on the batch around them, so the output is the same.
-    pin = lambda t: t.detach().cpu().pin_memory()
-    ref_out = out.detach().cpu()
-    B = w.batch
-    NC = min(4, B)
-    groups = []
-    for c in range(NC):
-        b0, b1 = c * B // NC, (c + 1) * B // NC
-        r0, r1 = int(d.cu_q[b0]), int(d.cu_q[b1])
-        cu = (d.cu_q[b0:b1 + 1] - d.cu_q[b0]).astype(np.int32)
-        plan_c, grid_c = pkv.prefill_plan(pool, cu, d.seq_lens[b0:b1], Hq, d.max_blocks)
-        groups.append(dict(
-            rows=(r0, r1), bts=(b0, b1), grid=grid_c,
-            hq=pin(d.q[r0:r1]), hk=pin(d.k_chunk[r0:r1]), hv=pin(d.v_chunk[r0:r1]), hbt=pin(bt[b0:b1]),
-            hsm=pin(sm[r0:r1]), hplan=torch.from_numpy(plan_c).pin_memory(),
-            dplan=torch.empty(plan_c.shape, dtype=torch.uint8, device=dev),
-            hout=torch.empty((r1 - r0,) + tuple(out.shape[1:]), dtype=out.dtype).pin_memory()))
-    h2d = sum(x.numel() * x.element_size() for g in groups for x in (g["hq"], g["hk"], g["hv"], g["hbt"], g["hsm"], g["hplan"]))
-    d2h = sum(g["hout"].numel() * g["hout"].element_size() for g in groups)
-    s_up, s_run, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
-    ee = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    ev_in = [torch.cuda.Event() for _ in groups]
-    ev_run = [torch.cuda.Event() for _ in groups]
-    e2e_t = []
-    for i in range(max(5, min(K, 100)) + 3):
-        torch.sum(flush_buf, dim=0, out=flush_out)
-        torch.cuda.synchronize()
-        ee[0].record(s_up)
-        for g, ei, er in zip(groups, ev_in, ev_run):
-            (r0, r1), (b0, b1) = g["rows"], g["bts"]
-            with torch.cuda.stream(s_up):
-                for dst, src in ((d.q[r0:r1], g["hq"]), (d.k_chunk[r0:r1], g["hk"]), (d.v_chunk[r0:r1], g["hv"]),
-                                 (bt[b0:b1], g["hbt"]), (sm[r0:r1], g["hsm"]), (g["dplan"], g["hplan"])):
-                    dst.copy_(src, non_blocking=True)
-                ei.record(s_up)
-            s_run.wait_event(ei)
-            pkv.kv_append(pool, d.k_chunk[r0:r1], d.v_chunk[r0:r1], sm[r0:r1], kc, vc, stream=s_run)
-            pkv.paged_prefill(pool, d.q[r0:r1], kc, vc, bt[b0:b1], w.scale, g["dplan"], g["grid"], out[r0:r1],
-                              stream=s_run)
-            er.record(s_run)
-            s_down.wait_event(er)
-            with torch.cuda.stream(s_down):
-                g["hout"].copy_(out[r0:r1], non_blocking=True)
-        ee[1].record(s_down)
-        ee[1].synchronize()
-        if i >= 3:
-            e2e_t.append(ee[0].elapsed_time(ee[1]) * 1e-3)
-    for g in groups:                                    # the grouped step gives the same bits
-        r0, r1 = g["rows"]
-        if not torch.equal(g["hout"].view(torch.int16), ref_out[r0:r1].view(torch.int16)):
-            raise RuntimeError("grouped end-to-end prefill output differs from the single launch")
-    e2e_step = float(statistics.median(e2e_t))
+    def e2e_leg():
+        # end to end: the step's inputs from pinned host memory, the output back, every step.
+        # The batch is cut into groups of whole sequences, each with its own host plan; group
+        # i+1's upload overlaps group i's kv_append + prefill and group i-1's download (three
+        # streams).  Rows do not depend on the batch around them, so the output is the same.
+        pin = lambda t: t.detach().cpu().pin_memory()
+        ref_out = out.detach().cpu()
+        B = w.batch
+        NC = min(4, B)
+        groups = []
+        for c in range(NC):
+            b0, b1 = c * B // NC, (c + 1) * B // NC
+            r0, r1 = int(d.cu_q[b0]), int(d.cu_q[b1])
+            cu = (d.cu_q[b0:b1 + 1] - d.cu_q[b0]).astype(np.int32)
+            plan_c, grid_c = pkv.prefill_plan(pool, cu, d.seq_lens[b0:b1], Hq, d.max_blocks)
+            groups.append(dict(
+                rows=(r0, r1), bts=(b0, b1), grid=grid_c,
+                hq=pin(d.q[r0:r1]), hk=pin(d.k_chunk[r0:r1]), hv=pin(d.v_chunk[r0:r1]), hbt=pin(bt[b0:b1]),
+                hsm=pin(sm[r0:r1]), hplan=torch.from_numpy(plan_c).pin_memory(),
+                dplan=torch.empty(plan_c.shape, dtype=torch.uint8, device=dev),
+                hout=torch.empty((r1 - r0,) + tuple(out.shape[1:]), dtype=out.dtype).pin_memory()))
+        h2d = sum(x.numel() * x.element_size() for g in groups for x in (g["hq"], g["hk"], g["hv"], g["hbt"], g["hsm"], g["hplan"]))
+        d2h = sum(g["hout"].numel() * g["hout"].element_size() for g in groups)
+        s_up, s_run, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev_in = [torch.cuda.Event() for _ in groups]
+        ev_run = [torch.cuda.Event() for _ in groups]
+        e2e_t = []
+        for i in range(max(5, min(K, 100)) + 3):
+            torch.sum(flush_buf, dim=0, out=flush_out)
+            torch.cuda.synchronize()
+            ee[0].record(s_up)
+            for g, ei, er in zip(groups, ev_in, ev_run):
+                (r0, r1), (b0, b1) = g["rows"], g["bts"]
+                with torch.cuda.stream(s_up):
+                    for dst, src in ((d.q[r0:r1], g["hq"]), (d.k_chunk[r0:r1], g["hk"]), (d.v_chunk[r0:r1], g["hv"]),
+                                     (bt[b0:b1], g["hbt"]), (sm[r0:r1], g["hsm"]), (g["dplan"], g["hplan"])):
+                        dst.copy_(src, non_blocking=True)
+                    ei.record(s_up)
+                s_run.wait_event(ei)
+                pkv.kv_append(pool, d.k_chunk[r0:r1], d.v_chunk[r0:r1], sm[r0:r1], kc, vc, stream=s_run)
+                pkv.paged_prefill(pool, d.q[r0:r1], kc, vc, bt[b0:b1], w.scale, g["dplan"], g["grid"], out[r0:r1],
+                                  stream=s_run)
+                er.record(s_run)
+                s_down.wait_event(er)
+                with torch.cuda.stream(s_down):
+                    g["hout"].copy_(out[r0:r1], non_blocking=True)
+            ee[1].record(s_down)
+            ee[1].synchronize()
+            if i >= 3:
+                e2e_t.append(ee[0].elapsed_time(ee[1]) * 1e-3)
+        for g in groups:                                    # the grouped step gives the same bits
+            r0, r1 = g["rows"]
+            if not torch.equal(g["hout"].view(torch.int16), ref_out[r0:r1].view(torch.int16)):
+                raise RuntimeError("grouped end-to-end prefill output differs from the single launch")
+        e2e_step = float(statistics.median(e2e_t))
+        api = ("kv_append + paged_prefill per group of %d sequences (%d groups, own plans); uploads, "
+               "kernels and downloads on three streams, overlapped across groups" % (B // NC, NC))
+        return e2e_step, h2d, d2h, api
+
+    e2e_step = h2d = d2h = None
+    if full:
+        e2e_step, h2d, d2h, e2e_api = e2e_leg()
     if world > 1:
-        total, pre_mean, e2e_step = reduce_max_over_ranks([total, pre_mean, e2e_step], dev)
+        total, pre_mean = reduce_max_over_ranks([total, pre_mean], dev)
+        if e2e_step is not None:
+            (e2e_step,) = reduce_max_over_ranks([e2e_step], dev)
     peak, peak_src = _tensor_peak()
     value = world * flops * K / total / 1e12
     achieved = flops / pre_mean / 1e12
+    traffic = _prefill_traffic(w.name)
+    # algorithmic bytes of one prefill launch: K and V of every position, q and out of every
+    # packed row, the tables
+    alg_bytes = (int(d.seq_lens.astype(np.int64).sum()) * Hkv * D * 2 * 2 + T * Hq * D * 2 * 2
+                 + w.batch * d.max_blocks * 4)
+    if not full:
+        return {"value": round(value, 2), "unit": "TFLOP/s", "step": "kv_append + paged_prefill (tcgen05)",
+                "ms_per_step": round(total / K * 1e3, 5), "kernel_us": round(pre_mean * 1e6, 2),
+                "frac": round(achieved / peak, 4), "achieved": round(achieved, 2), "flops_per_launch": flops,
+                "bytes_per_launch": alg_bytes, "traffic": traffic,
+                "traffic_ratio": round(traffic / alg_bytes, 3) if traffic else None,
+                "kernel": "prefill_kernel<%d>" % D, "steps": K, "warmup": W, "gpu_launches": 2 * K}
     res = {
         "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(total / K * 1e3, 5), "higher_is_better": True,
@@ -792,14 +897,12 @@ def run_prefill(args, world, rank, local_rank):
         },
         "query_tokens_per_s": round(world * T * K / total, 1),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": _prefill_traffic(w.name),
-                     "kernel": "prefill_kernel<%d>" % D,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "prefill_kernel<%d>" % D, "bytes_per_launch": alg_bytes,
                      "flops_per_launch": flops, "peak_source": peak_src},
         "e2e": {"value": round(world * flops / e2e_step / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(e2e_step * 1e3, 4),
-                "api": "kv_append + paged_prefill per group of %d sequences (%d groups, own plans); uploads, "
-                       "kernels and downloads on three streams, overlapped across groups" % (B // NC, NC)},
+                "ms_per_step": round(e2e_step * 1e3, 4), "api": e2e_api},
         "gpu_launches": 2 * K,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 3),
@@ -835,6 +938,27 @@ def run_prefill_reference(args):
     }
 
 
+OTHER_CONFIGS = ("ragged", "llama3_70b_long", "qwen25_7b_prefix", "qwen25_7b_prefix_fp8",
+                 "qwen25_7b_prefix_cow", "llama3_8b_32l", "prefill_llama3_8b", "chunked_prefill_llama3_8b")
+
+
+def run_other_configs(args, world, rank, local_rank):
+    """Every other workload, timed in the same process after the headline: a compact line
+    each (value, roofline fraction, traffic ratio, ms per step), and the clocks seen while
+    they ran."""
+    import gc
+    import torch
+    out = {}
+    with ClockSampler(local_rank) as clk:
+        for name in OTHER_CONFIGS:
+            run = run_prefill if name in workloads.PREFILL_WORKLOADS else run_decode
+            out[name] = run(args, name, world, rank, local_rank, args.other_steps, 5, full=False)
+            gc.collect()
+            torch.cuda.empty_cache()
+    out["clocks"] = clk.summary()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -848,6 +972,11 @@ def main():
     ap.add_argument("--separate-append", action="store_true",
                     help="time kv_append and decode as two launches instead of decode_step")
     ap.add_argument("--opts", default="", help='decode knobs as JSON, e.g. {"warps_per_cta": 8}')
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="time only --workload (the default run also times every other workload)")
+    ap.add_argument("--other-steps", type=int, default=30, help="timed steps of each other workload")
+    ap.add_argument("--steady-steps", type=int, default=8000,
+                    help="steps of the headline's steady repeat (clock samples under load); 0: none")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -863,8 +992,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        run = run_prefill if args.workload in workloads.PREFILL_WORKLOADS else run_ours
-        res = run(args, world, rank, local_rank)
+        run = run_prefill if args.workload in workloads.PREFILL_WORKLOADS else run_decode
+        res = run(args, args.workload, world, rank, local_rank, args.steps, args.warmup, full=True)
+        if args.workload == DEFAULT_WORKLOAD and not args.no_other_configs:
+            res["other_configs"] = run_other_configs(args, world, rank, local_rank)
         if rank == 0:
             print(json.dumps(res), flush=True)
     finally:

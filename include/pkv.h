@@ -406,12 +406,17 @@ int pkv_decode_step_host(pkv_pool *pool, const pkv_host_step *host, const pkv_de
  * PKV_NOALLOC_SCRATCH_BYTES compiled into the library, held by every GPU that loads it
  * until the process exits.  Returns PKV_ERR_INVALID, launching nothing, if the shape needs
  * more scratch than that (pkv_decode_workspace_bytes() tells how much it needs).  The
- * first call on a device looks up the array's device address (once per device, with that
- * device current); make that first call before any stream capture.  Every call clears the
- * array's counters with an asynchronous memset on `stream`, then runs the same kernel as
- * pkv_paged_attention_decode.  All calls on a device share the array, so calls that
- * overlap on the GPU race and must not be issued.  The pool must be attached beforehand
- * (pkv_pool_attach_device allocates its 4-byte error word once). */
+ * pool's device must be the current device (INVALID otherwise).  The first call on a device
+ * looks up the array's device address (once per device, with that device current); make
+ * that first call before any stream capture.  The cached address does not survive
+ * cudaDeviceReset(), which invalidates the pools' error words as well: create and attach
+ * pools again and do not call this entry point across a reset.  Every argument check is
+ * made before anything is queued; a call that passes them clears the array's counters with
+ * an asynchronous memset on `stream`, then runs the same kernel with the same launch plan
+ * as pkv_paged_attention_decode, so the two give bit-identical outputs.  All calls on a
+ * device share the array, so calls that overlap on the GPU race and must not be issued.
+ * The pool must be attached beforehand (pkv_pool_attach_device allocates its 4-byte error
+ * word once). */
 int pkv_paged_attention_decode_noalloc(pkv_pool *pool, const void *q, const void *key_cache,
                                        const void *value_cache, const int32_t *block_tables,
                                        const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
@@ -421,6 +426,23 @@ int pkv_paged_attention_decode_noalloc(pkv_pool *pool, const void *q, const void
  * Returns PKV_OK if it was zero, PKV_ERR_TIMEOUT if the timeout bit was set, else
  * PKV_ERR_DEVICE. */
 int pkv_get_device_error(pkv_pool *pool, void *stream, uint32_t *bits_out);
+
+/* Test hook for the failure path of the kernels' bounded waits (the pages have no
+ * counterpart; it exists so that a test can see that path run).  While `which` is
+ * PKV_TEST_EXPIRE_DECODE (every decode entry point) or PKV_TEST_EXPIRE_PREFILL
+ * (pkv_paged_prefill), every launch of that kernel makes one of its roles -- the decode's
+ * streaming warps before their first block, the prefill's Q loader before its first load --
+ * wait about 1 ms on an mbarrier that nothing completes.  The wait runs out, the kernel sets
+ * PKV_DEVERR_TIMEOUT, and the roles that depend on the stalled one give up in turn (each
+ * after its normal bound of about 1 s at most); copies already in flight are waited for
+ * (bounded) before a CTA leaves, so the context stays usable and pkv_get_device_error()
+ * returns PKV_ERR_TIMEOUT.  Outputs of such a launch are unspecified.  Decode workspace
+ * counters still return to zero.  PKV_TEST_EXPIRE_NONE (the default) turns it off.  The
+ * setting is process-wide and read when a call launches; INVALID for any other value. */
+#define PKV_TEST_EXPIRE_NONE 0
+#define PKV_TEST_EXPIRE_DECODE 1
+#define PKV_TEST_EXPIRE_PREFILL 2
+int pkv_test_expire_waits(int32_t which);
 
 /* Device-to-device copy of `bytes` (a multiple of 16; both pointers 16-byte aligned) by a
  * plain streaming kernel: the bandwidth denominator measured in the same process. */

@@ -37,6 +37,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libpkv.so")
 
 OK, ERR_INVALID, ERR_OOM, ERR_DEVICE, ERR_TIMEOUT, ERR_CUDA = range(6)
+TEST_EXPIRE_NONE, TEST_EXPIRE_DECODE, TEST_EXPIRE_PREFILL = range(3)
 DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT, DEVERR_PLAN = 0x1, 0x2, 0x4, 0x8, 0x10
 KV_BF16, KV_FP8E4M3 = 0, 1
 BLOCK_SIZE = 16
@@ -52,7 +53,7 @@ EXPORTED = (
     "pkv_prefill_plan_bytes", "pkv_prefill_plan", "pkv_paged_prefill", "pkv_decode_step_host",
     "pkv_decode_workspace_bytes", "pkv_paged_attention_decode",
     "pkv_paged_attention_decode_ex", "pkv_decode_step", "pkv_paged_attention_decode_noalloc",
-    "pkv_get_device_error", "pkv_probe_copy",
+    "pkv_get_device_error", "pkv_test_expire_waits", "pkv_probe_copy",
     "pkv_device_sm_count", "pkv_status_string",
 )
 
@@ -148,6 +149,7 @@ def lib():
             "pkv_paged_attention_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32,
                                                                   _I32, ctypes.c_float, _P, _P]),
             "pkv_get_device_error": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+            "pkv_test_expire_waits": (ctypes.c_int, [_I32]),
             "pkv_probe_copy": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
             "pkv_device_sm_count": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(_I32)]),
             "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -558,6 +560,12 @@ def paged_attention_decode_noalloc(pool: Pool, q, key_cache, value_cache, block_
         _dev_ptr(value_cache, "value_cache"), _dev_ptr(block_tables, "block_tables"),
         _dev_ptr(seq_lens, "seq_lens"), int(B), int(Hq), int(block_tables.shape[1]),
         float(scale), _dev_ptr(out, "out"), _stream_ptr(stream)), "paged_attention_decode_noalloc")
+
+
+def test_expire_waits(which: int):
+    """Failure-path test hook (pkv_test_expire_waits): while set, every launch of the chosen
+    kernel runs one bounded wait out and reports PKV_DEVERR_TIMEOUT."""
+    _check(lib().pkv_test_expire_waits(int(which)), "test_expire_waits")
 
 
 def probe_copy(dst, src, stream=None):

@@ -84,6 +84,7 @@ struct DecodeParams {
     const uint16_t *k_new;        // bf16 [layers, B, Hkv, D]: appended at position L-1 (or null)
     const uint16_t *v_new;
     int layers;                   // layers decoded by this launch (stacked layer-major)
+    int test_stall;               // failure-path test: streaming warps wait on a barrier nothing completes
     int B, Hq, Hkv, group, MB, num_blocks;
     float score_scale;            // scale * k_scale * log2(e)
     float out_scale;              // v_scale (1 for bf16 pools)
@@ -108,7 +109,7 @@ struct Layout {
         prefix = o; o += align_up((B + 1) * 4, 16);              // task prefix over sequences
         lens = o;   o += align_up(B * 4, 16);                    // seq_lens
         phys = o;   o += align_up(NW * NS * 4, 16);              // tile index per stage
-        bar = o;    o += (NW * NS + 6) * 8;                      // stages, q, segment done/free
+        bar = o;    o += (NW * NS + 7) * 8;                      // stages, q, segment done/free, never
         flag = o;   o += 128;                                    // scan scratch, merge flag
         total = o;
     }
@@ -502,6 +503,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
     const uint32_t qbar0 = dev::smem_u32(bars + NW * NS);         // q slot j full: +8*j
     const uint32_t done0 = dev::smem_u32(bars + NW * NS + 2);     // merge slot j dumped
     const uint32_t free0 = dev::smem_u32(bars + NW * NS + 4);     // merge slot j merged
+    const uint32_t never = dev::smem_u32(bars + NW * NS + 6);     // no thread ever arrives here
     if (tid == 0) {
         auto slice = [&](const void *base, size_t bytes) {
             const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + bytes * c / gridDim.x + 15) & ~uintptr_t(15);
@@ -515,6 +517,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
             dev::mbar_init(done0 + 8 * j, NW * 32);
             dev::mbar_init(free0 + 8 * j, 1);
         }
+        dev::mbar_init(never, 1);
     }
     if (lane == 0 && warp < NW)
         for (int st = 0; st < NS; ++st) dev::mbar_init(dev::smem_u32(bars + warp * NS + st), 1);
@@ -874,6 +877,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
 
         // ---- 4. segments
         bool aborted = false;
+        if (p.test_stall)          // the failure-path test: a wait that runs out (copies in flight)
+            aborted = !__all_sync(dev::FULL, dev::mbar_wait_bounded_ns(never, 0, dev::TEST_EXPIRE_NS));
         int ic = 0;
         int k = 0;
         for (long long seg_lo = s; seg_lo < e; ++k) {

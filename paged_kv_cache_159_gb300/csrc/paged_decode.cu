@@ -104,6 +104,30 @@ namespace pkv {
 namespace decode {
 namespace {
 
+// Every host-side check of a decode call with batch >= 1, and its launch plan; launches
+// nothing and queues nothing.
+int check_call(const pkv_pool *pool, const void *q, const void *k_new, const void *v_new,
+               const void *key_cache, const void *value_cache, const int32_t *block_tables,
+               const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
+               float scale, const void *out, const void *workspace, size_t workspace_bytes,
+               const pkv_decode_opts *opts, Plan &pl)
+{
+    int st = check_attached(pool);
+    if (st != PKV_OK) return st;
+    if (batch < 1 || !std::isfinite(scale)) return PKV_ERR_INVALID;
+    if (!q || !key_cache || !value_cache || !block_tables || !seq_lens || !out || !workspace)
+        return PKV_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
+        return PKV_ERR_INVALID;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
+    if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))) return PKV_ERR_INVALID;
+    st = make_plan(pool->desc, batch, num_q_heads, max_blocks, opts, pl);
+    if (st != PKV_OK) return st;
+    if (workspace_bytes < pl.ws_bytes) return PKV_ERR_INVALID;
+    return PKV_OK;
+}
+
 int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, const void *v_new,
                 const void *key_cache, const void *value_cache, const int32_t *block_tables,
                 const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
@@ -114,18 +138,11 @@ int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, co
     if (st != PKV_OK) return st;
     if (batch < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID;
     if (batch == 0) return PKV_OK;
-    if (!q || !key_cache || !value_cache || !block_tables || !seq_lens || !out || !workspace)
-        return PKV_ERR_INVALID;
-    if (!aligned(q, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(out, 16) ||
-        !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
-        return PKV_ERR_INVALID;
-    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
-    if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))) return PKV_ERR_INVALID;
-    const pkv_pool_desc &d = pool->desc;
     Plan pl;
-    st = make_plan(d, batch, num_q_heads, max_blocks, opts, pl);
+    st = check_call(pool, q, k_new, v_new, key_cache, value_cache, block_tables, seq_lens, batch, num_q_heads,
+                    max_blocks, scale, out, workspace, workspace_bytes, opts, pl);
     if (st != PKV_OK) return st;
-    if (workspace_bytes < pl.ws_bytes) return PKV_ERR_INVALID;
+    const pkv_pool_desc &d = pool->desc;
 
     DecodeParams p;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -142,6 +159,7 @@ int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, co
     p.k_new = static_cast<const uint16_t *>(k_new);
     p.v_new = static_cast<const uint16_t *>(v_new);
     p.layers = layers;
+    p.test_stall = test_expire() == PKV_TEST_EXPIRE_DECODE;
     p.B = batch;
     p.Hq = num_q_heads;
     p.Hkv = d.num_kv_heads;
@@ -159,6 +177,17 @@ int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, co
 }
 
 }  // namespace
+
+int check_decode_call(const pkv_pool *pool, const void *q, const void *key_cache, const void *value_cache,
+                      const int32_t *block_tables, const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                      int32_t max_blocks, float scale, const void *out, const void *workspace,
+                      size_t workspace_bytes)
+{
+    Plan pl;
+    return check_call(pool, q, nullptr, nullptr, key_cache, value_cache, block_tables, seq_lens, batch,
+                      num_q_heads, max_blocks, scale, out, workspace, workspace_bytes, nullptr, pl);
+}
+
 }  // namespace decode
 }  // namespace pkv
 

@@ -96,6 +96,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     return false;
 }
 
+// The same with a caller-given time bound (ns), polled with the non-blocking probe so that
+// the bound holds even for a barrier whose phase never completes.
+__device__ __forceinline__ bool mbar_wait_bounded_ns(uint32_t bar, uint32_t parity, unsigned long long ns)
+{
+    const unsigned long long t0 = globaltimer();
+    for (unsigned i = 0; i < WAIT_POLLS; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 15u) == 15u && globaltimer() - t0 > ns) return false;
+    }
+    return false;
+}
+
+// Bound of the wait that pkv_test_expire_waits() makes a kernel run out (ns).
+constexpr unsigned long long TEST_EXPIRE_NS = 1000000ull;
+
 // 1-D bulk copy global -> this CTA's shared memory, completing on an mbarrier.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
@@ -133,6 +148,45 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D = A(16x32, row) * B(32x8, col) + C, E4M3 inputs (four codes per register, the lower k in
+// the lower byte), fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 matrices of 16-bit elements from shared memory: lanes 8i..8i+7 give the row
+// addresses of matrix i (16 bytes each); register i receives matrix i with lane l holding
+// row l/4, elements 2(l%4) and 2(l%4)+1 (the lower element in the low half).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// The same, transposed: lane l holds rows 2(l%4) and 2(l%4)+1 of element column l/4.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// Transpose an 8x8 matrix of 16-bit elements held one row pair per lane (lane l: row l/4,
+// elements 2(l%4), 2(l%4)+1): the result has the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
 }
 
 // Two E4M3 codes (low byte -> low half) to two fp16 values (exact).

@@ -26,8 +26,21 @@ namespace pkv {
 // Free the pool's prefix cache, if any (its block references are not released).
 void destroy_prefix_cache(pkv_pool *pool);
 
+// Which kernel (PKV_TEST_EXPIRE_*) the failure-path test hook currently targets.
+int test_expire();
+
 // Validation shared by the CUDA entry points.
 int check_attached(const pkv_pool *pool);
 inline int elem_bytes(const pkv_pool_desc &d) { return d.kv_dtype == PKV_KV_FP8E4M3 ? 1 : 2; }
+
+namespace decode {
+// Every host-side check of pkv_paged_attention_decode with batch >= 1 (arguments, alignment,
+// launch plan, workspace size), without launching or queueing anything: PKV_OK, or the
+// status that call would return.
+int check_decode_call(const pkv_pool *pool, const void *q, const void *key_cache, const void *value_cache,
+                      const int32_t *block_tables, const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                      int32_t max_blocks, float scale, const void *out, const void *workspace,
+                      size_t workspace_bytes);
+}  // namespace decode
 
 }  // namespace pkv

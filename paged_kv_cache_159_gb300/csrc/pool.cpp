@@ -10,6 +10,7 @@
 // steinslab.io page.
 #include <cuda_runtime_api.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -40,6 +41,12 @@ bool valid_desc(const pkv_pool_desc *d)
 }  // namespace
 
 namespace pkv {
+
+namespace {
+std::atomic<int> g_test_expire{PKV_TEST_EXPIRE_NONE};
+}
+
+int test_expire() { return g_test_expire.load(std::memory_order_relaxed); }
 
 int check_attached(const pkv_pool *pool)
 {
@@ -377,6 +384,14 @@ int pkv_device_sm_count(int device, int32_t *out)
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         return PKV_ERR_CUDA;
     *out = v;
+    return PKV_OK;
+}
+
+int pkv_test_expire_waits(int32_t which)
+{
+    if (which != PKV_TEST_EXPIRE_NONE && which != PKV_TEST_EXPIRE_DECODE && which != PKV_TEST_EXPIRE_PREFILL)
+        return PKV_ERR_INVALID;
+    pkv::g_test_expire.store(which, std::memory_order_relaxed);
     return PKV_OK;
 }
 

@@ -23,10 +23,10 @@
 //   * A host plan (pkv_prefill_plan) lists the units and assigns them, heaviest first, to
 //     the CTAs of a persistent one-wave grid (longest-processing-time first).  The same plan
 //     serves every layer of a batch.
-//   * One CTA per SM, 13 warps: warps 0, 10 and 11 issue the tiled bulk-tensor (TMA) loads of
-//     K, V and Q, warp 1 the tcgen05.mma instructions of S and warp 12 those of P.V; warps
-//     2-5 run the softmax and epilogue of q-tile 0, warps 6-9 of q-tile 1, one query row per
-//     thread.
+//   * One CTA per SM, 15 warps: warps 0, 10 and 11 issue the tiled bulk-tensor (TMA) loads of
+//     K, V and Q; warps 1 and 12 issue the tcgen05.mma instructions of S for q-tiles 0 and 1,
+//     warps 13 and 14 those of P.V for q-tiles 0 and 1; warps 2-5 run the softmax and
+//     epilogue of q-tile 0, warps 6-9 of q-tile 1, one query row per thread.
 //   * Per K/V tile of 64 keys (4 paged blocks): S = Q.K^T (M 128, N 64, K D) per q-tile into
 //     tensor memory (double-buffered, so the next S is computed while the softmax reads
 //     this one); the softmax masks (causal, by select), updates the running max and sum
@@ -97,6 +97,7 @@ struct Params {
     uint32_t *err;
     int MB, Hq, Hkv, group, TP, num_blocks, grid;
     float score_scale;           // scale * log2(e)
+    int test_stall;              // failure-path test: the Q loader waits on a barrier nothing completes
 };
 
 template <int D>
@@ -109,10 +110,10 @@ struct Smem {
     static constexpr int KSTAGE = H * KHALF;          // one K (or V) tile
     static constexpr int K = Q + H * QHALF;           // NS K tiles
     static constexpr int V = K + NS * KSTAGE;         // NS V tiles
-    static constexpr int BAR = V + NS * KSTAGE;       // 12 + 4 NS mbarriers, then the TMEM slot
+    static constexpr int BAR = V + NS * KSTAGE;       // 13 + 4 NS mbarriers, then the TMEM slot
     static constexpr int TOTAL = BAR + 512;
     static constexpr int ALLOC = TOTAL + 1024;        // alignment slack
-    static_assert(8 * (12 + 4 * NS) + 4 <= 512, "barrier area");
+    static_assert(8 * (13 + 4 * NS) + 4 <= 512, "barrier area");
     static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
@@ -146,7 +147,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     auto p_full = [&](int w, int J) { return bars + 8 * (6 + 3 * NSTAGE + 2 * w + (J & 1)); };
     auto o_done = [&](int s) { return bars + 8 * (10 + 3 * NSTAGE + s); };
     auto o_free = [&](int w) { return bars + 8 * (10 + 4 * NSTAGE + w); };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (12 + 4 * NSTAGE));
+    const uint32_t never = bars + 8 * (12 + 4 * NSTAGE);     // no thread ever arrives here
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (13 + 4 * NSTAGE));
 
     const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(p.plan);
     const int32_t *cta_off = reinterpret_cast<const int32_t *>(p.plan + sizeof(PlanHeader));
@@ -174,6 +176,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             dev::mbar_init(p_full(b, 1), 4);
             dev::mbar_init(o_free(b), 4);             // the q-tile's four warps read O
         }
+        dev::mbar_init(never, 1);
         dev::fence_barrier_init();
     }
     if (warp == 1) tc::tmem_alloc(dev::smem_u32(tmem_slot), TMEM_COLS);
@@ -210,8 +213,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // ============ TMA producer of Q: a unit's rows once the previous unit's last S is done
         if (lane == 0) {
             int uq = 0;
-            bool ok = true;
-            for (int u = u0; u < u1; ++u, ++uq) {
+            // the failure-path test: a wait that runs out before the first load (nothing in flight)
+            bool ok = !p.test_stall || dev::mbar_wait_bounded_ns(never, 0, dev::TEST_EXPIRE_NS);
+            for (int u = u0; u < u1 && ok; ++u, ++uq) {
                 const Unit un = units[u];
                 if (uq > 0 && !dev::mbar_wait_bounded(q_free, (uq - 1) & 1)) {
                     ok = false;
@@ -719,6 +723,7 @@ extern "C" int pkv_paged_prefill(pkv_pool *pool, const void *q, const void *key_
     p.num_blocks = d.num_blocks;
     p.grid = grid;
     p.score_scale = scale * LOG2E;
+    p.test_stall = pkv::test_expire() == PKV_TEST_EXPIRE_PREFILL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e = D == 128 ? launch<128>(qm, km, vm, p, s) : launch<64>(qm, km, vm, p, s);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
