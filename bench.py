@@ -480,8 +480,10 @@ def run_decode(args, name, world, rank, local_rank, K, W, full=True):
     value = aggregate_value(world, kv_unique, K, total)
     achieved = launch_unique / dec_mean / 1e9
     traffic = _profiled_traffic(name)
-    kernel = "decode_mma_kernel (%s%s)" % ("decode_step" if w.append and not args.separate_append
-                                           else "paged_attention_decode", ", %d layers" % nl if nl > 1 else "")
+    variant = (decode_opts or {}).get("variant", 0) or 3
+    kernel = "%s (%s%s)" % ({1: "decode_simt_kernel", 2: "decode_mma_kernel", 3: "decode_tok_kernel"}[variant],
+                            "decode_step" if w.append and not args.separate_append
+                            else "paged_attention_decode", ", %d layers" % nl if nl > 1 else "")
     step = (("copy_blocks + " if len(cow_pairs) else "") +
             (("kv_append + paged_attention_decode" if args.separate_append else
               "decode_step (append at L-1 + paged decode, one launch)") if w.append

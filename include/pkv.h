@@ -245,7 +245,8 @@ int pkv_kv_append_layers(pkv_pool *pool, const void *k, const void *v,
 /* Tuning knobs for pkv_paged_attention_decode_ex; zero fields mean "choose". */
 typedef struct {
     int32_t grid_ctas;        /* CTAs of the persistent grid (0 = SM count x CTAs per SM) */
-    int32_t variant;          /* 0 = auto, 1 = CUDA-core dot products, 2 = tensor-core mma */
+    int32_t variant;          /* 0 = auto (3); 1 = CUDA-core dot products; 2 = tensor-core mma with
+                                 the heads as rows; 3 = tensor-core mma with the tokens as rows */
     int32_t warps_per_cta;    /* 0 = auto (4); 4 or 8 */
     int32_t stages;           /* 0 = auto (16 KiB of tiles: 2 bf16 / 4 FP8 at D 128); 2..4 */
 } pkv_decode_opts;

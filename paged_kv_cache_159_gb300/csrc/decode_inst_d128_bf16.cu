@@ -2,4 +2,4 @@
 #include "decode_kernels.cuh"
 
 template cudaError_t pkv::decode::dispatch_nw_ns<128, false>(const pkv::decode::Plan &, int, bool, int *, cudaStream_t,
-                                                        const pkv::decode::DecodeParams *);
+                                                        const pkv::decode::LaunchArgs *);

@@ -60,6 +60,7 @@
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "tc_device.cuh"
 
 namespace pkv {
 namespace decode {
@@ -147,6 +148,7 @@ __device__ __forceinline__ long long task_start(int c, long long W, int G) { ret
 // ------------------------------------------------------------------------------------
 template <int D, bool FP8, bool G16>
 struct MmaCompute {
+    static constexpr bool SWIZZLED = false;    // linear tiles (1-D bulk copies)
     static constexpr int ELEM = FP8 ? 1 : 2;
     static constexpr int ROW = D * ELEM;
     static constexpr int KS = D / 16;                   // k-steps of S = Q.K^T
@@ -359,6 +361,7 @@ struct MmaCompute {
 // ------------------------------------------------------------------------------------
 template <int D, bool FP8, int GP>
 struct SimtCompute {
+    static constexpr bool SWIZZLED = false;    // linear tiles (1-D bulk copies)
     static constexpr int ELEM = FP8 ? 1 : 2;
     static constexpr int ROW = D * ELEM;
     static constexpr int EPL = D / 32;
@@ -480,15 +483,324 @@ struct SimtCompute {
 };
 
 // ------------------------------------------------------------------------------------
+// Tensor-core compute with the block's 16 tokens as the mma rows (variant 3).
+//
+//   S^T = K . Q^T      (M 16 tokens, N 8 query heads per n-tile, K head_dim)
+//   O^T += V^T . P^T   (M 16 output columns per m-tile, N 8 heads, K 16 tokens)
+//
+// The g <= 8 heads of a group fill one n-tile of 8 (two for g <= 16), so at most half of each
+// product is padding, against 3/4 with the heads as the 16 rows.  K and V tiles arrive in
+// shared memory through tensor (TMA) copies with a 128-byte swizzle (64-byte for 64-byte
+// rows), so the 8 token rows that one ldmatrix reads lie in 8 different bank groups: the
+// reads are conflict-free.  The same per-lane ldmatrix addresses serve K (plain) and V
+// (transposed).  P^T, the B operand of the second product, comes from the S^T accumulators by
+// one movmatrix per 8 tokens.
+//
+// FP8 pools: S^T runs on the E4M3 tensor-core product (k 32), K straight from shared memory.
+// The queries, scaled by a power of two per unit (exact) so that their largest magnitude lies
+// in [128, 256), are split into two E4M3 terms q = q_hi + q_lo; for every bf16 query value
+// whose scaled magnitude is at least 2^-2 the split is exact (the rounding residual of a
+// 4-significant-bit code on an 8-significant-bit value has at most 4 significant bits), and
+// below that its error is at most 2^-10 of the scaled value's unit, 2^-18 of the largest
+// query.  V codes are converted to fp16 (exact) after a transposed ldmatrix and multiplied
+// with P in fp16.
+// ------------------------------------------------------------------------------------
+template <int D, bool FP8, int NH>
+struct TokCompute {
+    static constexpr bool SWIZZLED = true;
+    static constexpr int ELEM = FP8 ? 1 : 2;
+    static constexpr int ROWB = D * ELEM;                 // bytes of one token row
+    static constexpr int SEG = ROWB < 128 ? ROWB : 128;   // bytes of one swizzled row segment
+    static constexpr int SEGBYTES = BS * SEG;             // one [16 tokens][SEG] segment of a tile
+    static constexpr int STEPS = ROWB / 32;               // ldmatrix.x4 steps (two 16-byte chunks each)
+    static constexpr int MT = D / 16;                     // m-tiles of O^T
+    static constexpr int NOFF = STEPS < 4 ? STEPS : 4;
+    static constexpr int QW = FP8 ? 4 : 2;                // B-fragment words of Q^T per step
+
+    uint32_t qb[STEPS][NH][QW];
+    float acc[MT][NH][4];
+    float m[NH][2], l[NH][2];
+    uint32_t loff[NOFF];          // this lane's ldmatrix row address within a tile, per step % 4
+    float base_sc = 0.f;          // scale * k_scale * log2(e)
+    float sc = 0.f;               // the unit's score scale (FP8: with the queries' power of two)
+
+    // Output column of O^T row r (0..15) of m-tile mt.
+    __device__ static int dcol(int mt, int r) { return FP8 ? 16 * mt + 2 * (r & 7) + (r >> 3) : 16 * mt + r; }
+    __device__ static int slot_of_d(int d) { return d; }
+
+    // Lane l gives the row address of ldmatrix matrix l/8: token (l%8) + 8((l/8)%2), 16-byte
+    // chunk 2 step + l/16.  With the swizzle the chunk lands at (chunk % 8) xor (row % 8)
+    // (128-byte segments) or chunk xor ((row/2) % 4) (64-byte rows).
+    __device__ void setup(int lane)
+    {
+        const int tok = (lane & 7) + 8 * ((lane >> 3) & 1), hi = lane >> 4;
+#pragma unroll
+        for (int k = 0; k < NOFF; ++k) {
+            if constexpr (SEG == 128) loff[k] = tok * 128 + (((2 * k) ^ (hi ^ (tok & 7))) << 4);
+            else loff[k] = tok * 64 + (((2 * k) ^ (hi ^ ((tok >> 1) & 3))) << 4);
+        }
+    }
+
+    __device__ __forceinline__ uint32_t step_addr(uint32_t tile, int i) const
+    {
+        return tile + loff[i & 3] + (uint32_t)((i >> 2) * SEGBYTES);
+    }
+
+    // Four E4M3 codes (round to nearest even, saturating) of four floats.
+    __device__ static uint32_t e4m3x4(float a, float b, float c, float d)
+    {
+        return dev::e4m3x2_satfinite(a, b) | (dev::e4m3x2_satfinite(c, d) << 16);
+    }
+    __device__ static float2 e4m3x2_value(uint32_t codes)
+    {
+        const uint32_t h = dev::e4m3x2_to_f16x2((uint16_t)codes);
+        return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    }
+
+    // Load the Q^T fragments of the unit's g query rows (bf16 [group][D] in shared memory)
+    // and reset the softmax state.  Heads past the group are zero.
+    __device__ void start(const uint16_t *qs, int group, int lane)
+    {
+        const int gid = lane >> 2, tid = lane & 3;
+        sc = base_sc;
+        if constexpr (!FP8) {
+#pragma unroll
+            for (int i = 0; i < STEPS; ++i)
+#pragma unroll
+                for (int j = 0; j < NH; ++j) {
+                    const int head = 8 * j + gid;
+                    const uint32_t *row = reinterpret_cast<const uint32_t *>(qs + head * D + 16 * i + 2 * tid);
+                    qb[i][j][0] = head < group ? row[0] : 0u;     // d 16i + 2tid, +1
+                    qb[i][j][1] = head < group ? row[4] : 0u;     // d 16i + 8 + 2tid, +1
+                }
+        } else {
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < STEPS; ++i)
+#pragma unroll
+                for (int j = 0; j < NH; ++j) {
+                    const int head = 8 * j + gid;
+                    uint2 lo = make_uint2(0u, 0u), hi = make_uint2(0u, 0u);
+                    if (head < group) {
+                        lo = *reinterpret_cast<const uint2 *>(qs + head * D + 32 * i + 4 * tid);        // d 32i+4tid..+3
+                        hi = *reinterpret_cast<const uint2 *>(qs + head * D + 32 * i + 16 + 4 * tid);   // d 32i+16+4tid..
+                    }
+                    qb[i][j][0] = lo.x; qb[i][j][1] = lo.y; qb[i][j][2] = hi.x; qb[i][j][3] = hi.y;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                        amax = fmaxf(amax, fmaxf(fabsf(dev::bf16_lo(qb[i][j][w])), fabsf(dev::bf16_hi(qb[i][j][w]))));
+                }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(dev::FULL, amax, o));
+            // 2^e: amax * 2^e in [128, 256); e within the normal exponent range
+            int e = 0;
+            if (amax > 0.f) e = 7 - (((__float_as_uint(amax) >> 23) & 0xff) - 127);
+            e = max(-126, min(126, e));
+            const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+            sc = base_sc * __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+            for (int i = 0; i < STEPS; ++i)
+#pragma unroll
+                for (int j = 0; j < NH; ++j) {
+                    float x[8];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        x[2 * w] = dev::bf16_lo(qb[i][j][w]) * up;
+                        x[2 * w + 1] = dev::bf16_hi(qb[i][j][w]) * up;
+                    }
+                    const uint32_t h0 = e4m3x4(x[0], x[1], x[2], x[3]), h1 = e4m3x4(x[4], x[5], x[6], x[7]);
+                    const float2 a = e4m3x2_value(h0), b = e4m3x2_value(h0 >> 16);
+                    const float2 c = e4m3x2_value(h1), d = e4m3x2_value(h1 >> 16);
+                    qb[i][j][0] = h0;                                   // b0 of the high term
+                    qb[i][j][1] = h1;                                   // b1 of the high term
+                    qb[i][j][2] = e4m3x4(x[0] - a.x, x[1] - a.y, x[2] - b.x, x[3] - b.y);   // low term
+                    qb[i][j][3] = e4m3x4(x[4] - c.x, x[5] - c.y, x[6] - d.x, x[7] - d.y);
+                }
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int j = 0; j < NH; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[mt][j][c] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+            m[j][0] = m[j][1] = -INFINITY;
+            l[j][0] = l[j][1] = 0.f;
+        }
+    }
+
+    __device__ __forceinline__ void pv_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+    {
+        if constexpr (FP8) dev::mma_f16_16816(d, a, b0, b1);
+        else dev::mma_bf16_16816(d, a, b0, b1);
+    }
+
+    // One 16-token block; PARTIAL: only tokens < ntok are valid (the rest masked by select).
+    template <bool PARTIAL>
+    __device__ __forceinline__ void block_impl(uint32_t kt, uint32_t vt, int ntok, int lane)
+    {
+        const int gid = lane >> 2, tid = lane & 3;
+        // ---- S^T = K Q^T: rows = tokens gid, gid + 8; columns = heads 8j + 2tid, +1
+        float s[NH][4];
+#pragma unroll
+        for (int j = 0; j < NH; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+        for (int i = 0; i < STEPS; ++i) {
+            uint32_t a[4];
+            dev::ldsm_x4(step_addr(kt, i), a);
+#pragma unroll
+            for (int j = 0; j < NH; ++j) {
+                if constexpr (FP8) {
+                    dev::mma_e4m3_16832(s[j], a, qb[i][j][0], qb[i][j][1]);
+                    dev::mma_e4m3_16832(s[j], a, qb[i][j][2], qb[i][j][3]);
+                } else {
+                    dev::mma_bf16_16816(s[j], a, qb[i][j][0], qb[i][j][1]);
+                }
+            }
+        }
+        // ---- scale, mask, lazy running max (heads 8j + 2tid + r: values c = r and r + 2)
+        bool need = false;
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float x = s[j][c] * sc;
+                s[j][c] = (!PARTIAL || gid + 8 * (c >> 1) < ntok) ? x : -INFINITY;
+            }
+            need |= fmaxf(s[j][0], s[j][2]) > m[j][0] + RESCALE_TAU;
+            need |= fmaxf(s[j][1], s[j][3]) > m[j][1] + RESCALE_TAU;
+        }
+        if (__any_sync(dev::FULL, need)) {
+#pragma unroll
+            for (int j = 0; j < NH; ++j)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    float mx = fmaxf(s[j][r], s[j][r + 2]);
+                    mx = fmaxf(mx, __shfl_xor_sync(dev::FULL, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(dev::FULL, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(dev::FULL, mx, 16));
+                    const float mn = fmaxf(m[j][r], mx);
+                    const float alpha = dev::fast_exp2(m[j][r] - mn);
+                    m[j][r] = mn;
+                    l[j][r] *= alpha;
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        acc[mt][j][r] *= alpha;
+                        acc[mt][j][r + 2] *= alpha;
+                    }
+                }
+        }
+        // ---- P = exp2(S - m); P^T as the B operand of the second product (one movmatrix per
+        //      8 tokens: tokens 2tid, 2tid+1 of head gid in b0, tokens 8 + those in b1)
+        uint32_t pb[NH][2];
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+            const float p0 = dev::fast_exp2(s[j][0] - m[j][0]), p1 = dev::fast_exp2(s[j][1] - m[j][1]);
+            const float p2 = dev::fast_exp2(s[j][2] - m[j][0]), p3 = dev::fast_exp2(s[j][3] - m[j][1]);
+            l[j][0] += p0 + p2;
+            l[j][1] += p1 + p3;
+            const uint32_t r0 = FP8 ? dev::pack_f16x2(p0, p1) : dev::pack_bf16x2(p0, p1);
+            const uint32_t r1 = FP8 ? dev::pack_f16x2(p2, p3) : dev::pack_bf16x2(p2, p3);
+            pb[j][0] = dev::movmatrix_trans(r0);
+            pb[j][1] = dev::movmatrix_trans(r1);
+        }
+        // ---- O^T += V^T P^T.  Transposed ldmatrix of step i: registers 0 and 2 hold tokens
+        //      2tid, 2tid+1 (low and high halves), 1 and 3 tokens 8 + those; rows past ntok are
+        //      zeroed in the registers (a NaN there would survive P = 0).
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if constexpr (PARTIAL) {
+            mlo = (2 * tid < ntok ? 0x0000ffffu : 0u) | (2 * tid + 1 < ntok ? 0xffff0000u : 0u);
+            mhi = (2 * tid + 8 < ntok ? 0x0000ffffu : 0u) | (2 * tid + 9 < ntok ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < STEPS; ++i) {
+            uint32_t v[4];
+            dev::ldsm_x4_trans(step_addr(vt, i), v);
+            if constexpr (PARTIAL) {
+                v[0] &= mlo; v[2] &= mlo;
+                v[1] &= mhi; v[3] &= mhi;
+            }
+            if constexpr (!FP8) {
+                // m-tile i: rows d 16i + gid (chunk 2i) and 16i + 8 + gid (chunk 2i + 1)
+                const uint32_t a[4] = {v[0], v[2], v[1], v[3]};
+#pragma unroll
+                for (int j = 0; j < NH; ++j) pv_mma(acc[i][j], a, pb[j][0], pb[j][1]);
+            } else {
+                // m-tiles 2i (chunk 2i: v0, v1) and 2i + 1 (chunk 2i + 1: v2, v3); a register's
+                // bytes are (token 2tid: d, d + 1), (token 2tid + 1: d, d + 1) with d = 2gid in
+                // the chunk: bytes 0 and 2 make row d, bytes 1 and 3 row d + 1
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t x = v[2 * h], y = v[2 * h + 1];
+                    const uint32_t a[4] = {dev::e4m3x2_to_f16x2((uint16_t)__byte_perm(x, 0u, 0x20u)),
+                                           dev::e4m3x2_to_f16x2((uint16_t)__byte_perm(x, 0u, 0x31u)),
+                                           dev::e4m3x2_to_f16x2((uint16_t)__byte_perm(y, 0u, 0x20u)),
+                                           dev::e4m3x2_to_f16x2((uint16_t)__byte_perm(y, 0u, 0x31u))};
+#pragma unroll
+                    for (int j = 0; j < NH; ++j) pv_mma(acc[2 * i + h][j], a, pb[j][0], pb[j][1]);
+                }
+            }
+        }
+    }
+
+    __device__ void block(const uint8_t *kt, const uint8_t *vt, int ntok, float /*score_scale*/, int lane)
+    {
+        if (ntok == BS) block_impl<false>(dev::smem_u32(kt), dev::smem_u32(vt), BS, lane);
+        else block_impl<true>(dev::smem_u32(kt), dev::smem_u32(vt), ntok, lane);
+    }
+
+    // Write this warp's (max, sum) rows and accumulators into the merge area ([head][d]).
+    __device__ void dump(float *ml, float *accs, int group, int lane)
+    {
+        const int gid = lane >> 2, tid = lane & 3;
+#pragma unroll
+        for (int j = 0; j < NH; ++j)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                float x = l[j][r];
+                x += __shfl_xor_sync(dev::FULL, x, 4);
+                x += __shfl_xor_sync(dev::FULL, x, 8);
+                x += __shfl_xor_sync(dev::FULL, x, 16);
+                l[j][r] = x;
+            }
+#pragma unroll
+        for (int j = 0; j < NH; ++j)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int head = 8 * j + 2 * tid + r;
+                if (head < group) {
+                    if (gid == 0) {
+                        ml[head * 2] = m[j][r];
+                        ml[head * 2 + 1] = l[j][r];
+                    }
+                    float *row = accs + head * (D + ACC_PAD);
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        row[dcol(mt, gid)] = acc[mt][j][r];
+                        row[dcol(mt, gid + 8)] = acc[mt][j][r + 2];
+                    }
+                }
+            }
+    }
+};
+
+// ------------------------------------------------------------------------------------
 // The decode kernel body: NW streaming warps and one epilogue warp.
 // ------------------------------------------------------------------------------------
 template <int D, bool FP8, int NW, int NS, class Compute>
-__device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
+__device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp, const CUtensorMap *kmap,
+                                            const CUtensorMap *vmap)
 {
     constexpr int ELEM = FP8 ? 1 : 2;
     constexpr int TILE = BS * D * ELEM;
     constexpr int NTHR = (NW + 1) * 32;
-    extern __shared__ __align__(1024) uint8_t smem[];
+    // swizzled tiles: SEG-byte row segments, [segment][16 tokens][SEG] per tile
+    constexpr int SEG = D * ELEM < 128 ? D * ELEM : 128;
+    constexpr int NSEG = D * ELEM / SEG;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the stage ring starts 1024-byte aligned (the swizzle pattern repeats every 1024 bytes)
+    uint8_t *smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
     const Layout lay(NW, NS, TILE, D, p.group, p.B);
     int32_t *prefix = reinterpret_cast<int32_t *>(smem + lay.prefix);
     int32_t *stage_tile = reinterpret_cast<int32_t *>(smem + lay.phys);
@@ -861,11 +1173,21 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp)
                 uint8_t *stage = smem + lay.stage + (warp * NS + st) * 2 * TILE;
                 stage_tile[warp * NS + st] = t;
                 if (t >= 0) {
-                    const size_t off = (size_t)t * TILE;
                     dev::fence_proxy_async_smem();
                     dev::mbar_arrive_expect_tx(bar, 2 * TILE);
-                    dev::bulk_g2s(dev::smem_u32(stage), p.key_cache + off, TILE, bar);
-                    dev::bulk_g2s(dev::smem_u32(stage + TILE), p.value_cache + off, TILE, bar);
+                    if constexpr (Compute::SWIZZLED) {
+                        // tensor copies [16 tokens][SEG bytes] per segment, swizzled
+                        const uint32_t dk = dev::smem_u32(stage);
+#pragma unroll
+                        for (int g = 0; g < NSEG; ++g) {
+                            tc::tma_load_3d(dk + g * BS * SEG, kmap, g * (SEG / ELEM), 0, t, bar);
+                            tc::tma_load_3d(dk + TILE + g * BS * SEG, vmap, g * (SEG / ELEM), 0, t, bar);
+                        }
+                    } else {
+                        const size_t off = (size_t)t * TILE;
+                        dev::bulk_g2s(dev::smem_u32(stage), p.key_cache + off, TILE, bar);
+                        dev::bulk_g2s(dev::smem_u32(stage + TILE), p.value_cache + off, TILE, bar);
+                    }
                 } else {
                     dev::mbar_arrive(bar);                    // nothing to copy; block is masked
                 }
@@ -944,7 +1266,18 @@ template <int D, bool FP8, int NW, int NS, bool G16>
 __global__ void __launch_bounds__((NW + 1) * 32, 8 / NW) decode_mma_kernel(const DecodeParams p)
 {
     MmaCompute<D, FP8, G16> cmp;
-    decode_body<D, FP8, NW, NS>(p, cmp);
+    decode_body<D, FP8, NW, NS>(p, cmp, nullptr, nullptr);
+}
+
+template <int D, bool FP8, int NW, int NS, int NH>
+__global__ void __launch_bounds__((NW + 1) * 32, 8 / NW)
+decode_tok_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const DecodeParams p)
+{
+    TokCompute<D, FP8, NH> cmp;
+    cmp.setup(threadIdx.x & 31);
+    cmp.base_sc = p.score_scale;
+    decode_body<D, FP8, NW, NS>(p, cmp, &kmap, &vmap);
 }
 
 template <int D, bool FP8, int NW, int NS, int GP>
@@ -952,12 +1285,18 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_simt_kernel(const Decode
 {
     SimtCompute<D, FP8, GP> cmp;
     cmp.sscale = p.score_scale;
-    decode_body<D, FP8, NW, NS>(p, cmp);
+    decode_body<D, FP8, NW, NS>(p, cmp, nullptr, nullptr);
 }
 
 // ------------------------------------------------------------------------------------
 // Launch plan and per-instantiation launchers.
 // ------------------------------------------------------------------------------------
+// Everything a launch needs: the parameters and, for variant 3, the K and V tensor maps.
+struct LaunchArgs {
+    DecodeParams p;
+    CUtensorMap kmap, vmap;
+};
+
 struct Plan {
     int variant, nw, ns;
     int grid;                 // CTAs (one wave)
@@ -1013,15 +1352,25 @@ cudaError_t prepare(K kernel, size_t smem, int threads, int *per_sm)
 // Either report CTAs per SM (launch == false) or launch.
 template <int D, bool FP8, int NW, int NS>
 cudaError_t run_decode(const Plan &pl, int group, bool launch, int *per_sm, cudaStream_t s,
-                       const DecodeParams *p)
+                       const LaunchArgs *a)
 {
     const int threads = (NW + 1) * 32;                   // + the epilogue warp
     auto go = [&](auto kernel) -> cudaError_t {
         cudaError_t e = prepare(kernel, pl.smem, threads, launch ? nullptr : per_sm);
         if (e != cudaSuccess || !launch) return e;
-        kernel<<<pl.grid, threads, pl.smem, s>>>(*p);
+        kernel<<<pl.grid, threads, pl.smem, s>>>(a->p);
         return cudaGetLastError();
     };
+    if (pl.variant == 3) {
+        auto go_tok = [&](auto kernel) -> cudaError_t {
+            cudaError_t e = prepare(kernel, pl.smem, threads, launch ? nullptr : per_sm);
+            if (e != cudaSuccess || !launch) return e;
+            kernel<<<pl.grid, threads, pl.smem, s>>>(a->kmap, a->vmap, a->p);
+            return cudaGetLastError();
+        };
+        if (group > 8) return go_tok(decode_tok_kernel<D, FP8, NW, NS, 2>);
+        return go_tok(decode_tok_kernel<D, FP8, NW, NS, 1>);
+    }
     if (pl.variant == 2) {
         if (group > 8) return go(decode_mma_kernel<D, FP8, NW, NS, true>);
         return go(decode_mma_kernel<D, FP8, NW, NS, false>);
@@ -1039,14 +1388,14 @@ cudaError_t run_decode(const Plan &pl, int group, bool launch, int *per_sm, cuda
 // for comparison only and is compiled for one pair.
 template <int D, bool FP8>
 cudaError_t dispatch_nw_ns(const Plan &pl, int group, bool launch, int *per_sm, cudaStream_t s,
-                           const DecodeParams *p)
+                           const LaunchArgs *a)
 {
     if (pl.variant == 1 && !(pl.nw == 4 && pl.ns == 2)) return cudaErrorInvalidConfiguration;
-    if (pl.nw == 4 && pl.ns == 2) return run_decode<D, FP8, 4, 2>(pl, group, launch, per_sm, s, p);
-    if (pl.nw == 4 && pl.ns == 3) return run_decode<D, FP8, 4, 3>(pl, group, launch, per_sm, s, p);
-    if (pl.nw == 4 && pl.ns == 4) return run_decode<D, FP8, 4, 4>(pl, group, launch, per_sm, s, p);
-    if (pl.nw == 8 && pl.ns == 2) return run_decode<D, FP8, 8, 2>(pl, group, launch, per_sm, s, p);
-    if (pl.nw == 8 && pl.ns == 3) return run_decode<D, FP8, 8, 3>(pl, group, launch, per_sm, s, p);
+    if (pl.nw == 4 && pl.ns == 2) return run_decode<D, FP8, 4, 2>(pl, group, launch, per_sm, s, a);
+    if (pl.nw == 4 && pl.ns == 3) return run_decode<D, FP8, 4, 3>(pl, group, launch, per_sm, s, a);
+    if (pl.nw == 4 && pl.ns == 4) return run_decode<D, FP8, 4, 4>(pl, group, launch, per_sm, s, a);
+    if (pl.nw == 8 && pl.ns == 2) return run_decode<D, FP8, 8, 2>(pl, group, launch, per_sm, s, a);
+    if (pl.nw == 8 && pl.ns == 3) return run_decode<D, FP8, 8, 3>(pl, group, launch, per_sm, s, a);
     return cudaErrorInvalidConfiguration;
 }
 

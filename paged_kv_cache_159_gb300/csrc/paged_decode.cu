@@ -9,13 +9,13 @@
 #include "decode_kernels.cuh"
 
 extern template cudaError_t pkv::decode::dispatch_nw_ns<128, false>(const pkv::decode::Plan &, int, bool, int *,
-                                                                    cudaStream_t, const pkv::decode::DecodeParams *);
+                                                                    cudaStream_t, const pkv::decode::LaunchArgs *);
 extern template cudaError_t pkv::decode::dispatch_nw_ns<128, true>(const pkv::decode::Plan &, int, bool, int *,
-                                                                   cudaStream_t, const pkv::decode::DecodeParams *);
+                                                                   cudaStream_t, const pkv::decode::LaunchArgs *);
 extern template cudaError_t pkv::decode::dispatch_nw_ns<64, false>(const pkv::decode::Plan &, int, bool, int *,
-                                                                   cudaStream_t, const pkv::decode::DecodeParams *);
+                                                                   cudaStream_t, const pkv::decode::LaunchArgs *);
 extern template cudaError_t pkv::decode::dispatch_nw_ns<64, true>(const pkv::decode::Plan &, int, bool, int *,
-                                                                  cudaStream_t, const pkv::decode::DecodeParams *);
+                                                                  cudaStream_t, const pkv::decode::LaunchArgs *);
 
 namespace pkv {
 namespace decode {
@@ -37,7 +37,7 @@ int sm_count_cached()
 }
 
 cudaError_t dispatch(const pkv_pool_desc &d, const Plan &pl, int group, bool launch, int *per_sm,
-                     cudaStream_t s, const DecodeParams *p)
+                     cudaStream_t s, const LaunchArgs *p)
 {
     const bool fp8 = d.kv_dtype == PKV_KV_FP8E4M3;
     if (d.head_dim == 128)
@@ -58,15 +58,15 @@ int make_plan(const pkv_pool_desc &d, int B, int Hq, int MB, const pkv_decode_op
     if ((long long)d.num_layers * B * d.num_kv_heads >= (1LL << 31)) return PKV_ERR_INVALID;
     pkv_decode_opts z{};
     if (!o) o = &z;
-    pl.variant = o->variant ? o->variant : 2;
-    if (pl.variant != 1 && pl.variant != 2) return PKV_ERR_INVALID;
+    pl.variant = o->variant ? o->variant : 3;
+    if (pl.variant < 1 || pl.variant > 3) return PKV_ERR_INVALID;
     if (pl.variant == 1 && group > 8) return PKV_ERR_INVALID;
     pl.nw = o->warps_per_cta ? o->warps_per_cta : 4;
     // default ring: 16 KiB of tiles per warp (2 bf16 or 4 FP8 stages at head_dim 128)
-    pl.ns = o->stages ? o->stages : (elem_bytes(d) == 1 && pl.variant == 2 ? 4 : 2);
+    pl.ns = o->stages ? o->stages : (elem_bytes(d) == 1 && pl.variant >= 2 ? 4 : 2);
     if (o->grid_ctas < 0) return PKV_ERR_INVALID;
     const int tile = BS * d.head_dim * elem_bytes(d);
-    pl.smem = Layout(pl.nw, pl.ns, tile, d.head_dim, group, B).total;
+    pl.smem = Layout(pl.nw, pl.ns, tile, d.head_dim, group, B).total + 1024;   // + alignment slack
     if (pl.smem > 227 * 1024) return PKV_ERR_INVALID;
     if (o->grid_ctas) {
         pl.grid = o->grid_ctas;
@@ -144,7 +144,22 @@ int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, co
     if (st != PKV_OK) return st;
     const pkv_pool_desc &d = pool->desc;
 
-    DecodeParams p;
+    LaunchArgs args;
+    DecodeParams &p = args.p;
+    if (pl.variant == 3) {
+        // K and V tiles of every (layer, block, head) of the launch: [tiles][16 tokens][row]
+        // with rows of D elements, copied per SEG-byte row segment with the matching swizzle
+        const int eb = elem_bytes(d), rowb = d.head_dim * eb, seg = rowb < 128 ? rowb : 128;
+        const uint64_t tiles = (uint64_t)layers * d.num_blocks * d.num_kv_heads;
+        const CUtensorMapDataType type = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const CUtensorMapSwizzle sw = seg == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        const uint64_t dims[3] = {(uint64_t)d.head_dim, (uint64_t)BS, tiles};
+        const uint64_t strides[2] = {(uint64_t)rowb, (uint64_t)rowb * BS};
+        const uint32_t box[3] = {(uint32_t)(seg / eb), (uint32_t)BS, 1u};
+        if (!encode_tiled_3d(&args.kmap, key_cache, type, dims, strides, box, sw) ||
+            !encode_tiled_3d(&args.vmap, value_cache, type, dims, strides, box, sw))
+            return PKV_ERR_CUDA;
+    }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.q = static_cast<const uint16_t *>(q);
     p.key_cache = static_cast<const uint8_t *>(key_cache);
@@ -171,7 +186,7 @@ int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, co
     p.inv_k_scale = pool->inv_k_scale;
     p.inv_v_scale = pool->inv_v_scale;
 
-    cudaError_t e = dispatch(d, pl, p.group, true, nullptr, static_cast<cudaStream_t>(stream), &p);
+    cudaError_t e = dispatch(d, pl, p.group, true, nullptr, static_cast<cudaStream_t>(stream), &args);
     if (e == cudaErrorInvalidConfiguration) return PKV_ERR_INVALID;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

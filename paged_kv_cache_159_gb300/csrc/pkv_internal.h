@@ -2,6 +2,8 @@
 // translation units of libpkv.so.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstdint>
 #include <deque>
 #include <vector>
@@ -25,6 +27,11 @@ namespace pkv {
 
 // Free the pool's prefix cache, if any (its block references are not released).
 void destroy_prefix_cache(pkv_pool *pool);
+
+// A 3-D tiled tensor map (TMA descriptor) over `ptr`: dims innermost first, strides in bytes
+// of dims 1 and 2, box in elements.  false if the driver's encoder is unavailable or refuses.
+bool encode_tiled_3d(CUtensorMap *map, const void *ptr, CUtensorMapDataType type, const uint64_t (&dims)[3],
+                     const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle);
 
 // Which kernel (PKV_TEST_EXPIRE_*) the failure-path test hook currently targets.
 int test_expire();

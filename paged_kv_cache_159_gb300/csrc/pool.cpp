@@ -8,11 +8,14 @@
 // stored once and referenced by many tables ("KV Cache 与推理优化", PagedAttention
 // section), which is why blocks carry reference counts.  Slot addressing is §3.3 of the
 // steinslab.io page.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime_api.h>
 
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "pkv_internal.h"
@@ -47,6 +50,26 @@ std::atomic<int> g_test_expire{PKV_TEST_EXPIRE_NONE};
 }
 
 int test_expire() { return g_test_expire.load(std::memory_order_relaxed); }
+
+bool encode_tiled_3d(CUtensorMap *map, const void *ptr, CUtensorMapDataType type, const uint64_t (&dims)[3],
+                     const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle)
+{
+    // the driver's encoder, looked up once through the runtime (no link against libcuda)
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    if (!enc) return false;
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]}, st[2] = {strides[0], strides[1]};
+    const cuuint32_t b[3] = {box[0], box[1], box[2]}, es[3] = {1, 1, 1};
+    return enc(map, type, 3, const_cast<void *>(ptr), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int check_attached(const pkv_pool *pool)
 {

@@ -504,30 +504,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 // ------------------------------------------------------------------------------------
 // Host side.
 // ------------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
 bool encode_3d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
                uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {d0, d1, d2}, strides[2] = {s1, s2};
-    const cuuint32_t box[3] = {b0, b1, b2}, es[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_tiled_3d(map, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, {d0, d1, d2}, {s1, s2}, {b0, b1, b2},
+                           CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int sm_count()

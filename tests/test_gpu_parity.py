@@ -146,19 +146,20 @@ def test_shapes_both_variants_and_grids(shape):
         pkv.kv_append(c.pool, c.k_new, c.v_new, slots, c.key_cache, c.value_cache)
         _append_bit_exact(c)
     ref = C.oracle_decode(c)
-    variants = [2] + ([1] if Hq // Hkv <= 8 else [])
+    variants = [3, 2] + ([1] if Hq // Hkv <= 8 else [])
     for variant in variants:
         # grid 1: every unit whole in one CTA; small grids: units cut across CTAs
         for grid in (0, 1, 2, 3, 7, 64, 1000):
             out = C.gpu_step(c, dict(variant=variant, grid_ctas=grid), append=False)
             C.tol_check(C.bf16_to_f64(out), ref)
-    for nw, ns in ((4, 2), (4, 4), (8, 2), (8, 3)):
-        for grid in (0, 5):
-            opts = dict(variant=2, warps_per_cta=nw, stages=ns, grid_ctas=grid)
-            if pkv.decode_workspace_bytes(c.pool, len(lens), Hq, bt.shape[1], opts) == 0:
-                continue                        # this ring does not fit in shared memory
-            out = C.gpu_step(c, opts, append=False)
-            C.tol_check(C.bf16_to_f64(out), ref)
+    for variant in (3, 2):
+        for nw, ns in ((4, 2), (4, 4), (8, 2), (8, 3)):
+            for grid in (0, 5):
+                opts = dict(variant=variant, warps_per_cta=nw, stages=ns, grid_ctas=grid)
+                if pkv.decode_workspace_bytes(c.pool, len(lens), Hq, bt.shape[1], opts) == 0:
+                    continue                        # this ring does not fit in shared memory
+                out = C.gpu_step(c, opts, append=False)
+                C.tol_check(C.bf16_to_f64(out), ref)
     # the same call twice gives the same bits
     a = C.gpu_step(c, dict(grid_ctas=7), append=False)
     b = C.gpu_step(c, dict(grid_ctas=7), append=False)
@@ -181,7 +182,8 @@ def test_physical_placement_does_not_change_a_single_bit():
         c.key_cache[pt] = kc0
         c.value_cache[pt] = vc0
         c.tables = np.where(t0 >= 0, perm[np.maximum(t0, 0)], -1).astype(np.int32)
-        for opts in (None, dict(grid_ctas=3), dict(grid_ctas=11), dict(variant=1), dict(warps_per_cta=8)):
+        for opts in (None, dict(grid_ctas=3), dict(grid_ctas=11), dict(variant=1), dict(variant=2),
+                     dict(warps_per_cta=8)):
             by_opts.setdefault(repr(opts), []).append(C.gpu_step(c, opts, append=False))
     for o, lst in by_opts.items():
         assert np.isfinite(lst[0].float().cpu().numpy()).all()
