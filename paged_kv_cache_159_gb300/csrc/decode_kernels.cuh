@@ -110,7 +110,7 @@ struct Layout {
         prefix = o; o += align_up((B + 1) * 4, 16);              // task prefix over sequences
         lens = o;   o += align_up(B * 4, 16);                    // seq_lens
         phys = o;   o += align_up(NW * NS * 4, 16);              // tile index per stage
-        bar = o;    o += (NW * NS + 7) * 8;                      // stages, q, segment done/free, never
+        bar = o;    o += (2 * NW * NS + 7) * 8;                  // stage full/empty, q, segment done/free, never
         flag = o;   o += 128;                                    // scan scratch, merge flag
         total = o;
     }
@@ -149,6 +149,7 @@ __device__ __forceinline__ long long task_start(int c, long long W, int G) { ret
 template <int D, bool FP8, bool G16>
 struct MmaCompute {
     static constexpr bool SWIZZLED = false;    // linear tiles (1-D bulk copies)
+    static constexpr bool IDENTITY_SLOTS = false;   // merge-area columns in fragment order
     static constexpr int ELEM = FP8 ? 1 : 2;
     static constexpr int ROW = D * ELEM;
     static constexpr int KS = D / 16;                   // k-steps of S = Q.K^T
@@ -362,6 +363,7 @@ struct MmaCompute {
 template <int D, bool FP8, int GP>
 struct SimtCompute {
     static constexpr bool SWIZZLED = false;    // linear tiles (1-D bulk copies)
+    static constexpr bool IDENTITY_SLOTS = true;    // merge-area column d at d
     static constexpr int ELEM = FP8 ? 1 : 2;
     static constexpr int ROW = D * ELEM;
     static constexpr int EPL = D / 32;
@@ -508,6 +510,7 @@ struct SimtCompute {
 template <int D, bool FP8, int NH>
 struct TokCompute {
     static constexpr bool SWIZZLED = true;
+    static constexpr bool IDENTITY_SLOTS = true;    // merge-area column d at d
     static constexpr int ELEM = FP8 ? 1 : 2;
     static constexpr int ROWB = D * ELEM;                 // bytes of one token row
     static constexpr int SEG = ROWB < 128 ? ROWB : 128;   // bytes of one swizzled row segment
@@ -794,7 +797,10 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
 {
     constexpr int ELEM = FP8 ? 1 : 2;
     constexpr int TILE = BS * D * ELEM;
-    constexpr int NTHR = (NW + 1) * 32;
+    constexpr int NWARP = NW + 2;                 // NW consumers, the epilogue warp, the producer
+    constexpr int NTHR = NWARP * 32;
+    constexpr int NSTAGE = NW * NS;               // CTA-wide ring; stage i % NSTAGE, consumer i % NW
+    static_assert(NSTAGE <= 32 && 32 % NW == 0, "one producer lane per stage, whole steps per 32 tasks");
     // swizzled tiles: SEG-byte row segments, [segment][16 tokens][SEG] per tile
     constexpr int SEG = D * ELEM < 128 ? D * ELEM : 128;
     constexpr int NSEG = D * ELEM / SEG;
@@ -812,10 +818,12 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
     // ---- 0. warm L2 with this CTA's share of the block tables and queries (hints), and
     //         set up the barriers; both overlap the scan below.
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar);
-    const uint32_t qbar0 = dev::smem_u32(bars + NW * NS);         // q slot j full: +8*j
-    const uint32_t done0 = dev::smem_u32(bars + NW * NS + 2);     // merge slot j dumped
-    const uint32_t free0 = dev::smem_u32(bars + NW * NS + 4);     // merge slot j merged
-    const uint32_t never = dev::smem_u32(bars + NW * NS + 6);     // no thread ever arrives here
+    const uint32_t full0 = dev::smem_u32(bars);                   // stage j loaded: +8*j
+    const uint32_t empty0 = dev::smem_u32(bars + NSTAGE);         // stage j consumed: +8*j
+    const uint32_t qbar0 = dev::smem_u32(bars + 2 * NSTAGE);      // q slot j full: +8*j
+    const uint32_t done0 = dev::smem_u32(bars + 2 * NSTAGE + 2);  // merge slot j dumped
+    const uint32_t free0 = dev::smem_u32(bars + 2 * NSTAGE + 4);  // merge slot j merged
+    const uint32_t never = dev::smem_u32(bars + 2 * NSTAGE + 6);  // no thread ever arrives here
     if (tid == 0) {
         auto slice = [&](const void *base, size_t bytes) {
             const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + bytes * c / gridDim.x + 15) & ~uintptr_t(15);
@@ -831,8 +839,10 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
         }
         dev::mbar_init(never, 1);
     }
-    if (lane == 0 && warp < NW)
-        for (int st = 0; st < NS; ++st) dev::mbar_init(dev::smem_u32(bars + warp * NS + st), 1);
+    if (warp == NW + 1 && lane < NSTAGE) {
+        dev::mbar_init(full0 + 8 * lane, 1);          // the producer's arrive (+ the copies' bytes)
+        dev::mbar_init(empty0 + 8 * lane, 1);         // the consumer warp's arrive
+    }
     dev::fence_barrier_init();
 
     // ---- 1. tasks per sequence (Hkv * ceil(L/16); 0 for an invalid length) and their
@@ -867,7 +877,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             lo = min(lo, __shfl_xor_sync(dev::FULL, lo, o));
             hi = max(hi, __shfl_xor_sync(dev::FULL, hi, o));
         }
-        int *wsum = flag, *wlo = flag + 9, *whi = flag + 18;   // NW + 1 <= 9 warps
+        int *wsum = flag, *wlo = flag + 10, *whi = flag + 20;  // NWARP <= 10 warps
         if (lane == 31) wsum[warp] = incl;
         if (lane == 0) {
             wlo[warp] = lo;
@@ -880,7 +890,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             // every CTA gets whole units and nothing is merged.  Lanes test 32 candidates at
             // a time; the result goes to flag[30] (0: keep the grid).
             int glo = INT_MAX, ghi = -1;
-            for (int w = 0; w <= NW; ++w) {
+            for (int w = 0; w < NWARP; ++w) {
                 glo = min(glo, wlo[w]);
                 ghi = max(ghi, whi[w]);
             }
@@ -948,36 +958,69 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
     auto seg_epilogue = [&](const Unit &u, long long seg_lo, long long seg_hi, int k, bool team_cta) {
         const long long U1 = u.U0 + u.nb;
         const int tt = team_cta ? tid : lane, tn = team_cta ? NTHR : 32;
-        const int twarp = team_cta ? warp : 0, tnw = team_cta ? NW + 1 : 1;
+        const int twarp = team_cta ? warp : 0, tnw = team_cta ? NWARP : 1;
         const float *ml_all = ml_base + (k & 1) * (lay.ml_slot / 4);
         const float *acc_all = acc_base + (k & 1) * (lay.acc_slot / 4);
         const bool whole = seg_lo == u.U0 && seg_hi == U1;
         const int slot = k == 0 ? 0 : 1;
         const size_t prow = ((size_t)c * 2 + slot) * group;        // partial rows of this CTA
-        for (int x = tt; x < group * D; x += tn) {
-            const int row = x / D, d = x - row * D;
-            const int sd = Compute::slot_of_d(d);
-            float M = -INFINITY;
+        // a warp per output row: the streaming warps' weights 2^(m_w - M) and the sum once per
+        // row, then lane l combines columns l*DPL .. l*DPL + DPL - 1 (vector accesses where the
+        // merge area keeps columns in order)
+        constexpr int DPL = D / 32;
+        for (int row = twarp; row < group; row += tnw) {
+            float mw[NW], M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) M = fmaxf(M, ml_all[w * 32 + row * 2]);
-            float num = 0.f, den = 0.f;
-            if (M != -INFINITY) {
+            for (int w = 0; w < NW; ++w) {
+                mw[w] = ml_all[w * 32 + row * 2];
+                M = fmaxf(M, mw[w]);
+            }
+            float wt[NW], den = 0.f;
 #pragma unroll
-                for (int w = 0; w < NW; ++w) {
-                    const float mw = ml_all[w * 32 + row * 2];
-                    const float wt = mw == -INFINITY ? 0.f : dev::fast_exp2(mw - M);
-                    num += wt * acc_all[(w * group + row) * rowstride + sd];
-                    den += wt * ml_all[w * 32 + row * 2 + 1];
+            for (int w = 0; w < NW; ++w) {
+                wt[w] = (M == -INFINITY || mw[w] == -INFINITY) ? 0.f : dev::fast_exp2(mw[w] - M);
+                den += wt[w] * ml_all[w * 32 + row * 2 + 1];
+            }
+            float num[DPL];
+#pragma unroll
+            for (int x = 0; x < DPL; ++x) num[x] = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float *src = acc_all + (w * group + row) * rowstride;
+                float a[DPL];
+                if constexpr (Compute::IDENTITY_SLOTS && DPL == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src + lane * 4);
+                    a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
+                } else if constexpr (Compute::IDENTITY_SLOTS && DPL == 2) {
+                    const float2 v = *reinterpret_cast<const float2 *>(src + lane * 2);
+                    a[0] = v.x; a[1] = v.y;
+                } else {
+#pragma unroll
+                    for (int x = 0; x < DPL; ++x) a[x] = src[Compute::slot_of_d(lane * DPL + x)];
                 }
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) num[x] += wt[w] * a[x];
             }
             if (whole) {
-                const float o = den > 0.f ? num / den * p.out_scale : 0.f;
-                const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-                p.out[((size_t)u.lb * p.Hq + (size_t)u.h * group + row) * D + d] =
-                    *reinterpret_cast<const uint16_t *>(&ob);
+                uint16_t ob[DPL];
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) {
+                    const __nv_bfloat16 b = __float2bfloat16_rn(den > 0.f ? num[x] / den * p.out_scale : 0.f);
+                    ob[x] = *reinterpret_cast<const uint16_t *>(&b);
+                }
+                uint16_t *dst = p.out + ((size_t)u.lb * p.Hq + (size_t)u.h * group + row) * D + lane * DPL;
+                if constexpr (DPL == 4)
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(ob[0] | ((uint32_t)ob[1] << 16), ob[2] | ((uint32_t)ob[3] << 16));
+                else
+                    *reinterpret_cast<uint32_t *>(dst) = ob[0] | ((uint32_t)ob[1] << 16);
             } else {
-                p.part_o[(prow + row) * D + d] = num * p.out_scale;
-                if (d == 0) {
+                float *dst = p.part_o + (prow + row) * D + lane * DPL;
+                if constexpr (DPL == 4)
+                    *reinterpret_cast<float4 *>(dst) = make_float4(num[0] * p.out_scale, num[1] * p.out_scale,
+                                                                   num[2] * p.out_scale, num[3] * p.out_scale);
+                else
+                    *reinterpret_cast<float2 *>(dst) = make_float2(num[0] * p.out_scale, num[1] * p.out_scale);
+                if (lane == 0) {
                     p.part_ml[(prow + row) * 2] = M;
                     p.part_ml[(prow + row) * 2 + 1] = den;
                 }
@@ -1006,7 +1049,6 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
         // merge: a warp per output row, lanes own D/32 columns; an online merge over the
         // partials in CTA order, four partials' loads in flight at a time
         const bool c0_shared = task_start(c0, W, G) < u.U0;          // unit is c0's 2nd+ segment
-        constexpr int DPL = D / 32;
         for (int row = twarp; row < group; row += tnw) {
             float Mr = -INFINITY, den = 0.f, num[DPL];
 #pragma unroll
@@ -1093,20 +1135,23 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             if (lane == 0) dev::mbar_arrive(free0 + 8 * (k & 1)); // merge slot k&1 reusable
             seg_lo = seg_hi;
         }
-    } else {
-        // ================= streaming warps ==================================================
-        // ---- 3. per-warp producer: tasks r_i = s + warp + NW*i, copies issued NS ahead
-        const int n_mine = (int)max(0LL, (e - s - warp + NW - 1) / NW);
+    } else if (warp == NW + 1) {
+        // ================= producer warp: every copy of the CTA's tasks ===================
+        // Task i of the CTA (global task s + i) is loaded into stage i % NSTAGE and consumed
+        // by warp i % NW.  The tasks go NW at a time: lane j < NW issues task i0 + j, so one
+        // warp-instruction issues the copies of a whole step, once each of those stages has
+        // been released by its consumer.
+        const int n_all = (int)(e - s);
         // tile index ((layer * NB + phys) * Hkv + h, or -1 if the table entry is invalid) of
-        // warp task i, for a chunk of 32 tasks: lane j holds task chunk*32 + j; and, when
-        // appending, (layer * B + b) * 16 + the new token's offset if task i is its unit's last
-        // block
+        // task i, for a chunk of 32 tasks: lane x holds task chunk*32 + x; and, when
+        // appending, (layer * B + b) * 16 + the new token's offset if task i is its unit's
+        // last block
         auto load_tiles = [&](int chunk, int &app) {
             const int i = chunk * 32 + lane;
             int t = -1;
             app = -1;
-            if (i < n_mine) {
-                const long long r = s + warp + (long long)NW * i;
+            if (i < n_all) {
+                const long long r = s + i;
                 const Unit u = unit_of(r);
                 const int blk = (int)(r - u.U0);
                 const int id = __ldg(p.block_tables + (size_t)u.b * p.MB + blk);
@@ -1116,88 +1161,118 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             }
             return t;
         };
+        // the whole warp writes the new token's K/V row (a = (layer * B + b) * 16 + offset)
+        // into tile t's slot
+        auto write_row = [&](int a, int t) {
+            const int lb = a / BS, off = a % BS, h = t % Hkv;
+            const size_t src = ((size_t)lb * Hkv + h) * D;
+            const size_t dst = ((size_t)t * BS + off) * D;               // element index
+            constexpr int EPL = D / 32;
+            if constexpr (FP8) {
+                const uint16_t *ks = p.k_new + src + lane * EPL;
+                const uint16_t *vs = p.v_new + src + lane * EPL;
+                uint32_t kc = 0, vc = 0;
+#pragma unroll
+                for (int x = 0; x < EPL; x += 2) {
+                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(ks + x);
+                    const uint32_t vw = *reinterpret_cast<const uint32_t *>(vs + x);
+                    kc |= dev::e4m3x2_satfinite(dev::bf16_lo(kw) * p.inv_k_scale, dev::bf16_hi(kw) * p.inv_k_scale) << (8 * x);
+                    vc |= dev::e4m3x2_satfinite(dev::bf16_lo(vw) * p.inv_v_scale, dev::bf16_hi(vw) * p.inv_v_scale) << (8 * x);
+                }
+                uint8_t *kd = const_cast<uint8_t *>(p.key_cache) + dst + lane * EPL;
+                uint8_t *vd = const_cast<uint8_t *>(p.value_cache) + dst + lane * EPL;
+                if constexpr (EPL == 4) {
+                    *reinterpret_cast<uint32_t *>(kd) = kc;
+                    *reinterpret_cast<uint32_t *>(vd) = vc;
+                } else {
+                    *reinterpret_cast<uint16_t *>(kd) = (uint16_t)kc;
+                    *reinterpret_cast<uint16_t *>(vd) = (uint16_t)vc;
+                }
+            } else {
+                uint16_t *kd = reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(p.key_cache)) + dst + lane * EPL;
+                uint16_t *vd = reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(p.value_cache)) + dst + lane * EPL;
+                if constexpr (EPL == 4) {
+                    *reinterpret_cast<uint2 *>(kd) = *reinterpret_cast<const uint2 *>(p.k_new + src + lane * EPL);
+                    *reinterpret_cast<uint2 *>(vd) = *reinterpret_cast<const uint2 *>(p.v_new + src + lane * EPL);
+                } else {
+                    *reinterpret_cast<uint32_t *>(kd) = *reinterpret_cast<const uint32_t *>(p.k_new + src + lane * EPL);
+                    *reinterpret_cast<uint32_t *>(vd) = *reinterpret_cast<const uint32_t *>(p.v_new + src + lane * EPL);
+                }
+            }
+        };
         int acur, anext;
         int tcur = load_tiles(0, acur), tnext = load_tiles(1, anext);
-        auto issue = [&](int i) {                              // warp-collective
-            if ((i & 31) == 0 && i > 0) {
+        bool ok = true;
+        int issued = 0;                                   // tasks whose copies are issued
+        for (int i0 = 0; i0 < n_all; i0 += NW) {
+            if ((i0 & 31) == 0 && i0 > 0) {
                 tcur = tnext;
                 acur = anext;
-                tnext = load_tiles((i >> 5) + 1, anext);
+                tnext = load_tiles((i0 >> 5) + 1, anext);
             }
+            const int i = i0 + lane % NW;
             const int t = __shfl_sync(dev::FULL, tcur, i & 31);
             const int a = __shfl_sync(dev::FULL, acur, i & 31);
-            if (a >= 0) {
-                // this block holds the new token: write its K/V row into the slot first, then
-                // order those generic writes before the bulk copy that reads the block
-                const int lb = a / BS, off = a % BS, h = t % Hkv;
-                const size_t src = ((size_t)lb * Hkv + h) * D;
-                const size_t dst = ((size_t)t * BS + off) * D;               // element index
-                constexpr int EPL = D / 32;
-                if constexpr (FP8) {
-                    const uint16_t *ks = p.k_new + src + lane * EPL;
-                    const uint16_t *vs = p.v_new + src + lane * EPL;
-                    uint32_t kc = 0, vc = 0;
-    #pragma unroll
-                    for (int e = 0; e < EPL; e += 2) {
-                        const uint32_t kw = *reinterpret_cast<const uint32_t *>(ks + e);
-                        const uint32_t vw = *reinterpret_cast<const uint32_t *>(vs + e);
-                        kc |= dev::e4m3x2_satfinite(dev::bf16_lo(kw) * p.inv_k_scale, dev::bf16_hi(kw) * p.inv_k_scale) << (8 * e);
-                        vc |= dev::e4m3x2_satfinite(dev::bf16_lo(vw) * p.inv_v_scale, dev::bf16_hi(vw) * p.inv_v_scale) << (8 * e);
-                    }
-                    uint8_t *kd = const_cast<uint8_t *>(p.key_cache) + dst + lane * EPL;
-                    uint8_t *vd = const_cast<uint8_t *>(p.value_cache) + dst + lane * EPL;
-                    if constexpr (EPL == 4) {
-                        *reinterpret_cast<uint32_t *>(kd) = kc;
-                        *reinterpret_cast<uint32_t *>(vd) = vc;
-                    } else {
-                        *reinterpret_cast<uint16_t *>(kd) = (uint16_t)kc;
-                        *reinterpret_cast<uint16_t *>(vd) = (uint16_t)vc;
-                    }
-                } else {
-                    uint16_t *kd = reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(p.key_cache)) + dst + lane * EPL;
-                    uint16_t *vd = reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(p.value_cache)) + dst + lane * EPL;
-                    if constexpr (EPL == 4) {
-                        *reinterpret_cast<uint2 *>(kd) = *reinterpret_cast<const uint2 *>(p.k_new + src + lane * EPL);
-                        *reinterpret_cast<uint2 *>(vd) = *reinterpret_cast<const uint2 *>(p.v_new + src + lane * EPL);
-                    } else {
-                        *reinterpret_cast<uint32_t *>(kd) = *reinterpret_cast<const uint32_t *>(p.k_new + src + lane * EPL);
-                        *reinterpret_cast<uint32_t *>(vd) = *reinterpret_cast<const uint32_t *>(p.v_new + src + lane * EPL);
-                    }
+            const bool mine = lane < NW && i < n_all;
+            const int st = i % NSTAGE;
+            // the stage's previous task has been consumed
+            const bool freed = !mine || i < NSTAGE ||
+                               dev::mbar_wait_bounded(empty0 + 8 * st, (uint32_t)(((i / NSTAGE) - 1) & 1));
+            if (!__all_sync(dev::FULL, freed)) {
+                ok = false;
+                break;
+            }
+            // blocks holding a new token: write each K/V row into its slot first, then order
+            // those generic writes before the copies that read the block
+            unsigned am = __ballot_sync(dev::FULL, mine && a >= 0);
+            if (am) {
+                while (am) {
+                    const int from = __ffs(am) - 1;
+                    am &= am - 1;
+                    write_row(__shfl_sync(dev::FULL, a, from), __shfl_sync(dev::FULL, t, from));
                 }
                 dev::fence_proxy_async_global();
                 __syncwarp();
             }
-            if (lane == 0) {
-                const int st = i % NS;
-                const uint32_t bar = dev::smem_u32(bars + warp * NS + st);
-                uint8_t *stage = smem + lay.stage + (warp * NS + st) * 2 * TILE;
-                stage_tile[warp * NS + st] = t;
+            if (mine) {
+                const uint32_t bar = full0 + 8 * st;
+                stage_tile[st] = t;
                 if (t >= 0) {
-                    dev::fence_proxy_async_smem();
                     dev::mbar_arrive_expect_tx(bar, 2 * TILE);
+                    const uint32_t dk = dev::smem_u32(smem + lay.stage + st * 2 * TILE);
                     if constexpr (Compute::SWIZZLED) {
-                        // tensor copies [16 tokens][SEG bytes] per segment, swizzled
-                        const uint32_t dk = dev::smem_u32(stage);
-#pragma unroll
-                        for (int g = 0; g < NSEG; ++g) {
-                            tc::tma_load_3d(dk + g * BS * SEG, kmap, g * (SEG / ELEM), 0, t, bar);
-                            tc::tma_load_3d(dk + TILE + g * BS * SEG, vmap, g * (SEG / ELEM), 0, t, bar);
+                        // one tensor copy per tile, [segment][16 tokens][SEG bytes], swizzled
+                        // (two row segments: a 4-D map whose third dimension is the segment)
+                        if constexpr (NSEG == 2) {
+                            tc::tma_load_4d(dk, kmap, 0, 0, 0, t, bar);
+                            tc::tma_load_4d(dk + TILE, vmap, 0, 0, 0, t, bar);
+                        } else {
+                            static_assert(NSEG == 1, "row segments");
+                            tc::tma_load_3d(dk, kmap, 0, 0, t, bar);
+                            tc::tma_load_3d(dk + TILE, vmap, 0, 0, t, bar);
                         }
                     } else {
                         const size_t off = (size_t)t * TILE;
-                        dev::bulk_g2s(dev::smem_u32(stage), p.key_cache + off, TILE, bar);
-                        dev::bulk_g2s(dev::smem_u32(stage + TILE), p.value_cache + off, TILE, bar);
+                        dev::bulk_g2s(dk, p.key_cache + off, TILE, bar);
+                        dev::bulk_g2s(dk + TILE, p.value_cache + off, TILE, bar);
                     }
                 } else {
-                    dev::mbar_arrive(bar);                    // nothing to copy; block is masked
+                    dev::mbar_arrive(bar);                // nothing to copy; the block is masked
                 }
             }
-        };
-        int ip = 0;
-        for (; ip < NS && ip < n_mine; ++ip) issue(ip);
-
-
-        // ---- 4. segments
+            issued = min(n_all, i0 + NW);
+        }
+        if (!ok && lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+        // no copy may land after the CTA has left: wait (bounded) for the last task issued
+        // into each stage (at once if its consumer already has)
+        if (lane < NSTAGE && lane < issued) {
+            const int last = lane + (issued - 1 - lane) / NSTAGE * NSTAGE;
+            (void)dev::mbar_wait_bounded(full0 + 8 * lane, (uint32_t)((last / NSTAGE) & 1));
+        }
+    } else {
+        // ================= consumer warps: tasks warp, warp + NW, ... of the CTA =========
+        const int n_all = (int)(e - s);
+        const int n_mine = max(0, (n_all - warp + NW - 1) / NW);
         bool aborted = false;
         if (p.test_stall)          // the failure-path test: a wait that runs out (copies in flight)
             aborted = !__all_sync(dev::FULL, dev::mbar_wait_bounded_ns(never, 0, dev::TEST_EXPIRE_NS));
@@ -1210,21 +1285,20 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             aborted |= !qok;
             cmp.start(reinterpret_cast<const uint16_t *>(smem + lay.q + (k & 1) * qslot_bytes), group, lane);
             while (!aborted && ic < n_mine && s + warp + (long long)NW * ic < seg_hi) {
-                const int st = ic % NS;
-                const uint32_t bar = dev::smem_u32(bars + warp * NS + st);
-                if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(bar, (uint32_t)((ic / NS) & 1)))) {
+                const int i = warp + NW * ic;
+                const int st = i % NSTAGE;
+                if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(full0 + 8 * st, (uint32_t)((i / NSTAGE) & 1)))) {
                     aborted = true;
                     break;
                 }
-                const long long r = s + warp + (long long)NW * ic;
-                const int blk = (int)(r - u.U0);
-                const int ntok = stage_tile[warp * NS + st] >= 0 ? min(BS, u.L - blk * BS) : 0;
+                const int blk = (int)(s + i - u.U0);
+                const int ntok = stage_tile[st] >= 0 ? min(BS, u.L - blk * BS) : 0;
                 if (ntok > 0) {
-                    const uint8_t *stage = smem + lay.stage + (warp * NS + st) * 2 * TILE;
+                    const uint8_t *stage = smem + lay.stage + st * 2 * TILE;
                     cmp.block(stage, stage + TILE, ntok, p.score_scale, lane);
                 }
                 __syncwarp();
-                if (ip < n_mine) issue(ip++);
+                if (lane == 0) dev::mbar_arrive(empty0 + 8 * st);   // the stage may be reloaded
                 ++ic;
             }
             // hand this segment's state to the epilogue (merge slot k&1, free once the
@@ -1236,13 +1310,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             if (seg_hi < e) dev::mbar_arrive(done0 + 8 * (k & 1));
             seg_lo = seg_hi;
         }
-        if (aborted) {
-            // A wait gave up: report it, then give the copies still in flight one more
-            // bounded wait so that none lands after this CTA has left.
-            if (lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
-            for (int i = ic; i < ip; ++i)
-                (void)dev::mbar_wait_bounded(dev::smem_u32(bars + warp * NS + i % NS), (uint32_t)((i / NS) & 1));
-        }
+        // a wait gave up: report it (the producer waits for every copy it issued)
+        if (aborted && lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
     }
 
     // ---- 5. the CTA's last segment, by every warp together
@@ -1260,17 +1329,17 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
     }
 }
 
-// Register budget for two CTAs of NW + 1 warps per SM (the shared-memory ring allows no
+// Register budget for two CTAs of NW + 2 warps per SM (the shared-memory ring allows no
 // more with NW = 4).
 template <int D, bool FP8, int NW, int NS, bool G16>
-__global__ void __launch_bounds__((NW + 1) * 32, 8 / NW) decode_mma_kernel(const DecodeParams p)
+__global__ void __launch_bounds__((NW + 2) * 32, 8 / NW) decode_mma_kernel(const DecodeParams p)
 {
     MmaCompute<D, FP8, G16> cmp;
     decode_body<D, FP8, NW, NS>(p, cmp, nullptr, nullptr);
 }
 
 template <int D, bool FP8, int NW, int NS, int NH>
-__global__ void __launch_bounds__((NW + 1) * 32, 8 / NW)
+__global__ void __launch_bounds__((NW + 2) * 32, 8 / NW)
 decode_tok_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p)
 {
@@ -1281,7 +1350,7 @@ decode_tok_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 }
 
 template <int D, bool FP8, int NW, int NS, int GP>
-__global__ void __launch_bounds__((NW + 1) * 32) decode_simt_kernel(const DecodeParams p)
+__global__ void __launch_bounds__((NW + 2) * 32) decode_simt_kernel(const DecodeParams p)
 {
     SimtCompute<D, FP8, GP> cmp;
     cmp.sscale = p.score_scale;
@@ -1354,7 +1423,7 @@ template <int D, bool FP8, int NW, int NS>
 cudaError_t run_decode(const Plan &pl, int group, bool launch, int *per_sm, cudaStream_t s,
                        const LaunchArgs *a)
 {
-    const int threads = (NW + 1) * 32;                   // + the epilogue warp
+    const int threads = (NW + 2) * 32;                   // + the epilogue and producer warps
     auto go = [&](auto kernel) -> cudaError_t {
         cudaError_t e = prepare(kernel, pl.smem, threads, launch ? nullptr : per_sm);
         if (e != cudaSuccess || !launch) return e;

@@ -153,12 +153,23 @@ int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, co
         const uint64_t tiles = (uint64_t)layers * d.num_blocks * d.num_kv_heads;
         const CUtensorMapDataType type = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         const CUtensorMapSwizzle sw = seg == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-        const uint64_t dims[3] = {(uint64_t)d.head_dim, (uint64_t)BS, tiles};
-        const uint64_t strides[2] = {(uint64_t)rowb, (uint64_t)rowb * BS};
-        const uint32_t box[3] = {(uint32_t)(seg / eb), (uint32_t)BS, 1u};
-        if (!encode_tiled_3d(&args.kmap, key_cache, type, dims, strides, box, sw) ||
-            !encode_tiled_3d(&args.vmap, value_cache, type, dims, strides, box, sw))
-            return PKV_ERR_CUDA;
+        bool ok;
+        if (rowb == 2 * seg) {
+            // two row segments: [segment][token][seg] in shared memory from one 4-D copy whose
+            // dimensions are (element in segment, token, segment, tile)
+            const uint64_t dims[4] = {(uint64_t)(seg / eb), (uint64_t)BS, 2u, tiles};
+            const uint64_t strides[3] = {(uint64_t)rowb, (uint64_t)seg, (uint64_t)rowb * BS};
+            const uint32_t box[4] = {(uint32_t)(seg / eb), (uint32_t)BS, 2u, 1u};
+            ok = encode_tiled(&args.kmap, key_cache, type, 4, dims, strides, box, sw) &&
+                 encode_tiled(&args.vmap, value_cache, type, 4, dims, strides, box, sw);
+        } else {
+            const uint64_t dims[3] = {(uint64_t)d.head_dim, (uint64_t)BS, tiles};
+            const uint64_t strides[2] = {(uint64_t)rowb, (uint64_t)rowb * BS};
+            const uint32_t box[3] = {(uint32_t)(seg / eb), (uint32_t)BS, 1u};
+            ok = encode_tiled_3d(&args.kmap, key_cache, type, dims, strides, box, sw) &&
+                 encode_tiled_3d(&args.vmap, value_cache, type, dims, strides, box, sw);
+        }
+        if (!ok) return PKV_ERR_CUDA;
     }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.q = static_cast<const uint16_t *>(q);

@@ -28,10 +28,16 @@ namespace pkv {
 // Free the pool's prefix cache, if any (its block references are not released).
 void destroy_prefix_cache(pkv_pool *pool);
 
-// A 3-D tiled tensor map (TMA descriptor) over `ptr`: dims innermost first, strides in bytes
-// of dims 1 and 2, box in elements.  false if the driver's encoder is unavailable or refuses.
-bool encode_tiled_3d(CUtensorMap *map, const void *ptr, CUtensorMapDataType type, const uint64_t (&dims)[3],
-                     const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle);
+// A tiled tensor map (TMA descriptor) of rank 3 or 4 over `ptr`: dims innermost first,
+// strides in bytes of dims 1 .. rank-1, box in elements.  false if the driver's encoder is
+// unavailable or refuses.
+bool encode_tiled(CUtensorMap *map, const void *ptr, CUtensorMapDataType type, int rank, const uint64_t *dims,
+                  const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle swizzle);
+inline bool encode_tiled_3d(CUtensorMap *map, const void *ptr, CUtensorMapDataType type, const uint64_t (&dims)[3],
+                            const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle)
+{
+    return encode_tiled(map, ptr, type, 3, dims, strides, box, swizzle);
+}
 
 // Which kernel (PKV_TEST_EXPIRE_*) the failure-path test hook currently targets.
 int test_expire();

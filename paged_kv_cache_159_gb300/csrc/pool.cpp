@@ -51,8 +51,8 @@ std::atomic<int> g_test_expire{PKV_TEST_EXPIRE_NONE};
 
 int test_expire() { return g_test_expire.load(std::memory_order_relaxed); }
 
-bool encode_tiled_3d(CUtensorMap *map, const void *ptr, CUtensorMapDataType type, const uint64_t (&dims)[3],
-                     const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle)
+bool encode_tiled(CUtensorMap *map, const void *ptr, CUtensorMapDataType type, int rank, const uint64_t *dims,
+                  const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle swizzle)
 {
     // the driver's encoder, looked up once through the runtime (no link against libcuda)
     static std::once_flag once;
@@ -64,10 +64,16 @@ bool encode_tiled_3d(CUtensorMap *map, const void *ptr, CUtensorMapDataType type
                 cudaSuccess && q == cudaDriverEntryPointSuccess)
             enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
     });
-    if (!enc) return false;
-    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]}, st[2] = {strides[0], strides[1]};
-    const cuuint32_t b[3] = {box[0], box[1], box[2]}, es[3] = {1, 1, 1};
-    return enc(map, type, 3, const_cast<void *>(ptr), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+    if (!enc || rank < 3 || rank > 4) return false;
+    cuuint64_t d[4], st[3];
+    cuuint32_t b[4], es[4];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    return enc(map, type, (cuuint32_t)rank, const_cast<void *>(ptr), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
