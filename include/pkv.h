@@ -248,7 +248,11 @@ typedef struct {
     int32_t variant;          /* 0 = auto (3); 1 = CUDA-core dot products; 2 = tensor-core mma with
                                  the heads as rows; 3 = tensor-core mma with the tokens as rows */
     int32_t warps_per_cta;    /* 0 = auto (4); 4 or 8 */
-    int32_t stages;           /* 0 = auto (16 KiB of tiles: 2 bf16 / 4 FP8 at D 128); 2..4 */
+    int32_t stages;           /* 0 = auto (16 KiB of tiles per warp: 2 bf16 / 4 FP8 at D 128); 2..4 */
+    int32_t heads_per_copy;   /* variant 3: KV heads loaded by one copy (the block's tiles of
+                                 consecutive heads are contiguous, so one copy brings several),
+                                 which halves or quarters the units and their merges; must divide
+                                 num_kv_heads and not exceed warps_per_cta; 0 = auto (1); 1, 2, 4 */
 } pkv_decode_opts;
 
 /* Device workspace bytes the decode needs for this shape and these opts (0 if the shape or

@@ -84,7 +84,8 @@ class device_step(ctypes.Structure):
 
 class decode_opts(ctypes.Structure):
     _fields_ = [("grid_ctas", ctypes.c_int32), ("variant", ctypes.c_int32),
-                ("warps_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32)]
+                ("warps_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("heads_per_copy", ctypes.c_int32)]
 
 
 _lib = None
@@ -428,7 +429,8 @@ def _opts(opts):
     if isinstance(opts, decode_opts):
         return opts
     return decode_opts(int(opts.get("grid_ctas", 0)), int(opts.get("variant", 0)),
-                       int(opts.get("warps_per_cta", 0)), int(opts.get("stages", 0)))
+                       int(opts.get("warps_per_cta", 0)), int(opts.get("stages", 0)),
+                       int(opts.get("heads_per_copy", 0)))
 
 
 def decode_workspace_bytes(pool: Pool, batch: int, num_q_heads: int, max_blocks: int,

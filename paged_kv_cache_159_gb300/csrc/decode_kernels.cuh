@@ -57,6 +57,7 @@
 #include <climits>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -98,11 +99,11 @@ __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / 
 struct Layout {
     int stage, q, ml, acc, prefix, lens, phys, bar, flag, total;
     int ml_slot, acc_slot;                                       // bytes of one merge slot
-    __host__ __device__ Layout(int NW, int NS, int tile, int D, int group, int B)
+    __host__ __device__ Layout(int NW, int NS, int tile, int D, int group, int B, int hp)
     {
         int o = 0;
-        stage = o;  o += NW * NS * 2 * tile;                      // K and V tiles per stage
-        q = o;      o += 2 * align_up(group * D * 2, 128);       // two segments' q rows
+        stage = o;  o += NW * NS * 2 * tile;                      // K and V tiles of every stage
+        q = o;      o += 2 * align_up(hp * group * D * 2, 128);  // two segments' q rows
         ml_slot = NW * 16 * 2 * 4;                               // per-warp (max, sum) rows
         ml = o;     o += 2 * ml_slot;
         acc_slot = align_up(NW * group * (D + ACC_PAD) * 4, 128);
@@ -644,10 +645,14 @@ struct TokCompute {
     __device__ __forceinline__ void block_impl(uint32_t kt, uint32_t vt, int ntok, int lane)
     {
         const int gid = lane >> 2, tid = lane & 3;
-        // ---- S^T = K Q^T: rows = tokens gid, gid + 8; columns = heads 8j + 2tid, +1
-        float s[NH][4];
+        // ---- S^T = K Q^T: rows = tokens gid, gid + 8; columns = heads 8j + 2tid, +1.  Two
+        //      independent accumulator chains (FP8: the high and low query terms; bf16: even
+        //      and odd k-steps) halve the dependent mma latency, then add.
+        float s[NH][4], s2[NH][4];
 #pragma unroll
-        for (int j = 0; j < NH; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+        for (int j = 0; j < NH; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s[j][c] = s2[j][c] = 0.f;
 #pragma unroll
         for (int i = 0; i < STEPS; ++i) {
             uint32_t a[4];
@@ -656,12 +661,16 @@ struct TokCompute {
             for (int j = 0; j < NH; ++j) {
                 if constexpr (FP8) {
                     dev::mma_e4m3_16832(s[j], a, qb[i][j][0], qb[i][j][1]);
-                    dev::mma_e4m3_16832(s[j], a, qb[i][j][2], qb[i][j][3]);
+                    dev::mma_e4m3_16832(s2[j], a, qb[i][j][2], qb[i][j][3]);
                 } else {
-                    dev::mma_bf16_16816(s[j], a, qb[i][j][0], qb[i][j][1]);
+                    dev::mma_bf16_16816((i & 1) ? s2[j] : s[j], a, qb[i][j][0], qb[i][j][1]);
                 }
             }
         }
+#pragma unroll
+        for (int j = 0; j < NH; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s[j][c] += s2[j][c];
         // ---- scale, mask, lazy running max (heads 8j + 2tid + r: values c = r and r + 2)
         bool need = false;
 #pragma unroll
@@ -791,29 +800,34 @@ struct TokCompute {
 // ------------------------------------------------------------------------------------
 // The decode kernel body: NW streaming warps and one epilogue warp.
 // ------------------------------------------------------------------------------------
-template <int D, bool FP8, int NW, int NS, class Compute>
+template <int D, bool FP8, int NW, int NS, int HP, class Compute>
 __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp, const CUtensorMap *kmap,
                                             const CUtensorMap *vmap)
 {
     constexpr int ELEM = FP8 ? 1 : 2;
-    constexpr int TILE = BS * D * ELEM;
+    constexpr int TILE = BS * D * ELEM;           // one (block, KV head) tile of K or V
     constexpr int NWARP = NW + 2;                 // NW consumers, the epilogue warp, the producer
     constexpr int NTHR = NWARP * 32;
-    constexpr int NSTAGE = NW * NS;               // CTA-wide ring; stage i % NSTAGE, consumer i % NW
-    static_assert(NSTAGE <= 32 && 32 % NW == 0, "one producer lane per stage, whole steps per 32 tasks");
+    // A task is one block of HP consecutive KV heads, loaded by one copy of HP tiles for K and
+    // one for V.  Consumer warp w takes head w % HP of the tasks of stream w / HP.
+    constexpr int NSTREAM = NW / HP;
+    constexpr int NSTAGE = NSTREAM * NS;          // CTA-wide ring; task i: stage i % NSTAGE, stream i % NSTREAM
+    constexpr int STAGE = 2 * HP * TILE;          // K tiles, then V tiles
+    static_assert(NW % HP == 0 && NSTAGE <= 32 && 32 % NSTREAM == 0, "ring and step shapes");
     // swizzled tiles: SEG-byte row segments, [segment][16 tokens][SEG] per tile
     constexpr int SEG = D * ELEM < 128 ? D * ELEM : 128;
     constexpr int NSEG = D * ELEM / SEG;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the stage ring starts 1024-byte aligned (the swizzle pattern repeats every 1024 bytes)
     uint8_t *smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
-    const Layout lay(NW, NS, TILE, D, p.group, p.B);
+    const Layout lay(NW, NS, TILE, D, p.group, p.B, HP);
     int32_t *prefix = reinterpret_cast<int32_t *>(smem + lay.prefix);
     int32_t *stage_tile = reinterpret_cast<int32_t *>(smem + lay.phys);
     int *flag = reinterpret_cast<int *>(smem + lay.flag);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int Hkv = p.Hkv, group = p.group;
+    const int HG = Hkv / HP;                      // head groups: units are (layer, sequence, head group)
 
     // ---- 0. warm L2 with this CTA's share of the block tables and queries (hints), and
     //         set up the barriers; both overlap the scan below.
@@ -841,7 +855,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
     }
     if (warp == NW + 1 && lane < NSTAGE) {
         dev::mbar_init(full0 + 8 * lane, 1);          // the producer's arrive (+ the copies' bytes)
-        dev::mbar_init(empty0 + 8 * lane, 1);         // the consumer warp's arrive
+        dev::mbar_init(empty0 + 8 * lane, HP);        // the stream's HP consumer warps
     }
     dev::fence_barrier_init();
 
@@ -862,7 +876,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                     for (int e = 0; e < p.Hq * D; ++e) p.out[((size_t)l * p.B + b) * p.Hq * D + e] = 0;
             }
             const int nb = ok ? (L + BS - 1) / BS : 0;    // an invalid length breaks uniformity
-            run += Hkv * nb;
+            run += HG * nb;
             lo = min(lo, nb);
             hi = max(hi, nb);
         }
@@ -894,7 +908,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                 glo = min(glo, wlo[w]);
                 ghi = max(ghi, whi[w]);
             }
-            const int units = p.layers * p.B * Hkv, grid = (int)gridDim.x;
+            const int units = p.layers * p.B * HG, grid = (int)gridDim.x;
             int pick = 0;
             if (glo == ghi && glo > 0 && units >= grid) {
                 for (int g0 = grid; pick == 0 && 5 * g0 >= 4 * grid; g0 -= 32) {
@@ -913,7 +927,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             prefix[b] = acc;
             const int L = lens[b];
             const bool ok = L >= 1 && L <= p.MB * BS;
-            acc += ok ? Hkv * ((L + BS - 1) / BS) : 0;
+            acc += ok ? HG * ((L + BS - 1) / BS) : 0;
         }
         if (tid == NTHR - 1) prefix[p.B] = base + incl;
         __syncthreads();
@@ -927,8 +941,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
     if (c >= G) return;                                    // uniform over the CTA
     const long long s = task_start(c, W, G), e = task_start(c + 1, W, G);
 
-    // Unit geometry of task r: layer, sequence, (layer, sequence) row lb = l * B + b, head,
-    // first task of the unit, blocks in it.  Layers are laid end to end, each with the same
+    // Unit geometry of task r: layer, sequence, (layer, sequence) row lb = l * B + b, head
+    // group h (KV heads h*HP .. h*HP + HP - 1), first task of the unit, blocks in it.  Layers are laid end to end, each with the same
     // task layout.
     struct Unit { int l, b, lb, h, L, nb; long long U0; };
     auto unit_of = [&](long long r) {
@@ -938,13 +952,14 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
         u.b = find_seq(prefix, p.B, rl);
         u.lb = u.l * p.B + u.b;
         const int tasks = prefix[u.b + 1] - prefix[u.b];
-        u.nb = tasks / Hkv;
+        u.nb = tasks / HG;
         u.h = (rl - prefix[u.b]) / u.nb;
         u.U0 = (long long)u.l * W1 + prefix[u.b] + (long long)u.h * u.nb;
         u.L = lens[u.b];
         return u;
     };
-    const int qbytes = group * D * 2;
+    const int R = HP * group;                              // query rows of a unit
+    const int qbytes = R * D * 2;
     const int qslot_bytes = align_up(qbytes, 128);
     float *ml_base = reinterpret_cast<float *>(smem + lay.ml);
     float *acc_base = reinterpret_cast<float *>(smem + lay.acc);
@@ -963,30 +978,32 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
         const float *acc_all = acc_base + (k & 1) * (lay.acc_slot / 4);
         const bool whole = seg_lo == u.U0 && seg_hi == U1;
         const int slot = k == 0 ? 0 : 1;
-        const size_t prow = ((size_t)c * 2 + slot) * group;        // partial rows of this CTA
-        // a warp per output row: the streaming warps' weights 2^(m_w - M) and the sum once per
-        // row, then lane l combines columns l*DPL .. l*DPL + DPL - 1 (vector accesses where the
-        // merge area keeps columns in order)
+        const size_t prow = ((size_t)c * 2 + slot) * R;            // partial rows of this CTA
+        // a warp per output row (head j = row / group of the unit, query row r): the weights
+        // 2^(m_w - M) of the stream warps that held head j, and the sum, once per row; then lane
+        // l combines columns l*DPL .. l*DPL + DPL - 1 (vector accesses where the merge area
+        // keeps columns in order)
         constexpr int DPL = D / 32;
-        for (int row = twarp; row < group; row += tnw) {
-            float mw[NW], M = -INFINITY;
+        for (int row = twarp; row < R; row += tnw) {
+            const int hj = row / group, r = row - hj * group;
+            float mw[NSTREAM], M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                mw[w] = ml_all[w * 32 + row * 2];
-                M = fmaxf(M, mw[w]);
+            for (int q = 0; q < NSTREAM; ++q) {
+                mw[q] = ml_all[(q * HP + hj) * 32 + r * 2];
+                M = fmaxf(M, mw[q]);
             }
-            float wt[NW], den = 0.f;
+            float wt[NSTREAM], den = 0.f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                wt[w] = (M == -INFINITY || mw[w] == -INFINITY) ? 0.f : dev::fast_exp2(mw[w] - M);
-                den += wt[w] * ml_all[w * 32 + row * 2 + 1];
+            for (int q = 0; q < NSTREAM; ++q) {
+                wt[q] = (M == -INFINITY || mw[q] == -INFINITY) ? 0.f : dev::fast_exp2(mw[q] - M);
+                den += wt[q] * ml_all[(q * HP + hj) * 32 + r * 2 + 1];
             }
             float num[DPL];
 #pragma unroll
             for (int x = 0; x < DPL; ++x) num[x] = 0.f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float *src = acc_all + (w * group + row) * rowstride;
+            for (int q = 0; q < NSTREAM; ++q) {
+                const float *src = acc_all + ((q * HP + hj) * group + r) * rowstride;
                 float a[DPL];
                 if constexpr (Compute::IDENTITY_SLOTS && DPL == 4) {
                     const float4 v = *reinterpret_cast<const float4 *>(src + lane * 4);
@@ -999,7 +1016,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                     for (int x = 0; x < DPL; ++x) a[x] = src[Compute::slot_of_d(lane * DPL + x)];
                 }
 #pragma unroll
-                for (int x = 0; x < DPL; ++x) num[x] += wt[w] * a[x];
+                for (int x = 0; x < DPL; ++x) num[x] += wt[q] * a[x];
             }
             if (whole) {
                 uint16_t ob[DPL];
@@ -1008,7 +1025,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                     const __nv_bfloat16 b = __float2bfloat16_rn(den > 0.f ? num[x] / den * p.out_scale : 0.f);
                     ob[x] = *reinterpret_cast<const uint16_t *>(&b);
                 }
-                uint16_t *dst = p.out + ((size_t)u.lb * p.Hq + (size_t)u.h * group + row) * D + lane * DPL;
+                uint16_t *dst = p.out + ((size_t)u.lb * p.Hq + (size_t)u.h * R + row) * D + lane * DPL;
                 if constexpr (DPL == 4)
                     *reinterpret_cast<uint2 *>(dst) = make_uint2(ob[0] | ((uint32_t)ob[1] << 16), ob[2] | ((uint32_t)ob[3] << 16));
                 else
@@ -1031,7 +1048,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
         // add of the team's first thread; the merge's loads follow that add through the next
         // team barrier.
         const int c0 = cta_of(u.U0, W, G), c1 = cta_of(U1 - 1, W, G);
-        int *counter = p.counters + (size_t)u.lb * Hkv + u.h;
+        int *counter = p.counters + (size_t)u.lb * HG + u.h;
         int last;
         if (team_cta) {
             __syncthreads();
@@ -1049,7 +1066,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
         // merge: a warp per output row, lanes own D/32 columns; an online merge over the
         // partials in CTA order, four partials' loads in flight at a time
         const bool c0_shared = task_start(c0, W, G) < u.U0;          // unit is c0's 2nd+ segment
-        for (int row = twarp; row < group; row += tnw) {
+        for (int row = twarp; row < R; row += tnw) {
             float Mr = -INFINITY, den = 0.f, num[DPL];
 #pragma unroll
             for (int x = 0; x < DPL; ++x) num[x] = 0.f;
@@ -1065,7 +1082,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                     for (int x = 0; x < DPL; ++x) oc[j][x] = 0.f;
                     if (cc <= c1) {
                         const int sl = (cc == c0 && c0_shared) ? 1 : 0;
-                        const size_t pr = ((size_t)cc * 2 + sl) * group + row;
+                        const size_t pr = ((size_t)cc * 2 + sl) * R + row;
                         ml[j] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pr * 2));
                         if constexpr (DPL == 4) {
                             const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + pr * D) + lane);
@@ -1088,7 +1105,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                     Mr = Mn;
                 }
             }
-            uint16_t *dst = p.out + ((size_t)u.lb * p.Hq + (size_t)u.h * group + row) * D + lane * DPL;
+            uint16_t *dst = p.out + ((size_t)u.lb * p.Hq + (size_t)u.h * R + row) * D + lane * DPL;
 #pragma unroll
             for (int x = 0; x < DPL; ++x) {
                 const __nv_bfloat16 ob = __float2bfloat16_rn(den > 0.f ? num[x] / den : 0.f);
@@ -1106,7 +1123,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             dev::fence_proxy_async_smem();
             dev::mbar_arrive_expect_tx(bar, qbytes);
             dev::bulk_g2s(dev::smem_u32(smem + lay.q + (k & 1) * qslot_bytes),
-                          p.q + ((size_t)u.lb * p.Hq + (size_t)u.h * group) * D, qbytes, bar);
+                          p.q + ((size_t)u.lb * p.Hq + (size_t)u.h * R) * D, qbytes, bar);
         };
         long long nxt = s;                                        // first two segments' q rows
         for (int k = 0; k < 2 && nxt < e; ++k) {
@@ -1138,26 +1155,41 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
     } else if (warp == NW + 1) {
         // ================= producer warp: every copy of the CTA's tasks ===================
         // Task i of the CTA (global task s + i) is loaded into stage i % NSTAGE and consumed
-        // by warp i % NW.  The tasks go NW at a time: lane j < NW issues task i0 + j, so one
-        // warp-instruction issues the copies of a whole step, once each of those stages has
-        // been released by its consumer.
+        // by the HP warps of stream i % NSTREAM.  The tasks go NSTREAM at a time: lane j issues
+        // task i0 + j, so one warp-instruction issues the copies of a whole step, once each of
+        // those stages has been released by its consumers.
         const int n_all = (int)(e - s);
-        // tile index ((layer * NB + phys) * Hkv + h, or -1 if the table entry is invalid) of
-        // task i, for a chunk of 32 tasks: lane x holds task chunk*32 + x; and, when
-        // appending, (layer * B + b) * 16 + the new token's offset if task i is its unit's
-        // last block
-        auto load_tiles = [&](int chunk, int &app) {
+        // index of the first tile ((layer * NB + phys) * Hkv + h*HP, or -1 if the table entry
+        // is invalid) of task i, for a chunk of 32 tasks: lane x holds task chunk*32 + x; and,
+        // when appending, (layer * B + b) * 16 + the new token's offset if task i is its
+        // unit's last block
+        // The lookup is split in two so that the table load is in flight for a whole chunk of
+        // 32 tasks before its value is needed: fetch() issues it, finish() checks the entry.
+        struct Pending { int id, tbase, app, valid; };
+        auto fetch = [&](int chunk) {
             const int i = chunk * 32 + lane;
-            int t = -1;
-            app = -1;
+            Pending q{-1, 0, -1, 0};
             if (i < n_all) {
                 const long long r = s + i;
                 const Unit u = unit_of(r);
                 const int blk = (int)(r - u.U0);
-                const int id = __ldg(p.block_tables + (size_t)u.b * p.MB + blk);
-                if (id >= 0 && id < p.num_blocks) t = (u.l * p.num_blocks + id) * Hkv + u.h;
-                else dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-                if (p.k_new && blk == u.nb - 1 && t >= 0) app = u.lb * BS + (u.L - 1) % BS;
+                q.id = __ldg(p.block_tables + (size_t)u.b * p.MB + blk);
+                q.tbase = u.l * p.num_blocks * Hkv + u.h * HP;
+                if (p.k_new && blk == u.nb - 1) q.app = u.lb * BS + (u.L - 1) % BS;
+                q.valid = 1;
+            }
+            return q;
+        };
+        auto finish = [&](const Pending &q, int &app) {
+            int t = -1;
+            app = -1;
+            if (q.valid) {
+                if (q.id >= 0 && q.id < p.num_blocks) {
+                    t = q.tbase + q.id * Hkv;
+                    app = q.app;
+                } else {
+                    dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+                }
             }
             return t;
         };
@@ -1200,20 +1232,21 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                 }
             }
         };
-        int acur, anext;
-        int tcur = load_tiles(0, acur), tnext = load_tiles(1, anext);
+        const Pending first = fetch(0);
+        Pending pend = fetch(1);                          // both chunks' loads in flight
+        int acur;
+        int tcur = finish(first, acur);
         bool ok = true;
         int issued = 0;                                   // tasks whose copies are issued
-        for (int i0 = 0; i0 < n_all; i0 += NW) {
+        for (int i0 = 0; i0 < n_all; i0 += NSTREAM) {
             if ((i0 & 31) == 0 && i0 > 0) {
-                tcur = tnext;
-                acur = anext;
-                tnext = load_tiles((i0 >> 5) + 1, anext);
+                tcur = finish(pend, acur);                // loaded a chunk ago
+                pend = fetch((i0 >> 5) + 1);
             }
-            const int i = i0 + lane % NW;
+            const int i = i0 + lane % NSTREAM;
             const int t = __shfl_sync(dev::FULL, tcur, i & 31);
             const int a = __shfl_sync(dev::FULL, acur, i & 31);
-            const bool mine = lane < NW && i < n_all;
+            const bool mine = lane < NSTREAM && i < n_all;
             const int st = i % NSTAGE;
             // the stage's previous task has been consumed
             const bool freed = !mine || i < NSTAGE ||
@@ -1229,7 +1262,9 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                 while (am) {
                     const int from = __ffs(am) - 1;
                     am &= am - 1;
-                    write_row(__shfl_sync(dev::FULL, a, from), __shfl_sync(dev::FULL, t, from));
+                    const int aa = __shfl_sync(dev::FULL, a, from), tt0 = __shfl_sync(dev::FULL, t, from);
+#pragma unroll
+                    for (int j = 0; j < HP; ++j) write_row(aa, tt0 + j);
                 }
                 dev::fence_proxy_async_global();
                 __syncwarp();
@@ -1238,29 +1273,30 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                 const uint32_t bar = full0 + 8 * st;
                 stage_tile[st] = t;
                 if (t >= 0) {
-                    dev::mbar_arrive_expect_tx(bar, 2 * TILE);
-                    const uint32_t dk = dev::smem_u32(smem + lay.stage + st * 2 * TILE);
+                    dev::mbar_arrive_expect_tx(bar, STAGE);
+                    const uint32_t dk = dev::smem_u32(smem + lay.stage + st * STAGE);
                     if constexpr (Compute::SWIZZLED) {
-                        // one tensor copy per tile, [segment][16 tokens][SEG bytes], swizzled
-                        // (two row segments: a 4-D map whose third dimension is the segment)
+                        // one tensor copy of HP tiles each, [head][segment][16 tokens][SEG
+                        // bytes], swizzled (two row segments: a 4-D map whose third
+                        // dimension is the segment)
                         if constexpr (NSEG == 2) {
                             tc::tma_load_4d(dk, kmap, 0, 0, 0, t, bar);
-                            tc::tma_load_4d(dk + TILE, vmap, 0, 0, 0, t, bar);
+                            tc::tma_load_4d(dk + HP * TILE, vmap, 0, 0, 0, t, bar);
                         } else {
                             static_assert(NSEG == 1, "row segments");
                             tc::tma_load_3d(dk, kmap, 0, 0, t, bar);
-                            tc::tma_load_3d(dk + TILE, vmap, 0, 0, t, bar);
+                            tc::tma_load_3d(dk + HP * TILE, vmap, 0, 0, t, bar);
                         }
                     } else {
                         const size_t off = (size_t)t * TILE;
-                        dev::bulk_g2s(dk, p.key_cache + off, TILE, bar);
-                        dev::bulk_g2s(dk + TILE, p.value_cache + off, TILE, bar);
+                        dev::bulk_g2s(dk, p.key_cache + off, HP * TILE, bar);
+                        dev::bulk_g2s(dk + HP * TILE, p.value_cache + off, HP * TILE, bar);
                     }
                 } else {
                     dev::mbar_arrive(bar);                // nothing to copy; the block is masked
                 }
             }
-            issued = min(n_all, i0 + NW);
+            issued = min(n_all, i0 + NSTREAM);
         }
         if (!ok && lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
         // no copy may land after the CTA has left: wait (bounded) for the last task issued
@@ -1270,9 +1306,10 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             (void)dev::mbar_wait_bounded(full0 + 8 * lane, (uint32_t)((last / NSTAGE) & 1));
         }
     } else {
-        // ================= consumer warps: tasks warp, warp + NW, ... of the CTA =========
+        // ================= consumer warps: head hj of tasks sw, sw + NSTREAM, ... ========
+        const int sw = warp / HP, hj = warp - sw * HP;
         const int n_all = (int)(e - s);
-        const int n_mine = max(0, (n_all - warp + NW - 1) / NW);
+        const int n_mine = max(0, (n_all - sw + NSTREAM - 1) / NSTREAM);
         bool aborted = false;
         if (p.test_stall)          // the failure-path test: a wait that runs out (copies in flight)
             aborted = !__all_sync(dev::FULL, dev::mbar_wait_bounded_ns(never, 0, dev::TEST_EXPIRE_NS));
@@ -1283,9 +1320,10 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             const long long seg_hi = min(e, u.U0 + (long long)u.nb);
             const bool qok = __all_sync(dev::FULL, dev::mbar_wait_bounded(qbar0 + 8 * (k & 1), (uint32_t)((k >> 1) & 1)));
             aborted |= !qok;
-            cmp.start(reinterpret_cast<const uint16_t *>(smem + lay.q + (k & 1) * qslot_bytes), group, lane);
-            while (!aborted && ic < n_mine && s + warp + (long long)NW * ic < seg_hi) {
-                const int i = warp + NW * ic;
+            cmp.start(reinterpret_cast<const uint16_t *>(smem + lay.q + (k & 1) * qslot_bytes) + hj * group * D,
+                      group, lane);
+            while (!aborted && ic < n_mine && s + sw + (long long)NSTREAM * ic < seg_hi) {
+                const int i = sw + NSTREAM * ic;
                 const int st = i % NSTAGE;
                 if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(full0 + 8 * st, (uint32_t)((i / NSTAGE) & 1)))) {
                     aborted = true;
@@ -1294,11 +1332,11 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                 const int blk = (int)(s + i - u.U0);
                 const int ntok = stage_tile[st] >= 0 ? min(BS, u.L - blk * BS) : 0;
                 if (ntok > 0) {
-                    const uint8_t *stage = smem + lay.stage + st * 2 * TILE;
-                    cmp.block(stage, stage + TILE, ntok, p.score_scale, lane);
+                    const uint8_t *stage = smem + lay.stage + st * STAGE + hj * TILE;
+                    cmp.block(stage, stage + HP * TILE, ntok, p.score_scale, lane);
                 }
                 __syncwarp();
-                if (lane == 0) dev::mbar_arrive(empty0 + 8 * st);   // the stage may be reloaded
+                if (lane == 0) dev::mbar_arrive(empty0 + 8 * st);   // this head of the stage is done
                 ++ic;
             }
             // hand this segment's state to the epilogue (merge slot k&1, free once the
@@ -1335,10 +1373,10 @@ template <int D, bool FP8, int NW, int NS, bool G16>
 __global__ void __launch_bounds__((NW + 2) * 32, 8 / NW) decode_mma_kernel(const DecodeParams p)
 {
     MmaCompute<D, FP8, G16> cmp;
-    decode_body<D, FP8, NW, NS>(p, cmp, nullptr, nullptr);
+    decode_body<D, FP8, NW, NS, 1>(p, cmp, nullptr, nullptr);
 }
 
-template <int D, bool FP8, int NW, int NS, int NH>
+template <int D, bool FP8, int NW, int NS, int HP, int NH>
 __global__ void __launch_bounds__((NW + 2) * 32, 8 / NW)
 decode_tok_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p)
@@ -1346,7 +1384,7 @@ decode_tok_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     TokCompute<D, FP8, NH> cmp;
     cmp.setup(threadIdx.x & 31);
     cmp.base_sc = p.score_scale;
-    decode_body<D, FP8, NW, NS>(p, cmp, &kmap, &vmap);
+    decode_body<D, FP8, NW, NS, HP>(p, cmp, &kmap, &vmap);
 }
 
 template <int D, bool FP8, int NW, int NS, int GP>
@@ -1354,7 +1392,7 @@ __global__ void __launch_bounds__((NW + 2) * 32) decode_simt_kernel(const Decode
 {
     SimtCompute<D, FP8, GP> cmp;
     cmp.sscale = p.score_scale;
-    decode_body<D, FP8, NW, NS>(p, cmp, nullptr, nullptr);
+    decode_body<D, FP8, NW, NS, 1>(p, cmp, nullptr, nullptr);
 }
 
 // ------------------------------------------------------------------------------------
@@ -1368,6 +1406,7 @@ struct LaunchArgs {
 
 struct Plan {
     int variant, nw, ns;
+    int hp;                   // KV heads per task (one copy of hp tiles); variant 3 only
     int grid;                 // CTAs (one wave)
     size_t smem;              // dynamic shared memory per CTA
     size_t ws_counters, ws_o, ws_ml, ws_bytes;
@@ -1437,8 +1476,15 @@ cudaError_t run_decode(const Plan &pl, int group, bool launch, int *per_sm, cuda
             kernel<<<pl.grid, threads, pl.smem, s>>>(a->kmap, a->vmap, a->p);
             return cudaGetLastError();
         };
-        if (group > 8) return go_tok(decode_tok_kernel<D, FP8, NW, NS, 2>);
-        return go_tok(decode_tok_kernel<D, FP8, NW, NS, 1>);
+        auto by_nh = [&](auto hpc) -> cudaError_t {
+            constexpr int H = decltype(hpc)::value;
+            if (group > 8) return go_tok(decode_tok_kernel<D, FP8, NW, NS, H, 2>);
+            return go_tok(decode_tok_kernel<D, FP8, NW, NS, H, 1>);
+        };
+        if (pl.hp == 1) return by_nh(std::integral_constant<int, 1>{});
+        if (pl.hp == 2) return by_nh(std::integral_constant<int, 2>{});
+        if (pl.hp == 4) return by_nh(std::integral_constant<int, 4>{});
+        return cudaErrorInvalidConfiguration;
     }
     if (pl.variant == 2) {
         if (group > 8) return go(decode_mma_kernel<D, FP8, NW, NS, true>);

@@ -62,11 +62,23 @@ int make_plan(const pkv_pool_desc &d, int B, int Hq, int MB, const pkv_decode_op
     if (pl.variant < 1 || pl.variant > 3) return PKV_ERR_INVALID;
     if (pl.variant == 1 && group > 8) return PKV_ERR_INVALID;
     pl.nw = o->warps_per_cta ? o->warps_per_cta : 4;
+    if (pl.variant == 3) {
+        if (o->heads_per_copy) {
+            pl.hp = o->heads_per_copy;
+            if ((pl.hp != 1 && pl.hp != 2 && pl.hp != 4) || d.num_kv_heads % pl.hp) return PKV_ERR_INVALID;
+        } else {
+            pl.hp = 1;
+        }
+        if (pl.hp > pl.nw) return PKV_ERR_INVALID;
+    } else {
+        if (o->heads_per_copy > 1) return PKV_ERR_INVALID;
+        pl.hp = 1;
+    }
     // default ring: 16 KiB of tiles per warp (2 bf16 or 4 FP8 stages at head_dim 128)
     pl.ns = o->stages ? o->stages : (elem_bytes(d) == 1 && pl.variant >= 2 ? 4 : 2);
     if (o->grid_ctas < 0) return PKV_ERR_INVALID;
     const int tile = BS * d.head_dim * elem_bytes(d);
-    pl.smem = Layout(pl.nw, pl.ns, tile, d.head_dim, group, B).total + 1024;   // + alignment slack
+    pl.smem = Layout(pl.nw, pl.ns, tile, d.head_dim, group, B, pl.hp).total + 1024;   // + alignment slack
     if (pl.smem > 227 * 1024) return PKV_ERR_INVALID;
     if (o->grid_ctas) {
         pl.grid = o->grid_ctas;
@@ -77,7 +89,7 @@ int make_plan(const pkv_pool_desc &d, int B, int Hq, int MB, const pkv_decode_op
         if (e != cudaSuccess || per_sm < 1) return PKV_ERR_CUDA;
         pl.grid = sm_count_cached() * per_sm;
     }
-    const size_t rows = (size_t)pl.grid * 2 * group;
+    const size_t rows = (size_t)pl.grid * 2 * group * pl.hp;
     pl.ws_counters = 0;
     pl.ws_o = ((size_t)d.num_layers * B * d.num_kv_heads * 4 + 255) / 256 * 256;   // counters
     pl.ws_ml = pl.ws_o + (rows * d.head_dim * 4 + 255) / 256 * 256;
@@ -159,13 +171,13 @@ int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, co
             // dimensions are (element in segment, token, segment, tile)
             const uint64_t dims[4] = {(uint64_t)(seg / eb), (uint64_t)BS, 2u, tiles};
             const uint64_t strides[3] = {(uint64_t)rowb, (uint64_t)seg, (uint64_t)rowb * BS};
-            const uint32_t box[4] = {(uint32_t)(seg / eb), (uint32_t)BS, 2u, 1u};
+            const uint32_t box[4] = {(uint32_t)(seg / eb), (uint32_t)BS, 2u, (uint32_t)pl.hp};
             ok = encode_tiled(&args.kmap, key_cache, type, 4, dims, strides, box, sw) &&
                  encode_tiled(&args.vmap, value_cache, type, 4, dims, strides, box, sw);
         } else {
             const uint64_t dims[3] = {(uint64_t)d.head_dim, (uint64_t)BS, tiles};
             const uint64_t strides[2] = {(uint64_t)rowb, (uint64_t)rowb * BS};
-            const uint32_t box[3] = {(uint32_t)(seg / eb), (uint32_t)BS, 1u};
+            const uint32_t box[3] = {(uint32_t)(seg / eb), (uint32_t)BS, (uint32_t)pl.hp};
             ok = encode_tiled_3d(&args.kmap, key_cache, type, dims, strides, box, sw) &&
                  encode_tiled_3d(&args.vmap, value_cache, type, dims, strides, box, sw);
         }

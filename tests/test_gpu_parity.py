@@ -124,6 +124,7 @@ SHAPES = [
     ((100, 513, 1000), 64, 8, 128, "bf16"),             # group 8
     ((29, 65, 700), 28, 4, 128, "bf16"),                # group 7
     ((47, 200), 48, 3, 128, "bf16"),                    # group 16
+    ((47, 300), 64, 4, 128, "bf16"),                    # group 16 over 4 KV heads (copies of 2, 4 heads)
     ((21, 50, 333), 28, 4, 128, "fp8"),
     ((9, 64, 257), 16, 2, 64, "fp8"),
     ((18, 33, 49, 600), 40, 4, 128, "fp8"),             # group 10 (16-row mma path)
@@ -151,6 +152,12 @@ def test_shapes_both_variants_and_grids(shape):
         # grid 1: every unit whole in one CTA; small grids: units cut across CTAs
         for grid in (0, 1, 2, 3, 7, 64, 1000):
             out = C.gpu_step(c, dict(variant=variant, grid_ctas=grid), append=False)
+            C.tol_check(C.bf16_to_f64(out), ref)
+    for hp in (1, 2, 4):                        # KV heads per copy (variant 3)
+        if Hkv % hp:
+            continue
+        for grid in (0, 1, 3, 64):
+            out = C.gpu_step(c, dict(variant=3, heads_per_copy=hp, grid_ctas=grid), append=False)
             C.tol_check(C.bf16_to_f64(out), ref)
     for variant in (3, 2):
         for nw, ns in ((4, 2), (4, 4), (8, 2), (8, 3)):
@@ -183,7 +190,7 @@ def test_physical_placement_does_not_change_a_single_bit():
         c.value_cache[pt] = vc0
         c.tables = np.where(t0 >= 0, perm[np.maximum(t0, 0)], -1).astype(np.int32)
         for opts in (None, dict(grid_ctas=3), dict(grid_ctas=11), dict(variant=1), dict(variant=2),
-                     dict(warps_per_cta=8)):
+                     dict(warps_per_cta=8), dict(heads_per_copy=1), dict(heads_per_copy=2)):
             by_opts.setdefault(repr(opts), []).append(C.gpu_step(c, opts, append=False))
     for o, lst in by_opts.items():
         assert np.isfinite(lst[0].float().cpu().numpy()).all()
