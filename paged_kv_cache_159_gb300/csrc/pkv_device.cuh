@@ -84,14 +84,33 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
-// Wait for phase `parity` of a barrier; false if the bound ran out first.
+// The same, suspending the thread until the phase completes or about `ns` nanoseconds have
+// passed (a hint), so that a waiting warp takes no issue slots from the others.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return done != 0;
+}
+
+// Suspend-time hint of a polling wait (ns).
+constexpr uint32_t WAIT_SUSPEND_NS = 1000u;
+
+// Wait for phase `parity` of a barrier; false if the bound ran out first.  After one quick
+// check the thread sleeps between polls (the hint), and the bound is checked every 16 polls.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (unsigned i = 0; i < WAIT_POLLS; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u && globaltimer() - t0 > WAIT_NS) return false;
+        if (mbar_try_wait_suspend(bar, parity, WAIT_SUSPEND_NS)) return true;
+        if ((i & 15u) == 15u && globaltimer() - t0 > WAIT_NS) return false;
     }
     return false;
 }
