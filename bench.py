@@ -248,7 +248,8 @@ def run_decode(args, name, world, rank, local_rank, K, W, full=True):
 
     cow_src = torch.from_numpy(cow_pairs[:, 0].copy()).to(dev)
     cow_dst = torch.from_numpy(cow_pairs[:, 1].copy()).to(dev)
-    launches_per_step = (1 if w.append and args.separate_append else 0) + 1 + (1 if len(cow_pairs) else 0)
+    launches_per_step = ((1 if w.append and args.separate_append else 0) + 1 + (1 if len(cow_pairs) else 0) +
+                         (1 if (decode_opts or {}).get("shared_prefix_blocks", 0) else 0))
     # algorithmic bytes (no credit for tail-slot over-read; shared prefix blocks counted
     # once per reader here, i.e. logical bytes); every layer reads its own K/V, queries and
     # outputs, and all layers share one read of the tables

@@ -253,6 +253,23 @@ typedef struct {
                                  consecutive heads are contiguous, so one copy brings several),
                                  which halves or quarters the units and their merges; must divide
                                  num_kv_heads and not exceed warps_per_cta; 0 = auto (1); 1, 2, 4 */
+    int32_t shared_prefix_blocks;  /* variant 3 with heads_per_copy 1: blocks at the start of the
+                                 tables that a shared-prefix pass may cover (0 = no pass).  Blocks
+                                 that many sequences' tables share are stored once [Paged]; the
+                                 pass reads each such block once per KV head for up to 64 query
+                                 rows instead of once per sequence.  The reference is the longest
+                                 sequence's table (the smallest index among equals); sequence b's
+                                 covered blocks are its leading table entries -- at most this many,
+                                 never the block that receives an appended token -- that equal the
+                                 reference's.  The result is the same attention for any tables
+                                 (only the order of the fp32 sums changes); the pass is one more
+                                 launch on the stream before the decode, and the workspace grows
+                                 by a partial state per query row. */
+    int32_t unit_cost;        /* the persistent grid's split of the (block, KV head) tasks charges
+                                 every unit (sequence, KV head group) this many tasks besides its
+                                 blocks -- the fixed cost of a unit in a CTA -- so that a CTA
+                                 given many short units gets fewer blocks; 0 = auto (16); -1 = none
+                                 (an even split of the blocks); at most 4096 */
 } pkv_decode_opts;
 
 /* Device workspace bytes the decode needs for this shape and these opts (0 if the shape or

@@ -85,7 +85,8 @@ class device_step(ctypes.Structure):
 class decode_opts(ctypes.Structure):
     _fields_ = [("grid_ctas", ctypes.c_int32), ("variant", ctypes.c_int32),
                 ("warps_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("heads_per_copy", ctypes.c_int32)]
+                ("heads_per_copy", ctypes.c_int32), ("shared_prefix_blocks", ctypes.c_int32),
+                ("unit_cost", ctypes.c_int32)]
 
 
 _lib = None
@@ -430,7 +431,8 @@ def _opts(opts):
         return opts
     return decode_opts(int(opts.get("grid_ctas", 0)), int(opts.get("variant", 0)),
                        int(opts.get("warps_per_cta", 0)), int(opts.get("stages", 0)),
-                       int(opts.get("heads_per_copy", 0)))
+                       int(opts.get("heads_per_copy", 0)), int(opts.get("shared_prefix_blocks", 0)),
+                       int(opts.get("unit_cost", 0)))
 
 
 def decode_workspace_bytes(pool: Pool, batch: int, num_q_heads: int, max_blocks: int,

@@ -3,3 +3,4 @@
 
 template cudaError_t pkv::decode::dispatch_nw_ns<128, true>(const pkv::decode::Plan &, int, bool, int *, cudaStream_t,
                                                         const pkv::decode::LaunchArgs *);
+template cudaError_t pkv::decode::run_prefix<128, true>(const pkv::decode::LaunchArgs *, cudaStream_t);

@@ -91,13 +91,20 @@ struct DecodeParams {
     float score_scale;            // scale * k_scale * log2(e)
     float out_scale;              // v_scale (1 for bf16 pools)
     float inv_k_scale, inv_v_scale;   // fl32(1/scale) for FP8 appends
+    // shared-prefix pass (0: none): the leading table entries of sequence b that the prefix
+    // pass covered, and its partial state per query row (layer, KV head, sequence, row)
+    int shared_prefix;            // blocks the prefix pass may cover
+    int unit_cost;                // tasks the split charges each unit besides its blocks
+    int32_t *prefix_n;            // [B] covered entries (written by the prefix pass)
+    float *pref_o;                // [layers, Hkv, B, group, D]   num * out_scale
+    float *pref_ml;               // [layers, Hkv, B, group, 2]   (max in log2 units, sum)
 };
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 // Shared-memory plan of one CTA (host and device agree on it).
 struct Layout {
-    int stage, q, ml, acc, prefix, lens, phys, bar, flag, total;
+    int stage, q, ml, acc, prefix, lens, pre, nzp, phys, bar, flag, total;
     int ml_slot, acc_slot;                                       // bytes of one merge slot
     __host__ __device__ Layout(int NW, int NS, int tile, int D, int group, int B, int hp)
     {
@@ -110,9 +117,11 @@ struct Layout {
         acc = o;    o += 2 * acc_slot;                           // per-warp accumulators
         prefix = o; o += align_up((B + 1) * 4, 16);              // task prefix over sequences
         lens = o;   o += align_up(B * 4, 16);                    // seq_lens
+        pre = o;    o += align_up(B * 4, 16);                    // blocks covered by the prefix pass
+        nzp = o;    o += align_up((B + 1) * 4, 16);              // sequences with tasks, prefix over b
         phys = o;   o += align_up(NW * NS * 4, 16);              // tile index per stage
-        bar = o;    o += (2 * NW * NS + 7) * 8;                  // stage full/empty, q, segment done/free, never
-        flag = o;   o += 128;                                    // scan scratch, merge flag
+        bar = o;    o += (2 * NW * NS + 9) * 8;                  // stage full/empty, q full/free, segment done/free, never
+        flag = o;   o += 256;                                    // scan scratch, merge flag
         total = o;
     }
 };
@@ -122,6 +131,15 @@ __device__ __forceinline__ float warp_allreduce_sum(float x)
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(dev::FULL, x, o);
     return x;
+}
+
+// a / b for a >= 0, b > 0: the 64-bit division is a long instruction sequence, so operands
+// that fit in 32 bits (every practical launch) take the 32-bit one.
+__device__ __forceinline__ long long div_nonneg(long long a, long long b)
+{
+    if ((((unsigned long long)a | (unsigned long long)b) >> 32) == 0)
+        return (long long)((uint32_t)a / (uint32_t)b);
+    return a / b;
 }
 
 // Largest b in [0, B) with prefix[b] <= r (prefix[B] > r assumed).
@@ -136,13 +154,79 @@ __device__ __forceinline__ int find_seq(const int32_t *prefix, int B, int r)
     return lo;
 }
 
-// CTA that owns task r under the even split of W tasks over G CTAs.
-__device__ __forceinline__ int cta_of(long long r, long long W, int G)
+// Unit geometry of task r: layer, sequence, (layer, sequence) row lb = l * B + b, head group h
+// (KV heads h*HP .. h*HP + HP - 1), first task of the unit, blocks in it, the sequence's
+// length and its blocks covered by the shared-prefix pass.  Layers are laid end to end, each
+// with the same task layout (prefix: tasks before sequence b within a layer, W1 per layer).
+struct Unit { int l, b, lb, h, L, nb, pre; long long U0; };
+
+// Not inlined: the paths that call it run once per unit or per 32 tasks, mostly at a launch's
+// start and end while the instruction cache is cold, so they share one copy of the code.
+static __device__ __noinline__ Unit unit_at(long long r, const int32_t *prefix, const int32_t *lens, const int32_t *pre,
+                                     int B, int layers, int W1, int HG)
 {
-    return (int)(((r + 1) * G - 1) / W);
+    Unit u;
+    u.l = 0;
+    if (layers > 1) u.l = (int)div_nonneg(r, W1);
+    const int rl = (int)(r - (long long)u.l * W1);
+    u.b = find_seq(prefix, B, rl);
+    u.lb = u.l * B + u.b;
+    const int tasks = prefix[u.b + 1] - prefix[u.b];
+    u.nb = tasks / HG;
+    u.h = (rl - prefix[u.b]) / u.nb;
+    u.U0 = (long long)u.l * W1 + prefix[u.b] + (long long)u.h * u.nb;
+    u.L = lens[u.b];
+    u.pre = pre[u.b];
+    return u;
 }
 
-__device__ __forceinline__ long long task_start(int c, long long W, int G) { return W * c / G; }
+// The split of the tasks over G CTAs.  Every unit (layer, sequence, head group with at least
+// one task) is charged OV tasks' worth of cost besides its blocks -- the fixed work of a unit
+// in a CTA: its q rows, its softmax state's hand-off and merge -- so that a CTA given many
+// short units gets fewer blocks.  Cost position of task r: P(r) = r + OV * (ordinal of r's
+// unit); the C cost units are cut evenly: task r goes to CTA floor(P(r) G / C).  Within a
+// unit P grows by 1 per task and G <= W <= C, so no CTA inside a unit's run is skipped; a CTA
+// whose whole share falls between two units gets no task.  With OV = 0 this is the even split
+// of the tasks.
+struct Split {
+    const int32_t *prefix;        // [B + 1] tasks before sequence b, within a layer
+    const int32_t *nzp;           // [B + 1] sequences with tasks before b
+    int B, HG, OV, G;
+    long long W1, W, C1, C;       // tasks, cost of a layer; tasks, cost of the launch
+
+    // CTA of task r of unit (l, b, h)
+    __device__ __forceinline__ int owner(long long r, int l, int b, int h) const
+    {
+        const long long P = r + (long long)OV * ((long long)l * nzp[B] * HG + (long long)nzp[b] * HG + h);
+        return (int)div_nonneg(P * G, C);
+    }
+    // first task whose cost position is at least T (W past the last)
+    __device__ __forceinline__ long long first_at(long long T) const
+    {
+        if (T >= C) return W;
+        const int l = (int)div_nonneg(T, C1);
+        const long long Tl = T - (long long)l * C1;
+        if (Tl >= C1 - OV) return (long long)(l + 1) * W1;        // the gap after the layer's last unit
+        // the first sequence whose last task lies at Tl or later
+        const long long ovh = (long long)OV * HG;
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid + 1] + ovh * nzp[mid + 1] - OV > Tl) hi = mid;
+            else lo = mid + 1;
+        }
+        const int b = lo;
+        const long long local = Tl - (prefix[b] + ovh * nzp[b]);
+        long long r = prefix[b];
+        if (local > 0) {
+            const int nb = (prefix[b + 1] - prefix[b]) / HG;
+            const long long hh = div_nonneg(local, nb + OV), k = local - hh * (nb + OV);
+            r += hh * nb + (k < nb ? k : nb);
+        }
+        return (long long)l * W1 + r;
+    }
+    __device__ __forceinline__ long long start(int c) const { return first_at(div_nonneg(c * C + G - 1, G)); }
+};
 
 // ------------------------------------------------------------------------------------
 // Tensor-core compute (variant 2).  Lane l: gid = l/4 (mma row group), tid = l%4.
@@ -527,6 +611,7 @@ struct TokCompute {
     uint32_t loff[NOFF];          // this lane's ldmatrix row address within a tile, per step % 4
     float base_sc = 0.f;          // scale * k_scale * log2(e)
     float sc = 0.f;               // the unit's score scale (FP8: with the queries' power of two)
+    int lim[NH][2];               // column mode: positions < lim of this lane's columns are valid
 
     // Output column of O^T row r (0..15) of m-tile mt.
     __device__ static int dcol(int mt, int r) { return FP8 ? 16 * mt + 2 * (r & 7) + (r >> 3) : 16 * mt + r; }
@@ -641,8 +726,10 @@ struct TokCompute {
     }
 
     // One 16-token block; PARTIAL: only tokens < ntok are valid (the rest masked by select).
-    template <bool PARTIAL>
-    __device__ __forceinline__ void block_impl(uint32_t kt, uint32_t vt, int ntok, int lane)
+    // COLS: besides, position pos0 + token is valid for column (query row) c only below
+    // lim[][] -- the rows of several sequences over a shared block.
+    template <bool PARTIAL, bool COLS = false>
+    __device__ __forceinline__ void block_impl(uint32_t kt, uint32_t vt, int ntok, int lane, int pos0 = 0)
     {
         const int gid = lane >> 2, tid = lane & 3;
         // ---- S^T = K Q^T: rows = tokens gid, gid + 8; columns = heads 8j + 2tid, +1.  Two
@@ -678,7 +765,10 @@ struct TokCompute {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const float x = s[j][c] * sc;
-                s[j][c] = (!PARTIAL || gid + 8 * (c >> 1) < ntok) ? x : -INFINITY;
+                const int tok = gid + 8 * (c >> 1);
+                bool valid = !PARTIAL || tok < ntok;
+                if constexpr (COLS) valid = valid && pos0 + tok < lim[j][c & 1];
+                s[j][c] = valid ? x : -INFINITY;
             }
             need |= fmaxf(s[j][0], s[j][2]) > m[j][0] + RESCALE_TAU;
             need |= fmaxf(s[j][1], s[j][3]) > m[j][1] + RESCALE_TAU;
@@ -838,6 +928,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
     const uint32_t done0 = dev::smem_u32(bars + 2 * NSTAGE + 2);  // merge slot j dumped
     const uint32_t free0 = dev::smem_u32(bars + 2 * NSTAGE + 4);  // merge slot j merged
     const uint32_t never = dev::smem_u32(bars + 2 * NSTAGE + 6);  // no thread ever arrives here
+    const uint32_t qfree0 = dev::smem_u32(bars + 2 * NSTAGE + 7); // q slot j read into registers
     if (tid == 0) {
         auto slice = [&](const void *base, size_t bytes) {
             const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + bytes * c / gridDim.x + 15) & ~uintptr_t(15);
@@ -850,8 +941,13 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             dev::mbar_init(qbar0 + 8 * j, 1);
             dev::mbar_init(done0 + 8 * j, NW * 32);
             dev::mbar_init(free0 + 8 * j, 1);
+            dev::mbar_init(qfree0 + 8 * j, NW);
         }
         dev::mbar_init(never, 1);
+    }
+    if (warp == NW + 1 && lane == 31 && kmap) {               // descriptors, ahead of the first copy
+        tc::prefetch_tensormap(kmap);
+        tc::prefetch_tensormap(vmap);
     }
     if (warp == NW + 1 && lane < NSTAGE) {
         dev::mbar_init(full0 + 8 * lane, 1);          // the producer's arrive (+ the copies' bytes)
@@ -862,37 +958,48 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
     // ---- 1. tasks per sequence (Hkv * ceil(L/16); 0 for an invalid length) and their
     //         exclusive prefix, by a block-wide scan; CTA 0 zeroes invalid sequences' rows.
     int32_t *lens = reinterpret_cast<int32_t *>(smem + lay.lens);
+    int32_t *pre = reinterpret_cast<int32_t *>(smem + lay.pre);
+    int32_t *nzp = reinterpret_cast<int32_t *>(smem + lay.nzp);
     {
         const int per = (p.B + NTHR - 1) / NTHR;
         const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
-        int run = 0, lo = INT_MAX, hi = -1;               // lo/hi: blocks per sequence
+        int run = 0, nz = 0, lo = INT_MAX, hi = -1;       // lo/hi: blocks per sequence
         for (int b = b0; b < b1; ++b) {
             const int L = __ldg(p.seq_lens + b);
             lens[b] = L;
+            pre[b] = p.shared_prefix ? p.prefix_n[b] : 0;
             const bool ok = L >= 1 && L <= p.MB * BS;
             if (!ok && c == 0) {
                 dev::flag_error(p.err, PKV_DEVERR_SEQ_LEN);
                 for (int l = 0; l < p.layers; ++l)
                     for (int e = 0; e < p.Hq * D; ++e) p.out[((size_t)l * p.B + b) * p.Hq * D + e] = 0;
             }
-            const int nb = ok ? (L + BS - 1) / BS : 0;    // an invalid length breaks uniformity
+            // blocks past those the prefix pass covered; an invalid length breaks uniformity
+            const int nb = ok ? (L + BS - 1) / BS - pre[b] : 0;
             run += HG * nb;
+            nz += nb > 0;
             lo = min(lo, nb);
             hi = max(hi, nb);
         }
-        int incl = run;                                   // inclusive scan over the warp
+        int incl = run, incz = nz;                        // inclusive scans over the warp
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(dev::FULL, incl, o);
-            if (lane >= o) incl += v;
+            const int v = __shfl_up_sync(dev::FULL, incl, o), vz = __shfl_up_sync(dev::FULL, incz, o);
+            if (lane >= o) {
+                incl += v;
+                incz += vz;
+            }
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
             lo = min(lo, __shfl_xor_sync(dev::FULL, lo, o));
             hi = max(hi, __shfl_xor_sync(dev::FULL, hi, o));
         }
-        int *wsum = flag, *wlo = flag + 10, *whi = flag + 20;  // NWARP <= 10 warps
-        if (lane == 31) wsum[warp] = incl;
+        int *wsum = flag, *wlo = flag + 10, *whi = flag + 20, *wnz = flag + 32;  // NWARP <= 10 warps
+        if (lane == 31) {
+            wsum[warp] = incl;
+            wnz[warp] = incz;
+        }
         if (lane == 0) {
             wlo[warp] = lo;
             whi[warp] = hi;
@@ -920,50 +1027,72 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             }
             if (lane == 0) flag[30] = pick;
         }
-        int base = 0;
-        for (int w = 0; w < warp; ++w) base += wsum[w];
-        int acc = base + incl - run;                       // exclusive prefix of b0
+        int base = 0, zbase = 0;
+        for (int w = 0; w < warp; ++w) {
+            base += wsum[w];
+            zbase += wnz[w];
+        }
+        int acc = base + incl - run;                       // exclusive prefixes of b0
+        int zacc = zbase + incz - nz;
         for (int b = b0; b < b1; ++b) {
             prefix[b] = acc;
+            nzp[b] = zacc;
             const int L = lens[b];
             const bool ok = L >= 1 && L <= p.MB * BS;
-            acc += ok ? HG * ((L + BS - 1) / BS) : 0;
+            const int nb = ok ? (L + BS - 1) / BS - pre[b] : 0;
+            acc += HG * nb;
+            zacc += nb > 0;
         }
-        if (tid == NTHR - 1) prefix[p.B] = base + incl;
+        if (tid == NTHR - 1) {
+            prefix[p.B] = base + incl;
+            nzp[p.B] = zbase + incz;
+        }
         __syncthreads();
     }
     const int W1 = prefix[p.B];                            // tasks of one layer
     const long long W = (long long)W1 * p.layers;
-    // With fewer tasks than CTAs only the first W CTAs work, one task each; every working
-    // CTA then owns at least one task, so the CTAs that cut a unit are exactly c0..c1.
+    // With fewer tasks than CTAs only the first W CTAs take part.  A CTA whose share holds no
+    // task leaves; the CTAs that cut a unit are exactly c0..c1 (no CTA inside a unit's run is
+    // skipped).
     int G = (int)(W < (long long)gridDim.x ? W : (long long)gridDim.x);
     if (flag[30] > 0) G = flag[30];                        // whole units per CTA (see above)
     if (c >= G) return;                                    // uniform over the CTA
-    const long long s = task_start(c, W, G), e = task_start(c + 1, W, G);
+    Split sp;
+    sp.prefix = prefix;
+    sp.nzp = nzp;
+    sp.B = p.B;
+    sp.HG = HG;
+    sp.OV = p.unit_cost;
+    sp.G = G;
+    sp.W1 = W1;
+    sp.W = W;
+    sp.C1 = W1 + (long long)p.unit_cost * nzp[p.B] * HG;
+    sp.C = sp.C1 * p.layers;
+    const long long s = sp.start(c), e = sp.start(c + 1);
+    if (s >= e) return;                                    // uniform over the CTA
 
-    // Unit geometry of task r: layer, sequence, (layer, sequence) row lb = l * B + b, head
-    // group h (KV heads h*HP .. h*HP + HP - 1), first task of the unit, blocks in it.  Layers are laid end to end, each with the same
-    // task layout.
-    struct Unit { int l, b, lb, h, L, nb; long long U0; };
-    auto unit_of = [&](long long r) {
-        Unit u;
-        u.l = p.layers > 1 ? (int)(r / W1) : 0;
-        const int rl = (int)(r - (long long)u.l * W1);
-        u.b = find_seq(prefix, p.B, rl);
-        u.lb = u.l * p.B + u.b;
-        const int tasks = prefix[u.b + 1] - prefix[u.b];
-        u.nb = tasks / HG;
-        u.h = (rl - prefix[u.b]) / u.nb;
-        u.U0 = (long long)u.l * W1 + prefix[u.b] + (long long)u.h * u.nb;
-        u.L = lens[u.b];
-        return u;
-    };
+    auto unit_of = [&](long long r) { return unit_at(r, prefix, lens, pre, p.B, p.layers, W1, HG); };
     const int R = HP * group;                              // query rows of a unit
     const int qbytes = R * D * 2;
     const int qslot_bytes = align_up(qbytes, 128);
     float *ml_base = reinterpret_cast<float *>(smem + lay.ml);
     float *acc_base = reinterpret_cast<float *>(smem + lay.acc);
     const int rowstride = D + ACC_PAD;
+
+    // The shared-prefix pass's state of query row `row` of unit u: returns (max, sum) and this
+    // lane's DPL columns of num * out_scale.
+    auto load_pref = [&](const Unit &u, int row, float (&pn)[D / 32]) {
+        const int kvh = u.h * HP + row / group, r = row - (row / group) * group;
+        const size_t pr = (((size_t)u.l * Hkv + kvh) * p.B + u.b) * group + r;
+        if constexpr (D == 128) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.pref_o + pr * D) + lane);
+            pn[0] = v.x; pn[1] = v.y; pn[2] = v.z; pn[3] = v.w;
+        } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.pref_o + pr * D) + lane);
+            pn[0] = v.x; pn[1] = v.y;
+        }
+        return __ldcg(reinterpret_cast<const float2 *>(p.pref_ml + pr * 2));
+    };
 
     // The epilogue of segment k: merge the NW streaming warps' states (merge slot k&1), then
     // write the output of a whole unit, or this CTA's partial followed by the hand-off (the
@@ -972,7 +1101,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
     // every warp handles together once streaming is over.
     auto seg_epilogue = [&](const Unit &u, long long seg_lo, long long seg_hi, int k, bool team_cta) {
         const long long U1 = u.U0 + u.nb;
-        const int tt = team_cta ? tid : lane, tn = team_cta ? NTHR : 32;
+        const int tt = team_cta ? tid : lane;
         const int twarp = team_cta ? warp : 0, tnw = team_cta ? NWARP : 1;
         const float *ml_all = ml_base + (k & 1) * (lay.ml_slot / 4);
         const float *acc_all = acc_base + (k & 1) * (lay.acc_slot / 4);
@@ -984,7 +1113,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
         // l combines columns l*DPL .. l*DPL + DPL - 1 (vector accesses where the merge area
         // keeps columns in order)
         constexpr int DPL = D / 32;
-        for (int row = twarp; row < R; row += tnw) {
+        // one output row: pm, pn are the shared-prefix pass's state of the row (whole units)
+        auto merge_row = [&](int row, const float2 pm, const float (&pn)[DPL]) {
             const int hj = row / group, r = row - hj * group;
             float mw[NSTREAM], M = -INFINITY;
 #pragma unroll
@@ -1019,10 +1149,24 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                 for (int x = 0; x < DPL; ++x) num[x] += wt[q] * a[x];
             }
             if (whole) {
+                float o[DPL];
+                if (u.pre > 0) {
+                    // and the shared-prefix pass's state of this row
+                    const float Mn = fmaxf(M, pm.x);
+                    const float a = M == -INFINITY ? 0.f : dev::fast_exp2(M - Mn), bw = dev::fast_exp2(pm.x - Mn);
+                    const float dd = den * a + pm.y * bw;
+                    const float inv = dd > 0.f ? 1.f / dd : 0.f;
+#pragma unroll
+                    for (int x = 0; x < DPL; ++x) o[x] = (num[x] * p.out_scale * a + pn[x] * bw) * inv;
+                } else {
+                    const float inv = den > 0.f ? p.out_scale / den : 0.f;
+#pragma unroll
+                    for (int x = 0; x < DPL; ++x) o[x] = num[x] * inv;
+                }
                 uint16_t ob[DPL];
 #pragma unroll
                 for (int x = 0; x < DPL; ++x) {
-                    const __nv_bfloat16 b = __float2bfloat16_rn(den > 0.f ? num[x] / den * p.out_scale : 0.f);
+                    const __nv_bfloat16 b = __float2bfloat16_rn(o[x]);
                     ob[x] = *reinterpret_cast<const uint16_t *>(&b);
                 }
                 uint16_t *dst = p.out + ((size_t)u.lb * p.Hq + (size_t)u.h * R + row) * D + lane * DPL;
@@ -1042,12 +1186,26 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                     p.part_ml[(prow + row) * 2 + 1] = den;
                 }
             }
+        };
+        constexpr int RB = 4;               // rows whose prefix-pass states are loaded together
+        for (int row0 = twarp; row0 < R; row0 += RB * tnw) {
+            float2 pmb[RB];
+            float pnb[RB][DPL];
+#pragma unroll
+            for (int j = 0; j < RB; ++j) {
+                pmb[j] = make_float2(-INFINITY, 0.f);
+                const int row = row0 + j * tnw;
+                if (whole && u.pre > 0 && row < R) pmb[j] = load_pref(u, row, pnb[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < RB; ++j)
+                if (row0 + j * tnw < R) merge_row(row0 + j * tnw, pmb[j], pnb[j]);
         }
         if (whole) return;
         // hand-off.  The team barrier orders every partial store before the release-acquire
         // add of the team's first thread; the merge's loads follow that add through the next
         // team barrier.
-        const int c0 = cta_of(u.U0, W, G), c1 = cta_of(U1 - 1, W, G);
+        const int c0 = sp.owner(u.U0, u.l, u.b, u.h), c1 = sp.owner(U1 - 1, u.l, u.b, u.h);
         int *counter = p.counters + (size_t)u.lb * HG + u.h;
         int last;
         if (team_cta) {
@@ -1063,53 +1221,91 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             __syncwarp();
         }
         if (!last) return;
-        // merge: a warp per output row, lanes own D/32 columns; an online merge over the
-        // partials in CTA order, four partials' loads in flight at a time
-        const bool c0_shared = task_start(c0, W, G) < u.U0;          // unit is c0's 2nd+ segment
-        for (int row = twarp; row < R; row += tnw) {
-            float Mr = -INFINITY, den = 0.f, num[DPL];
+        // merge: a warp per pair of output rows, lanes own D/32 columns; an online merge over
+        // the partials in CTA order, four CTAs' partials of both rows in flight at a time.
+        // The unit is c0's second or later segment when c0 also owns the task before it.
+        bool c0_shared = false;
+        if (u.U0 > 0) {
+            const Unit v = unit_of(u.U0 - 1);
+            c0_shared = sp.owner(u.U0 - 1, v.l, v.b, v.h) == c0;
+        }
+        constexpr int RM = 2;                     // rows merged together, their loads in flight at once
+        for (int row0 = twarp; row0 < R; row0 += RM * tnw) {
+            float pn[RM][DPL];                    // the shared-prefix pass's states, loaded first
+            float2 pm[RM];
+            float Mr[RM], den[RM], num[RM][DPL];
 #pragma unroll
-            for (int x = 0; x < DPL; ++x) num[x] = 0.f;
+            for (int j = 0; j < RM; ++j) {
+                const int row = row0 + j * tnw;
+                pm[j] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) pn[j][x] = num[j][x] = 0.f;
+                if (u.pre > 0 && row < R) pm[j] = load_pref(u, row, pn[j]);
+                Mr[j] = -INFINITY;
+                den[j] = 0.f;
+            }
             for (int cb = c0; cb <= c1; cb += 4) {
-                float2 ml[4];
-                float oc[4][DPL];
+                float2 ml[RM][4];
+                float oc[RM][4][DPL];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int cc = cb + j;
-                    ml[j].x = -INFINITY;
-                    ml[j].y = 0.f;
+                for (int j = 0; j < RM; ++j)
 #pragma unroll
-                    for (int x = 0; x < DPL; ++x) oc[j][x] = 0.f;
-                    if (cc <= c1) {
-                        const int sl = (cc == c0 && c0_shared) ? 1 : 0;
-                        const size_t pr = ((size_t)cc * 2 + sl) * R + row;
-                        ml[j] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pr * 2));
-                        if constexpr (DPL == 4) {
-                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + pr * D) + lane);
-                            oc[j][0] = v.x; oc[j][1] = v.y; oc[j][2] = v.z; oc[j][3] = v.w;
-                        } else {
-                            const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.part_o + pr * D) + lane);
-                            oc[j][0] = v.x; oc[j][1] = v.y;
+                    for (int q = 0; q < 4; ++q) {
+                        const int cc = cb + q, row = row0 + j * tnw;
+                        ml[j][q] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                        for (int x = 0; x < DPL; ++x) oc[j][q][x] = 0.f;
+                        if (cc <= c1 && row < R) {
+                            const int sl = (cc == c0 && c0_shared) ? 1 : 0;
+                            const size_t pr = ((size_t)cc * 2 + sl) * R + row;
+                            ml[j][q] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pr * 2));
+                            if constexpr (DPL == 4) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + pr * D) + lane);
+                                oc[j][q][0] = v.x; oc[j][q][1] = v.y; oc[j][q][2] = v.z; oc[j][q][3] = v.w;
+                            } else {
+                                const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.part_o + pr * D) + lane);
+                                oc[j][q][0] = v.x; oc[j][q][1] = v.y;
+                            }
                         }
                     }
-                }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (ml[j].x == -INFINITY) continue;
-                    const float Mn = fmaxf(Mr, ml[j].x);
-                    const float a = Mr == -INFINITY ? 0.f : dev::fast_exp2(Mr - Mn);
-                    const float bw = dev::fast_exp2(ml[j].x - Mn);
-                    den = den * a + ml[j].y * bw;
+                for (int j = 0; j < RM; ++j)
 #pragma unroll
-                    for (int x = 0; x < DPL; ++x) num[x] = num[x] * a + oc[j][x] * bw;
-                    Mr = Mn;
-                }
+                    for (int q = 0; q < 4; ++q) {
+                        if (ml[j][q].x == -INFINITY) continue;
+                        const float Mn = fmaxf(Mr[j], ml[j][q].x);
+                        const float a = Mr[j] == -INFINITY ? 0.f : dev::fast_exp2(Mr[j] - Mn);
+                        const float bw = dev::fast_exp2(ml[j][q].x - Mn);
+                        den[j] = den[j] * a + ml[j][q].y * bw;
+#pragma unroll
+                        for (int x = 0; x < DPL; ++x) num[j][x] = num[j][x] * a + oc[j][q][x] * bw;
+                        Mr[j] = Mn;
+                    }
             }
-            uint16_t *dst = p.out + ((size_t)u.lb * p.Hq + (size_t)u.h * R + row) * D + lane * DPL;
 #pragma unroll
-            for (int x = 0; x < DPL; ++x) {
-                const __nv_bfloat16 ob = __float2bfloat16_rn(den > 0.f ? num[x] / den : 0.f);
-                dst[x] = *reinterpret_cast<const uint16_t *>(&ob);
+            for (int j = 0; j < RM; ++j) {
+                const int row = row0 + j * tnw;
+                if (row >= R) break;
+                if (u.pre > 0) {                  // and the shared-prefix pass's state of this row
+                    const float Mn = fmaxf(Mr[j], pm[j].x);
+                    const float a = Mr[j] == -INFINITY ? 0.f : dev::fast_exp2(Mr[j] - Mn);
+                    const float bw = dev::fast_exp2(pm[j].x - Mn);
+                    den[j] = den[j] * a + pm[j].y * bw;
+#pragma unroll
+                    for (int x = 0; x < DPL; ++x) num[j][x] = num[j][x] * a + pn[j][x] * bw;
+                }
+                const float inv = den[j] > 0.f ? 1.f / den[j] : 0.f;
+                uint16_t ob[DPL];
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) {
+                    const __nv_bfloat16 bv = __float2bfloat16_rn(num[j][x] * inv);
+                    ob[x] = *reinterpret_cast<const uint16_t *>(&bv);
+                }
+                uint16_t *dst = p.out + ((size_t)u.lb * p.Hq + (size_t)u.h * R + row) * D + lane * DPL;
+                if constexpr (DPL == 4)
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(ob[0] | ((uint32_t)ob[1] << 16), ob[2] | ((uint32_t)ob[3] << 16));
+                else
+                    *reinterpret_cast<uint32_t *>(dst) = ob[0] | ((uint32_t)ob[1] << 16);
             }
         }
         if (tt == 0) atomicExch(counter, 0);
@@ -1136,16 +1332,20 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             const Unit u = unit_of(seg_lo);
             const long long seg_hi = min(e, u.U0 + (long long)u.nb);
             if (seg_hi == e) break;                               // the last segment: below
-            if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(done0 + 8 * (k & 1), (uint32_t)((k >> 1) & 1)))) {
+            // every streaming warp holds segment k's q rows in registers, so q slot k&1 takes
+            // segment k+2's rows at once (two segments ahead of their use)
+            if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(qfree0 + 8 * (k & 1), (uint32_t)((k >> 1) & 1)))) {
                 if (lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
                 break;
             }
-            // every streaming warp has dumped segment k, so none reads q slot k&1 again
-            // before segment k+2: stage that segment's q rows into it
             {
                 const Unit u1 = unit_of(seg_hi);
                 const long long h1 = min(e, u1.U0 + (long long)u1.nb);
                 if (h1 < e && lane == 0) issue_q(h1, k + 2);
+            }
+            if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(done0 + 8 * (k & 1), (uint32_t)((k >> 1) & 1)))) {
+                if (lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+                break;
             }
             seg_epilogue(u, seg_lo, seg_hi, k, false);
             __syncwarp();
@@ -1173,7 +1373,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                 const long long r = s + i;
                 const Unit u = unit_of(r);
                 const int blk = (int)(r - u.U0);
-                q.id = __ldg(p.block_tables + (size_t)u.b * p.MB + blk);
+                q.id = __ldg(p.block_tables + (size_t)u.b * p.MB + u.pre + blk);
                 q.tbase = u.l * p.num_blocks * Hkv + u.h * HP;
                 if (p.k_new && blk == u.nb - 1) q.app = u.lb * BS + (u.L - 1) % BS;
                 q.valid = 1;
@@ -1322,6 +1522,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             aborted |= !qok;
             cmp.start(reinterpret_cast<const uint16_t *>(smem + lay.q + (k & 1) * qslot_bytes) + hj * group * D,
                       group, lane);
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(qfree0 + 8 * (k & 1));   // q slot k&1 read
             while (!aborted && ic < n_mine && s + sw + (long long)NSTREAM * ic < seg_hi) {
                 const int i = sw + NSTREAM * ic;
                 const int st = i % NSTAGE;
@@ -1329,7 +1531,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
                     aborted = true;
                     break;
                 }
-                const int blk = (int)(s + i - u.U0);
+                const int blk = (int)(s + i - u.U0) + u.pre;
                 const int ntok = stage_tile[st] >= 0 ? min(BS, u.L - blk * BS) : 0;
                 if (ntok > 0) {
                     const uint8_t *stage = smem + lay.stage + st * STAGE + hj * TILE;
@@ -1387,6 +1589,254 @@ decode_tok_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     decode_body<D, FP8, NW, NS, HP>(p, cmp, &kmap, &vmap);
 }
 
+// ------------------------------------------------------------------------------------
+// Shared-prefix pass.  Blocks that many sequences' tables share (a common prompt prefix stored
+// once and referenced by every table, "KV Cache 与推理优化", PagedAttention section) are read
+// once per KV head and up to 64 query rows -- all g query heads of up to 64 / g sequences --
+// instead of once per sequence.  The reference table is the longest sequence's (the smallest
+// index among equals).  Sequence b's covered blocks are the leading entries of its table,
+// at most shared_prefix of them and never the block that receives an appended token, that
+// equal the reference's, so any tables give the same result.  Each covered query row's
+// partial softmax state (max, sum, unnormalised output) over its covered positions goes to
+// the workspace -- or, for a sequence covered entirely, its output -- and the decode kernel
+// streams the remaining blocks and merges the two.
+// ------------------------------------------------------------------------------------
+constexpr int PRE_ROWS = 64;        // query rows per CTA: 4 consumer warps of 16
+constexpr int PRE_NST = 4;          // K/V ring stages
+constexpr int PRE_THREADS = 160;    // 4 consumer warps and the producer warp
+
+template <int D, bool FP8>
+struct PrefixSmem {
+    static constexpr int TILE = BS * D * (FP8 ? 1 : 2);
+    static constexpr int RING = 0;                          // PRE_NST x (K, V), 1024-aligned
+    static constexpr int Q = RING + PRE_NST * 2 * TILE;     // [64 rows][D] bf16
+    static constexpr int SEQ = Q + PRE_ROWS * D * 2;        // [64 sequences] (length, covered blocks)
+    static constexpr int TOK = SEQ + PRE_ROWS * 2 * 4;      // [PRE_NST] the stage holds a loaded tile
+    static constexpr int RED = TOK + PRE_NST * 4;           // reduction scratch
+    static constexpr int BAR = align_up(RED + 16 * 8, 8);   // full and empty mbarriers
+    static constexpr int TOTAL = BAR + 2 * PRE_NST * 8;
+    static constexpr int ALLOC = TOTAL + 1024;              // + alignment slack
+};
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(PRE_THREADS)
+decode_prefix_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                     const DecodeParams p)
+{
+    using SM = PrefixSmem<D, FP8>;
+    constexpr int ELEM = FP8 ? 1 : 2;
+    constexpr int TILE = SM::TILE;
+    constexpr int SEG = D * ELEM < 128 ? D * ELEM : 128;
+    constexpr int NSEG = D * ELEM / SEG;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = p.group, spc = PRE_ROWS / g;              // sequences per CTA
+    const int b0 = blockIdx.x * spc, h = blockIdx.y, l = blockIdx.z;
+    int32_t *seq = reinterpret_cast<int32_t *>(smem + SM::SEQ);
+    int32_t *tok_ok = reinterpret_cast<int32_t *>(smem + SM::TOK);
+    unsigned long long *red = reinterpret_cast<unsigned long long *>(smem + SM::RED);
+    const uint32_t full0 = dev::smem_u32(smem + SM::BAR), empty0 = full0 + 8 * PRE_NST;
+    if (tid == 0)
+        for (int st = 0; st < PRE_NST; ++st) {
+            dev::mbar_init(full0 + 8 * st, 1);
+            dev::mbar_init(empty0 + 8 * st, 4);         // the four consumer warps
+        }
+    dev::fence_barrier_init();
+
+    // ---- 1. the reference: the longest valid sequence, the smallest index among equals
+    unsigned long long key = 0;                           // length << 32 | (~index)
+    for (int b = tid; b < p.B; b += PRE_THREADS) {
+        const int L = __ldg(p.seq_lens + b);
+        if (L >= 1 && L <= p.MB * BS) {
+            const unsigned long long k = ((unsigned long long)L << 32) | (0xffffffffu - (unsigned)b);
+            key = k > key ? k : key;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const unsigned long long k = __shfl_xor_sync(dev::FULL, key, o);
+        key = k > key ? k : key;
+    }
+    if (lane == 0) red[warp] = key;
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long k = 0;
+        for (int w = 0; w < PRE_THREADS / 32; ++w) k = red[w] > k ? red[w] : k;
+        red[8] = k;
+    }
+    __syncthreads();
+    const unsigned long long best = red[8];
+    const int Lref = (int)(best >> 32);
+    const int bref = best ? (int)(0xffffffffu - (unsigned)(best & 0xffffffffu)) : -1;
+    const int spe = bref >= 0 ? min(p.shared_prefix, (Lref + BS - 1) / BS) : 0;
+
+    // ---- 2. blocks covered for each of this CTA's sequences (written once, by the CTAs of
+    //         KV head 0 of layer 0, for the decode kernel)
+    for (int sq = warp; sq < spc; sq += PRE_THREADS / 32) {
+        const int b = b0 + sq;
+        int L = 0, cov = 0;
+        if (b < p.B) {
+            L = __ldg(p.seq_lens + b);
+            if (L >= 1 && L <= p.MB * BS && spe > 0) {
+                const int nb = (L + BS - 1) / BS;
+                int lim = min(spe, nb);
+                if (p.k_new) lim = min(lim, nb - 1);    // the block that receives the new token
+                cov = lim;
+                for (int j0 = 0; j0 < lim; j0 += 32) {
+                    const int j = j0 + lane;
+                    const bool diff = j < lim && __ldg(p.block_tables + (size_t)b * p.MB + j) !=
+                                                     __ldg(p.block_tables + (size_t)bref * p.MB + j);
+                    const unsigned m = __ballot_sync(dev::FULL, diff);
+                    if (m) {
+                        cov = j0 + __ffs(m) - 1;
+                        break;
+                    }
+                }
+            }
+            if (lane == 0 && h == 0 && l == 0) p.prefix_n[b] = cov;
+        }
+        if (lane == 0) {
+            seq[2 * sq] = L;
+            seq[2 * sq + 1] = cov;
+        }
+    }
+    __syncthreads();
+    int spc_blocks = 0;                                   // blocks this CTA streams
+    for (int sq = 0; sq < spc; ++sq) spc_blocks = max(spc_blocks, seq[2 * sq + 1]);
+    if (spc_blocks == 0) return;                          // uniform over the CTA
+
+    if (warp == 4) {
+        // ================= producer: the reference's first spc_blocks blocks of head h
+        if (lane == 0) {
+            bool ok = true;
+            int issued = 0;
+            for (int j = 0; j < spc_blocks; ++j) {
+                const int st = j % PRE_NST;
+                if (j >= PRE_NST && !dev::mbar_wait_bounded(empty0 + 8 * st, (uint32_t)(((j / PRE_NST) - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const int id = __ldg(p.block_tables + (size_t)bref * p.MB + j);
+                const uint32_t bar = full0 + 8 * st;
+                if (id >= 0 && id < p.num_blocks) {
+                    tok_ok[st] = 1;
+                    const int t = (l * p.num_blocks + id) * p.Hkv + h;
+                    const uint32_t dk = dev::smem_u32(smem + SM::RING + st * 2 * TILE);
+                    dev::mbar_arrive_expect_tx(bar, 2 * TILE);
+                    if constexpr (NSEG == 2) {
+                        tc::tma_load_4d(dk, &kmap, 0, 0, 0, t, bar);
+                        tc::tma_load_4d(dk + TILE, &vmap, 0, 0, 0, t, bar);
+                    } else {
+                        tc::tma_load_3d(dk, &kmap, 0, 0, t, bar);
+                        tc::tma_load_3d(dk + TILE, &vmap, 0, 0, t, bar);
+                    }
+                } else {
+                    dev::flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+                    tok_ok[st] = 0;
+                    dev::mbar_arrive(bar);
+                }
+                issued = j + 1;
+            }
+            if (!ok) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+            // no copy may land after the CTA has left
+            for (int st = 0; st < PRE_NST && st < issued; ++st) {
+                const int last = st + (issued - 1 - st) / PRE_NST * PRE_NST;
+                (void)dev::mbar_wait_bounded(full0 + 8 * st, (uint32_t)((last / PRE_NST) & 1));
+            }
+        }
+        return;
+    }
+
+    // ================= consumers: warp w holds query rows 16w .. 16w + 15 of the CTA
+    // (row x: sequence b0 + x / g, query head h*g + x % g); rows of sequences with nothing
+    // covered, and padding rows, are zero and written nowhere.
+    uint16_t *qs = reinterpret_cast<uint16_t *>(smem + SM::Q) + warp * 16 * D;
+    for (int e = lane; e < 16 * D / 8; e += 32) {
+        const int i = e / (D / 8), c8 = e % (D / 8);
+        const int x = 16 * warp + i, sq = x / g;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (sq < spc && seq[2 * sq + 1] > 0)
+            v = *reinterpret_cast<const uint4 *>(p.q + (((size_t)l * p.B + b0 + sq) * p.Hq + (size_t)h * g + x % g) * D + c8 * 8);
+        *reinterpret_cast<uint4 *>(qs + i * D + c8 * 8) = v;
+    }
+    __syncwarp();
+    TokCompute<D, FP8, 2> cmp;
+    cmp.setup(lane);
+    cmp.base_sc = p.score_scale;
+    cmp.start(qs, 16, lane);
+    const int gid = lane >> 2, tid4 = lane & 3;
+#pragma unroll
+    for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int x = 16 * warp + 8 * jn + 2 * tid4 + c, sq = x / g;
+            const bool row = sq < spc && seq[2 * sq + 1] > 0;
+            cmp.lim[jn][c] = row ? min(seq[2 * sq], BS * seq[2 * sq + 1]) : BS * spc_blocks;
+        }
+    bool ok = true;
+    for (int j = 0; j < spc_blocks; ++j) {
+        const int st = j % PRE_NST;
+        if (!__all_sync(dev::FULL, dev::mbar_wait_bounded(full0 + 8 * st, (uint32_t)((j / PRE_NST) & 1)))) {
+            ok = false;
+            break;
+        }
+        const int ntok = min(BS, Lref - BS * j);          // positions the reference holds
+        if (tok_ok[st]) {
+            const uint32_t kt = dev::smem_u32(smem + SM::RING + st * 2 * TILE);
+            if (ntok == BS) cmp.template block_impl<false, true>(kt, kt + TILE, BS, lane, BS * j);
+            else cmp.template block_impl<true, true>(kt, kt + TILE, ntok, lane, BS * j);
+        }
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(empty0 + 8 * st);
+    }
+    if (!ok) {
+        if (lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+        return;
+    }
+    // ---- each covered row: its partial state, or the output of a sequence covered entirely
+#pragma unroll
+    for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            float x = cmp.l[jn][r];
+            x += __shfl_xor_sync(dev::FULL, x, 4);
+            x += __shfl_xor_sync(dev::FULL, x, 8);
+            x += __shfl_xor_sync(dev::FULL, x, 16);
+            cmp.l[jn][r] = x;
+        }
+#pragma unroll
+    for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int x = 16 * warp + 8 * jn + 2 * tid4 + c, sq = x / g;
+            if (sq >= spc || seq[2 * sq + 1] == 0) continue;
+            const int b = b0 + sq, r = x % g, L = seq[2 * sq];
+            const bool entire = !p.k_new && seq[2 * sq + 1] == (L + BS - 1) / BS;
+            const size_t pr = (((size_t)l * p.Hkv + h) * p.B + b) * g + r;
+            const float lsum = cmp.l[jn][c];
+            if (entire) {
+                uint16_t *dst = p.out + (((size_t)l * p.B + b) * p.Hq + (size_t)h * g + r) * D;
+                const float inv = lsum > 0.f ? p.out_scale / lsum : 0.f;
+#pragma unroll
+                for (int mt = 0; mt < TokCompute<D, FP8, 2>::MT; ++mt) {
+                    const __nv_bfloat16 v0 = __float2bfloat16_rn(cmp.acc[mt][jn][c] * inv);
+                    const __nv_bfloat16 v1 = __float2bfloat16_rn(cmp.acc[mt][jn][c + 2] * inv);
+                    dst[TokCompute<D, FP8, 2>::dcol(mt, gid)] = *reinterpret_cast<const uint16_t *>(&v0);
+                    dst[TokCompute<D, FP8, 2>::dcol(mt, gid + 8)] = *reinterpret_cast<const uint16_t *>(&v1);
+                }
+            } else {
+                float *dst = p.pref_o + pr * D;
+#pragma unroll
+                for (int mt = 0; mt < TokCompute<D, FP8, 2>::MT; ++mt) {
+                    dst[TokCompute<D, FP8, 2>::dcol(mt, gid)] = cmp.acc[mt][jn][c] * p.out_scale;
+                    dst[TokCompute<D, FP8, 2>::dcol(mt, gid + 8)] = cmp.acc[mt][jn][c + 2] * p.out_scale;
+                }
+                if (gid == 0) *reinterpret_cast<float2 *>(p.pref_ml + pr * 2) = make_float2(cmp.m[jn][c], lsum);
+            }
+        }
+}
+
 template <int D, bool FP8, int NW, int NS, int GP>
 __global__ void __launch_bounds__((NW + 2) * 32) decode_simt_kernel(const DecodeParams p)
 {
@@ -1407,6 +1857,9 @@ struct LaunchArgs {
 struct Plan {
     int variant, nw, ns;
     int hp;                   // KV heads per task (one copy of hp tiles); variant 3 only
+    int sp;                   // blocks the shared-prefix pass may cover (0: no pass)
+    int uc;                   // tasks the split charges each unit besides its blocks
+    size_t ws_pre_n, ws_pre_o, ws_pre_ml;   // its areas of the workspace
     int grid;                 // CTAs (one wave)
     size_t smem;              // dynamic shared memory per CTA
     size_t ws_counters, ws_o, ws_ml, ws_bytes;
@@ -1497,6 +1950,21 @@ cudaError_t run_decode(const Plan &pl, int group, bool launch, int *per_sm, cuda
         return go(decode_simt_kernel<D, FP8, NW, NS, 8>);
     }
     return cudaErrorInvalidConfiguration;
+}
+
+// The shared-prefix pass: grid (sequence groups, KV heads, layers); launched before the decode
+// on the same stream.
+template <int D, bool FP8>
+cudaError_t run_prefix(const LaunchArgs *a, cudaStream_t s)
+{
+    auto kernel = decode_prefix_kernel<D, FP8>;
+    const size_t smem = PrefixSmem<D, FP8>::ALLOC;
+    cudaError_t e = prepare(kernel, smem, PRE_THREADS, nullptr);
+    if (e != cudaSuccess) return e;
+    const int spc = PRE_ROWS / a->p.group;
+    const dim3 grid((unsigned)((a->p.B + spc - 1) / spc), (unsigned)a->p.Hkv, (unsigned)a->p.layers);
+    kernel<<<grid, PRE_THREADS, smem, s>>>(a->kmap, a->vmap, a->p);
+    return cudaGetLastError();
 }
 
 // (warps per CTA, stages per warp) pairs that are compiled.  The CUDA-core variant exists

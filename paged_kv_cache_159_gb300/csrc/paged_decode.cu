@@ -14,6 +14,10 @@ extern template cudaError_t pkv::decode::dispatch_nw_ns<128, true>(const pkv::de
                                                                    cudaStream_t, const pkv::decode::LaunchArgs *);
 extern template cudaError_t pkv::decode::dispatch_nw_ns<64, false>(const pkv::decode::Plan &, int, bool, int *,
                                                                    cudaStream_t, const pkv::decode::LaunchArgs *);
+extern template cudaError_t pkv::decode::run_prefix<128, false>(const pkv::decode::LaunchArgs *, cudaStream_t);
+extern template cudaError_t pkv::decode::run_prefix<128, true>(const pkv::decode::LaunchArgs *, cudaStream_t);
+extern template cudaError_t pkv::decode::run_prefix<64, false>(const pkv::decode::LaunchArgs *, cudaStream_t);
+extern template cudaError_t pkv::decode::run_prefix<64, true>(const pkv::decode::LaunchArgs *, cudaStream_t);
 extern template cudaError_t pkv::decode::dispatch_nw_ns<64, true>(const pkv::decode::Plan &, int, bool, int *,
                                                                   cudaStream_t, const pkv::decode::LaunchArgs *);
 
@@ -76,7 +80,11 @@ int make_plan(const pkv_pool_desc &d, int B, int Hq, int MB, const pkv_decode_op
     }
     // default ring: 16 KiB of tiles per warp (2 bf16 or 4 FP8 stages at head_dim 128)
     pl.ns = o->stages ? o->stages : (elem_bytes(d) == 1 && pl.variant >= 2 ? 4 : 2);
-    if (o->grid_ctas < 0) return PKV_ERR_INVALID;
+    if (o->grid_ctas < 0 || o->shared_prefix_blocks < 0) return PKV_ERR_INVALID;
+    pl.sp = o->shared_prefix_blocks;
+    if (pl.sp > 0 && (pl.variant != 3 || pl.hp != 1)) return PKV_ERR_INVALID;
+    if (o->unit_cost < -1 || o->unit_cost > 4096) return PKV_ERR_INVALID;
+    pl.uc = o->unit_cost == 0 ? 16 : (o->unit_cost < 0 ? 0 : o->unit_cost);
     const int tile = BS * d.head_dim * elem_bytes(d);
     pl.smem = Layout(pl.nw, pl.ns, tile, d.head_dim, group, B, pl.hp).total + 1024;   // + alignment slack
     if (pl.smem > 227 * 1024) return PKV_ERR_INVALID;
@@ -94,6 +102,15 @@ int make_plan(const pkv_pool_desc &d, int B, int Hq, int MB, const pkv_decode_op
     pl.ws_o = ((size_t)d.num_layers * B * d.num_kv_heads * 4 + 255) / 256 * 256;   // counters
     pl.ws_ml = pl.ws_o + (rows * d.head_dim * 4 + 255) / 256 * 256;
     pl.ws_bytes = pl.ws_ml + (rows * 2 * 4 + 255) / 256 * 256;
+    pl.ws_pre_n = pl.ws_pre_o = pl.ws_pre_ml = 0;
+    if (pl.sp > 0) {
+        // the shared-prefix pass: blocks covered per sequence, a partial state per query row
+        const size_t prow = (size_t)d.num_layers * d.num_kv_heads * B * group;
+        pl.ws_pre_n = pl.ws_bytes;
+        pl.ws_pre_o = pl.ws_pre_n + ((size_t)B * 4 + 255) / 256 * 256;
+        pl.ws_pre_ml = pl.ws_pre_o + (prow * d.head_dim * 4 + 255) / 256 * 256;
+        pl.ws_bytes = pl.ws_pre_ml + (prow * 2 * 4 + 255) / 256 * 256;
+    }
     return PKV_OK;
 }
 
@@ -198,6 +215,11 @@ int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, co
     p.v_new = static_cast<const uint16_t *>(v_new);
     p.layers = layers;
     p.test_stall = test_expire() == PKV_TEST_EXPIRE_DECODE;
+    p.shared_prefix = pl.sp;
+    p.unit_cost = pl.uc;
+    p.prefix_n = pl.sp ? reinterpret_cast<int32_t *>(ws + pl.ws_pre_n) : nullptr;
+    p.pref_o = pl.sp ? reinterpret_cast<float *>(ws + pl.ws_pre_o) : nullptr;
+    p.pref_ml = pl.sp ? reinterpret_cast<float *>(ws + pl.ws_pre_ml) : nullptr;
     p.B = batch;
     p.Hq = num_q_heads;
     p.Hkv = d.num_kv_heads;
@@ -209,6 +231,13 @@ int decode_impl(pkv_pool *pool, int layers, const void *q, const void *k_new, co
     p.inv_k_scale = pool->inv_k_scale;
     p.inv_v_scale = pool->inv_v_scale;
 
+    if (pl.sp > 0) {
+        const bool fp8 = d.kv_dtype == PKV_KV_FP8E4M3;
+        const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+        const cudaError_t pe = d.head_dim == 128 ? (fp8 ? run_prefix<128, true>(&args, cs) : run_prefix<128, false>(&args, cs))
+                                                 : (fp8 ? run_prefix<64, true>(&args, cs) : run_prefix<64, false>(&args, cs));
+        if (pe != cudaSuccess) return PKV_ERR_CUDA;
+    }
     cudaError_t e = dispatch(d, pl, p.group, true, nullptr, static_cast<cudaStream_t>(stream), &args);
     if (e == cudaErrorInvalidConfiguration) return PKV_ERR_INVALID;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
