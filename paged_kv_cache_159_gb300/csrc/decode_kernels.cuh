@@ -1097,12 +1097,15 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
     // The epilogue of segment k: merge the NW streaming warps' states (merge slot k&1), then
     // write the output of a whole unit, or this CTA's partial followed by the hand-off (the
     // last CTA of the unit to arrive merges every partial, in CTA order, and resets the
-    // counter).  Run by the epilogue warp alone for all but the CTA's last segment, which
-    // every warp handles together once streaming is over.
+    // counter).  Run by the epilogue warp alone for all but the CTA's last segment, which the
+    // team -- the streaming warps and the producer -- handles once streaming is over, while
+    // the epilogue warp may still be finishing the segment before it (another merge slot).
+    constexpr int TEAM = (NW + 1) * 32;                    // team threads (named barrier 1)
     auto seg_epilogue = [&](const Unit &u, long long seg_lo, long long seg_hi, int k, bool team_cta) {
         const long long U1 = u.U0 + u.nb;
-        const int tt = team_cta ? tid : lane;
-        const int twarp = team_cta ? warp : 0, tnw = team_cta ? NWARP : 1;
+        const int tw = warp < NW ? warp : NW;              // team warp index (the producer is NW)
+        const int tt = team_cta ? tw * 32 + lane : lane;
+        const int twarp = team_cta ? tw : 0, tnw = team_cta ? NW + 1 : 1;
         const float *ml_all = ml_base + (k & 1) * (lay.ml_slot / 4);
         const float *acc_all = acc_base + (k & 1) * (lay.acc_slot / 4);
         const bool whole = seg_lo == u.U0 && seg_hi == U1;
@@ -1209,9 +1212,9 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
         int *counter = p.counters + (size_t)u.lb * HG + u.h;
         int last;
         if (team_cta) {
-            __syncthreads();
-            if (tid == 0) flag[31] = dev::atomic_add_acq_rel_gpu(counter, 1) == c1 - c0;
-            __syncthreads();
+            dev::named_bar_sync(1, TEAM);
+            if (tt == 0) flag[31] = dev::atomic_add_acq_rel_gpu(counter, 1) == c1 - c0;
+            dev::named_bar_sync(1, TEAM);
             last = flag[31];
         } else {
             __syncwarp();
@@ -1221,8 +1224,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
             __syncwarp();
         }
         if (!last) return;
-        // merge: a warp per pair of output rows, lanes own D/32 columns; an online merge over
-        // the partials in CTA order, four CTAs' partials of both rows in flight at a time.
+        // merge: a warp per RM output rows, lanes own D/32 columns; an online merge over the
+        // partials in CTA order, four CTAs' partials of the RM rows in flight at a time.
         // The unit is c0's second or later segment when c0 also owns the task before it.
         bool c0_shared = false;
         if (u.U0 > 0) {
@@ -1554,8 +1557,10 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, Compute &cmp,
         if (aborted && lane == 0) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
     }
 
-    // ---- 5. the CTA's last segment, by every warp together
-    __syncthreads();
+    // ---- 5. the CTA's last segment, by the team (every warp but the epilogue warp, which
+    //         leaves once it has handled its segments)
+    if (warp == NW) return;
+    dev::named_bar_sync(1, TEAM);
     {
         long long seg_lo = s;
         int k = 0;

@@ -248,6 +248,12 @@ __device__ __forceinline__ void fence_proxy_async_global()
 }
 
 // Hint: bring [ptr, ptr + bytes) into L2 (16-byte aligned start, size a multiple of 16).
+// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
