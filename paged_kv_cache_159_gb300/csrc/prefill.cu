@@ -593,11 +593,35 @@ extern "C" int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const
     // rows, the S -> softmax -> P.V chain filling and draining, and writing its output
     // (per-CTA end times fit 2.5 to 4 tiles per unit).
     auto cost = [&](int i) { return (int64_t)units[(size_t)i].nkv + 3; };
-    // longest processing time first: heaviest unit to the least-loaded CTA
+    // Longest processing time first: heaviest unit to the least-loaded CTA.  The units of one
+    // (sequence, KV head) read the same K/V; when the K/V of the batch is larger than about
+    // half the L2, they are handed out together (groups heaviest first, heaviest unit first
+    // within a group), so that they run side by side on different CTAs and all but the first
+    // read of each tile hit L2.  Otherwise every unit is ranked on its own.
+    int l2 = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    std::vector<int64_t> group_kv((size_t)batch * Hkv, 0);      // largest key count of a group's units
+    for (const Unit &u : units) {
+        int64_t &gk = group_kv[(size_t)u.b * Hkv + u.h];
+        gk = std::max<int64_t>(gk, (int64_t)u.kmax + 1);
+    }
+    int64_t kv_bytes = 0;
+    for (int64_t k : group_kv) kv_bytes += k * pool->desc.head_dim * 2 * 2;
+    const bool grouped = kv_bytes > (int64_t)l2 / 2;
     std::vector<int> order(units.size());
     for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
-    std::stable_sort(order.begin(), order.end(),
-                     [&](int a, int b) { return units[(size_t)a].nkv > units[(size_t)b].nkv; });
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        const Unit &x = units[(size_t)a], &y = units[(size_t)b];
+        if (grouped) {
+            const size_t gx = (size_t)x.b * Hkv + x.h, gy = (size_t)y.b * Hkv + y.h;
+            if (group_kv[gx] != group_kv[gy]) return group_kv[gx] > group_kv[gy];
+            if (gx != gy) return gx < gy;
+        }
+        return x.nkv > y.nkv;
+    });
+    std::vector<int> rank(units.size());                      // position in the hand-out order
+    for (size_t i = 0; i < order.size(); ++i) rank[(size_t)order[i]] = (int)i;
     using Load = std::pair<int64_t, int>;
     std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
     for (int c = 0; c < grid; ++c) heap.push({0, c});
@@ -616,7 +640,7 @@ extern "C" int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const
     // ends).  With many units per CTA the greedy pass is already fine-grained: swaps are
     // searched only up to 64 units per CTA, which bounds the host time.
     const bool swaps = units.size() <= (size_t)64 * grid;
-    for (int it = 0; it < 16 * grid; ++it) {
+    for (int it = 0; it < (grouped ? 0 : 16 * grid); ++it) {
         const int ca = (int)(std::max_element(load.begin(), load.end()) - load.begin());
         const int cb = (int)(std::min_element(load.begin(), load.end()) - load.begin());
         const int64_t la = load[(size_t)ca], lb = load[(size_t)cb];
@@ -645,8 +669,10 @@ extern "C" int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const
         }
         per[(size_t)cb].push_back(i);
     }
-    for (auto &v : per)                                         // heaviest first within a CTA
-        std::stable_sort(v.begin(), v.end(), [&](int a, int b) { return units[(size_t)a].nkv > units[(size_t)b].nkv; });
+    // within a CTA, the hand-out order: the units of one round run at about the same time on
+    // every CTA (a unit the refinement moved keeps its place in that order)
+    for (auto &v : per)
+        std::sort(v.begin(), v.end(), [&](int a, int b) { return rank[(size_t)a] < rank[(size_t)b]; });
     uint8_t *out = static_cast<uint8_t *>(plan_out);
     PlanHeader hdr{PLAN_MAGIC, (int32_t)units.size(), grid, g, tp, num_q_heads, Hkv, 0};
     std::memcpy(out, &hdr, sizeof(hdr));
