@@ -39,7 +39,7 @@ import workloads  # noqa: E402
 METRIC = "decode-attn KV GB/s (% of HBM peak) and query-tokens/s, Llama-3-8B layer shape"
 DEFAULT_WORKLOAD = "llama3_8b"
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SOURCES = ("decode_kernels.cuh", "paged_decode.cu", "pkv_device.cuh")
+DECODE_SOURCES = ("decode_kernels.cuh", "paged_decode.cu", "pkv_device.cuh", "tc_device.cuh")
 
 
 # ------------------------------------------------------------------ helpers
@@ -710,7 +710,7 @@ def _prefill_oracle_sample(w, nrows=48, threads=None):
     return flops / sec / 1e12, sec, nrows, threads
 
 
-PREFILL_SOURCES = ("prefill.cu", "tc_device.cuh")
+PREFILL_SOURCES = ("prefill.cu", "tc_device.cuh", "pkv_device.cuh")
 
 
 def _prefill_traffic(workload: str):
