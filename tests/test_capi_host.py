@@ -129,6 +129,16 @@ def test_decode_workspace_bytes_follows_the_plan(lib):
     assert pkv.decode_workspace_bytes(p, 4, 60, 2048, {"grid_ctas": 8}) == 0      # Hq % Hkv != 0
     assert pkv.decode_workspace_bytes(p, 4, 8 * 17, 2048, {"grid_ctas": 8}) == 0  # group > 16
     assert pkv.decode_workspace_bytes(p, 5000, 32, 8, {"grid_ctas": 8}) == 0      # batch > 4096
+    # the split's cost per unit: -1 (an even split of the blocks) .. 4096; it sizes nothing
+    for uc in (-1, 0, 1, 16, 4096):
+        assert pkv.decode_workspace_bytes(p, 64, 32, 128, {"grid_ctas": 300, "unit_cost": uc}) == ws
+    for uc in (-2, 4097):
+        assert pkv.decode_workspace_bytes(p, 64, 32, 128, {"grid_ctas": 300, "unit_cost": uc}) == 0
+    # the shared-prefix pass adds a partial state per query row (variant 3, one head per copy)
+    wsp = pkv.decode_workspace_bytes(p, 64, 32, 128, {"grid_ctas": 300, "shared_prefix_blocks": 8})
+    assert wsp >= ws + 64 * 4 + 64 * 32 * 128 * 4 + 64 * 32 * 2 * 4
+    assert pkv.decode_workspace_bytes(p, 64, 32, 128, {"grid_ctas": 300, "shared_prefix_blocks": 8,
+                                                       "variant": 2}) == 0
 
 
 def test_device_calls_need_an_attached_pool(lib):

@@ -159,6 +159,12 @@ def test_shapes_both_variants_and_grids(shape):
         for grid in (0, 1, 3, 64):
             out = C.gpu_step(c, dict(variant=3, heads_per_copy=hp, grid_ctas=grid), append=False)
             C.tol_check(C.bf16_to_f64(out), ref)
+    # the split's cost per unit: an even split of the blocks, small and large costs (with a
+    # cost far above the blocks, most CTAs get no task and leave)
+    for uc in (-1, 1, 16, 64, 4096):
+        for grid in (0, 3, 64):
+            out = C.gpu_step(c, dict(unit_cost=uc, grid_ctas=grid), append=False)
+            C.tol_check(C.bf16_to_f64(out), ref)
     for variant in (3, 2):
         for nw, ns in ((4, 2), (4, 4), (8, 2), (8, 3)):
             for grid in (0, 5):
@@ -190,7 +196,8 @@ def test_physical_placement_does_not_change_a_single_bit():
         c.value_cache[pt] = vc0
         c.tables = np.where(t0 >= 0, perm[np.maximum(t0, 0)], -1).astype(np.int32)
         for opts in (None, dict(grid_ctas=3), dict(grid_ctas=11), dict(variant=1), dict(variant=2),
-                     dict(warps_per_cta=8), dict(heads_per_copy=1), dict(heads_per_copy=2)):
+                     dict(warps_per_cta=8), dict(heads_per_copy=1), dict(heads_per_copy=2),
+                     dict(unit_cost=-1), dict(unit_cost=200, grid_ctas=9)):
             by_opts.setdefault(repr(opts), []).append(C.gpu_step(c, opts, append=False))
     for o, lst in by_opts.items():
         assert np.isfinite(lst[0].float().cpu().numpy()).all()
