@@ -458,11 +458,65 @@ def run_decode(args, name, world, rank, local_rank, K, W, full=True):
             raise RuntimeError("end-to-end decode output differs from the timed steps'")
         api = ("DecodeStepHost.run (one pkv_decode_step_host call)" if one_call
                else "one packed upload + library calls on views of it")
-        return e2e_step, h2d, d2h, api
+        serial = None
+        if one_call:
+            # The same steps as a serving loop pipelines them: step i+1's upload overlaps step
+            # i's decode and step i-1's download (three streams, two sets of device buffers);
+            # the decodes stay in order on one stream, and a set is refilled only once its
+            # decode and download are done.  Every step still uploads its inputs and downloads
+            # its output.  No L2 flush between pipelined steps: the inputs exceed L2.
+            serial = (e2e_step, api)
+            sets = []
+            for _ in range(2):
+                db = torch.empty_like(dbuf)
+                views, off = {}, 0
+                for (name, t), n in zip(parts, sizes):
+                    views[name] = db[off:off + n].view(t.dtype).view(t.shape)
+                    off += n
+                sets.append({"buf": db, "v": views, "out": torch.empty_like(out), "ws": torch.zeros_like(ws),
+                             "hout": torch.empty(out.shape, dtype=out.dtype).pin_memory()})
+            s_up, s_run, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
+            n = e2e_steps
+            ev_in, ev_run, ev_down = ([torch.cuda.Event() for _ in range(n)] for _ in range(3))
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for _ in range(2):                                  # the first pass warms up
+                torch.cuda.synchronize()
+                t0.record(s_up)
+                for i in range(n):
+                    st = sets[i & 1]
+                    if i >= 2:
+                        s_up.wait_event(ev_run[i - 2])          # the set's inputs are read
+                    with torch.cuda.stream(s_up):
+                        st["buf"].copy_(hbuf, non_blocking=True)
+                    ev_in[i].record(s_up)
+                    s_run.wait_event(ev_in[i])
+                    if i >= 2:
+                        s_run.wait_event(ev_down[i - 2])        # the set's output is downloaded
+                    v = st["v"]
+                    if w.append:
+                        pkv.decode_step(pool, v["q"], v["k_new"], v["v_new"], kc, vc, v["block_tables"],
+                                        v["seq_lens"], w.scale, st["out"], st["ws"], opts=decode_opts, stream=s_run)
+                    else:
+                        pkv.paged_attention_decode(pool, v["q"], kc, vc, v["block_tables"], v["seq_lens"], w.scale,
+                                                   st["out"], st["ws"], opts=decode_opts, stream=s_run)
+                    ev_run[i].record(s_run)
+                    s_down.wait_event(ev_run[i])
+                    with torch.cuda.stream(s_down):
+                        st["hout"].copy_(st["out"], non_blocking=True)
+                    ev_down[i].record(s_down)
+                t1.record(s_down)
+                t1.synchronize()
+            e2e_step = t0.elapsed_time(t1) * 1e-3 / n
+            for st in sets:
+                if not torch.equal(st["hout"].view(torch.int16), ref_out.view(torch.int16)):
+                    raise RuntimeError("pipelined end-to-end decode output differs from the timed steps'")
+            api = ("torch uploads and downloads + pkv.%s, pipelined over three streams and two buffer sets"
+                   % ("decode_step" if w.append else "paged_attention_decode"))
+        return e2e_step, h2d, d2h, api, serial
 
-    e2e_step = h2d = d2h = None
+    e2e_step = h2d = d2h = e2e_serial = None
     if full:
-        e2e_step, h2d, d2h, e2e_api = e2e_leg()
+        e2e_step, h2d, d2h, e2e_api, e2e_serial = e2e_leg()
 
     # ---- reduce over ranks (max time), aggregate bytes over ranks
     if world > 1:
@@ -531,7 +585,12 @@ def run_decode(args, name, world, rank, local_rank, K, W, full=True):
                      "peak_source": peak_src + " hbm_gbs", "same_run_copy_gbs": round(copy_gbs, 1) if copy_gbs else None},
         "e2e": {"value": round(world * kv_unique / e2e_step / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(e2e_step * 1e3, 4), "api": e2e_api},
+                "ms_per_step": round(e2e_step * 1e3, 4), "api": e2e_api,
+                **({"l2": "not flushed between pipelined steps (the inputs exceed L2)",
+                    "serial": {"value": round(world * kv_unique / e2e_serial[0] / 1e9, 1),
+                               "ms_per_step": round(e2e_serial[0] * 1e3, 4), "api": e2e_serial[1],
+                               "l2": "flushed before each step; its copies and decode in series"}}
+                   if e2e_serial else {})},
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 3),
