@@ -761,9 +761,21 @@ def _prefill_oracle_sample(w, nrows=48, threads=None):
     rows = pos - (L - P)
     q = workloads.bf16_bits(d.q)[rows]
     threads = threads or os.cpu_count() or 1
+    dt, ks, vs = oracle.BF16, 1.0, 1.0
+    if w.kv_dtype == "fp8":
+        # the E4M3 pool of the GPU run, for sequence 0's positions (encoded outside the timing)
+        ks = float(np.float32(max(d.key_cache.float().abs().max().item(), d.k_chunk.float().abs().max().item()))
+                   / np.float32(448.0))
+        vs = float(np.float32(max(d.value_cache.float().abs().max().item(), d.v_chunk.float().abs().max().item()))
+                   / np.float32(448.0))
+        sl = oracle.all_slots(t[:1], d.seq_lens[:1])
+        k8, v8 = np.zeros(kb.shape, np.uint8), np.zeros(vb.shape, np.uint8)
+        assert oracle.kv_append(kb[sl // 16, :, sl % 16, :], vb[sl // 16, :, sl % 16, :], sl, k8, v8, 16,
+                                oracle.FP8E4M3, ks, vs) == 0
+        kb, vb, dt = k8, v8, oracle.FP8E4M3
     t0 = time.perf_counter()
     st, _ = oracle.paged_decode(q, kb, vb, np.repeat(t[:1], nrows, 0), (pos + 1).astype(np.int32), w.scale,
-                                w.num_kv_heads, num_threads=threads)
+                                w.num_kv_heads, 16, dt, ks, vs, num_threads=threads)
     sec = time.perf_counter() - t0
     flops = 4 * w.num_q_heads * w.head_dim * int((pos + 1).sum())
     return flops / sec / 1e12, sec, nrows, threads
@@ -798,15 +810,36 @@ def run_prefill(args, name, world, rank, local_rank, K, W, full=True):
     d = workloads.draw_prefill(w, dev)
     Hq, Hkv, D = w.num_q_heads, w.num_kv_heads, w.head_dim
     T = int(d.cu_q[-1])
-    pool = pkv.Pool(d.num_blocks, Hkv, D, free_order=d.free_order)
+    fp8 = w.kv_dtype == "fp8"
+    kc, vc = d.key_cache, d.value_cache
+    if fp8:
+        # an E4M3 pool, per-tensor scales amax / 448 over the bf16 history and chunks
+        ks = float(np.float32(max(kc.float().abs().max().item(), d.k_chunk.float().abs().max().item()))
+                   / np.float32(448.0))
+        vs = float(np.float32(max(vc.float().abs().max().item(), d.v_chunk.float().abs().max().item()))
+                   / np.float32(448.0))
+        pool = pkv.Pool(d.num_blocks, Hkv, D, pkv.KV_FP8E4M3, ks, vs, d.free_order)
+    else:
+        pool = pkv.Pool(d.num_blocks, Hkv, D, free_order=d.free_order)
     pool.attach_device(local_rank)
     tables = pool.build_block_tables(d.seq_lens, d.max_blocks)
     slots = pkv.slot_mapping_chunks(tables, d.seq_lens, d.cu_q)
+    if fp8:
+        # the history (every position but the chunks') encoded into the pool by kv_append
+        hist = np.setdiff1d(pkv.slot_mapping_all(tables, d.seq_lens), slots)
+        hs = torch.from_numpy(hist).to(dev)
+        k8 = torch.zeros(kc.shape, dtype=torch.uint8, device=dev)
+        v8 = torch.zeros(vc.shape, dtype=torch.uint8, device=dev)
+        for i in range(0, len(hist), 1 << 16):
+            h = hs[i:i + (1 << 16)]
+            pkv.kv_append(pool, kc[h // 16, :, h % 16, :].contiguous(), vc[h // 16, :, h % 16, :].contiguous(),
+                          h, k8, v8)
+        torch.cuda.synchronize()
+        kc, vc = k8, v8
     plan_h, grid = pkv.prefill_plan(pool, d.cu_q, d.seq_lens, Hq, d.max_blocks)
     plan = torch.from_numpy(plan_h).to(dev)
     bt = torch.from_numpy(tables).to(dev)
     sm = torch.from_numpy(slots).to(dev)
-    kc, vc = d.key_cache, d.value_cache
     out = torch.empty_like(d.q)
     flops = _prefill_flops(d, Hq, D)
     stream = torch.cuda.Stream(device=dev)
@@ -933,7 +966,7 @@ def run_prefill(args, name, world, rank, local_rank, K, W, full=True):
     traffic = _prefill_traffic(w.name)
     # algorithmic bytes of one prefill launch: K and V of every position, q and out of every
     # packed row, the tables
-    alg_bytes = (int(d.seq_lens.astype(np.int64).sum()) * Hkv * D * 2 * 2 + T * Hq * D * 2 * 2
+    alg_bytes = (int(d.seq_lens.astype(np.int64).sum()) * Hkv * D * (1 if fp8 else 2) * 2 + T * Hq * D * 2 * 2
                  + w.batch * d.max_blocks * 4)
     if not full:
         return {"value": round(value, 2), "unit": "TFLOP/s", "step": "kv_append + paged_prefill (tcgen05)",
@@ -941,7 +974,7 @@ def run_prefill(args, name, world, rank, local_rank, K, W, full=True):
                 "frac": round(achieved / peak, 4), "achieved": round(achieved, 2), "flops_per_launch": flops,
                 "bytes_per_launch": alg_bytes, "traffic": traffic,
                 "traffic_ratio": round(traffic / alg_bytes, 3) if traffic else None,
-                "kernel": "prefill_kernel<%d>" % D, "steps": K, "warmup": W, "gpu_launches": 2 * K}
+                "kernel": "prefill_kernel<%d%s>" % (D, ", fp8" if fp8 else ""), "steps": K, "warmup": W, "gpu_launches": 2 * K}
     res = {
         "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(total / K * 1e3, 5), "higher_is_better": True,
@@ -960,7 +993,7 @@ def run_prefill(args, name, world, rank, local_rank, K, W, full=True):
         "query_tokens_per_s": round(world * T * K / total, 1),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "prefill_kernel<%d>" % D, "bytes_per_launch": alg_bytes,
+                     "kernel": "prefill_kernel<%d%s>" % (D, ", fp8" if fp8 else ""), "bytes_per_launch": alg_bytes,
                      "flops_per_launch": flops, "peak_source": peak_src},
         "e2e": {"value": round(world * flops / e2e_step / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -1001,7 +1034,8 @@ def run_prefill_reference(args):
 
 
 OTHER_CONFIGS = ("ragged", "llama3_70b_long", "qwen25_7b_prefix", "qwen25_7b_prefix_fp8",
-                 "qwen25_7b_prefix_cow", "llama3_8b_32l", "prefill_llama3_8b", "chunked_prefill_llama3_8b")
+                 "qwen25_7b_prefix_cow", "llama3_8b_32l", "prefill_llama3_8b", "chunked_prefill_llama3_8b",
+                 "chunked_prefill_llama3_8b_fp8")
 
 
 def run_other_configs(args, world, rank, local_rank):

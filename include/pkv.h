@@ -365,7 +365,9 @@ int pkv_prefill_plan(const pkv_pool *pool, const int32_t *cu_q, const int32_t *s
                      int32_t *grid_out);
 
 /* Run a plan: q bf16 [total_q, num_q_heads, D] (device); caches of one layer as in
- * pkv_pool_desc (bf16 pools only; FP8 pools are INVALID); block_tables int32
+ * pkv_pool_desc, bf16 or FP8 E4M3 ("KV Cache 与推理优化", KV 量化: the cache stored in FP8,
+ * the arithmetic in higher precision: E4M3 tiles are converted to bf16 on the chip, exactly,
+ * k_scale multiplies the scores and v_scale the output); block_tables int32
  * [batch, max_blocks] (device); plan the device copy of pkv_prefill_plan's output and grid
  * its grid; out bf16 [total_q, num_q_heads, D] (device, fp32 accumulation, rounded to
  * nearest even).  Rows are computed on the tcgen05 tensor cores: S = Q.K^T and O += P.V in

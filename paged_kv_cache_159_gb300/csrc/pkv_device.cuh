@@ -223,6 +223,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Two floats to f16x2 (lo in the low half), round to nearest even, saturating to the finite
+// range.
+__device__ __forceinline__ uint32_t pack_f16x2_satfinite(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
     __half2 v = __floats2half2_rn(lo, hi);

@@ -76,6 +76,7 @@ constexpr int BM = 128;            // query rows per q-tile (two q-tiles per uni
 constexpr int BN = 64;             // keys per KV tile (4 blocks)
 constexpr int BS = 16;             // tokens per block
 constexpr int NTHREADS = 480;      // warp 0 K loads, 1 and 12 S MMAs, 2-9 softmax + epilogue, 10 V, 11 Q loads, 13-14 P.V MMAs
+constexpr float FP8_Q_SCALE = 1.0f / 256.0f;   // E4M3 pools: q is taken to f16 as q * 2^-8
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float TAU = 8.0f;        // raise the running max only beyond 2^8
 constexpr uint32_t PLAN_MAGIC = 0x504b5650u;   // "PVKP"
@@ -96,33 +97,41 @@ struct Params {
     uint16_t *out;
     uint32_t *err;
     int MB, Hq, Hkv, group, TP, num_blocks, grid;
-    float score_scale;           // scale * log2(e)
+    float score_scale;           // scale * k_scale * log2(e)
+    float out_scale;             // v_scale (1 for bf16 pools)
     int test_stall;              // failure-path test: the Q loader waits on a barrier nothing completes
 };
 
-template <int D>
+template <int D, bool FP8>
 struct Smem {
     static constexpr int H = D / 64;                  // 64-column atom columns per row
-    static constexpr int NS = D == 128 ? 5 : 8;       // K/V ring depth (what the room allows)
+    // K/V ring depth (what the room allows).  An E4M3 pool streams its tiles through a deeper
+    // ring of staging tiles as stored (NSG) and keeps a shallower ring of converted ones.
+    static constexpr int NS = FP8 ? (D == 128 ? 3 : 4) : (D == 128 ? 5 : 8);
+    static constexpr int NSG = FP8 ? (D == 128 ? 4 : 8) : 0;
     static constexpr int Q = 0;                       // H x [256 rows][64]
     static constexpr int QHALF = BM * 2 * 128;        // bytes of one atom column of Q (256 rows)
     static constexpr int KHALF = BN * 128;            // bytes of one atom column of a K or V tile
-    static constexpr int KSTAGE = H * KHALF;          // one K (or V) tile
+    static constexpr int KSTAGE = H * KHALF;          // one K (or V) tile (bf16)
     static constexpr int K = Q + H * QHALF;           // NS K tiles
     static constexpr int V = K + NS * KSTAGE;         // NS V tiles
-    static constexpr int BAR = V + NS * KSTAGE;       // 13 + 4 NS mbarriers, then the TMEM slot
+    // E4M3 pools: NSG staging tiles each for K and V, [64 keys][D bytes] as loaded
+    static constexpr int STG = BN * D;
+    static constexpr int SK = V + NS * KSTAGE;
+    static constexpr int SV = SK + NSG * STG;
+    static constexpr int BAR = SV + NSG * STG;        // 14 + 4 NS + 2 NSG mbarriers, then the TMEM slot
     static constexpr int TOTAL = BAR + 512;
     static constexpr int ALLOC = TOTAL + 1024;        // alignment slack
-    static_assert(8 * (13 + 4 * NS) + 4 <= 512, "barrier area");
+    static_assert(8 * (14 + 4 * NS + 2 * NSG) + 4 <= 512, "barrier area");
     static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const Params p)
 {
-    using L = Smem<D>;
+    using L = Smem<D, FP8>;
     constexpr int H = L::H;
     constexpr int NSTAGE = L::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -148,7 +157,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     auto o_done = [&](int s) { return bars + 8 * (10 + 3 * NSTAGE + s); };
     auto o_free = [&](int w) { return bars + 8 * (10 + 4 * NSTAGE + w); };
     const uint32_t never = bars + 8 * (12 + 4 * NSTAGE);     // no thread ever arrives here
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (13 + 4 * NSTAGE));
+    // E4M3 pools: staging tile x of K (or V) landed; a unit's Q rows converted to f16
+    constexpr int NSG = L::NSG;
+    auto stg_full = [&](bool isk, int x) { return bars + 8 * (13 + 4 * NSTAGE + (isk ? 0 : NSG) + x); };
+    const uint32_t q_ready = bars + 8 * (13 + 4 * NSTAGE + 2 * NSG);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::BAR + 8 * (14 + 4 * NSTAGE + 2 * NSG));
 
     const PlanHeader *hdr = reinterpret_cast<const PlanHeader *>(p.plan);
     const int32_t *cta_off = reinterpret_cast<const int32_t *>(p.plan + sizeof(PlanHeader));
@@ -177,6 +190,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             dev::mbar_init(o_free(b), 4);             // the q-tile's four warps read O
         }
         dev::mbar_init(never, 1);
+        if constexpr (FP8) {
+            for (int x = 0; x < NSG; ++x) {
+                dev::mbar_init(stg_full(true, x), 1);
+                dev::mbar_init(stg_full(false, x), 1);
+            }
+            dev::mbar_init(q_ready, 1);
+        }
         dev::fence_barrier_init();
     }
     if (warp == 1) tc::tmem_alloc(dev::smem_u32(tmem_slot), TMEM_COLS);
@@ -209,7 +229,161 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         return id;
     };
 
-    if (warp == 11) {
+    // E4M3 pools: the loader warp of K (warp 0) or V (warp 10), every lane.  Lane 0 walks the
+    // CTA's tiles as the bf16 loaders do and copies each tile's blocks, as stored ([16 keys][D
+    // bytes] each), into staging tile t % NSG, up to NSG tiles ahead.  Every lane converts
+    // tile J into ring stage J % NS as f16, in the 128-byte-swizzled layout that a bulk-tensor
+    // copy would have written (16-byte chunk c of row r at chunk c ^ (r % 8)); E4M3 -> f16 is
+    // exact.  The products then run in f16 (q is taken to f16 as q * 2^-8 and P is written as
+    // f16), and the pool's scales are applied outside: k_scale (and 2^8) in the score scale,
+    // v_scale in the epilogue.
+    auto load_fp8 = [&](bool isk) {
+        const CUtensorMap *map = isk ? &kmap : &vmap;
+        const uint32_t stg_base = base + (isk ? L::SK : L::SV);
+        const uint8_t *stg = sm + (isk ? L::SK : L::SV);
+        uint8_t *ring = sm + (isk ? L::K : L::V);
+        int nt = 0;                                  // the CTA's tiles
+        for (int u = u0; u < u1; ++u) nt += units[u].nkv;
+        // lane 0: the issue cursor (tile ti of unit un, tile jc within it) and the entries of
+        // tile ti, fetched one issue ahead; the loaded-block masks of the tiles in flight, 4
+        // bits each (tile t at bits 4 (t % 8))
+        int ti = 0, uc = u0, jc = 0;
+        Unit un = units[u0];
+        int raw[BN / BS];
+        unsigned masks = 0;
+        if (lane == 0) fetch_ids(un, 0, raw);
+        auto issue_next = [&]() {
+            int ids[BN / BS], n = 0;
+            unsigned m = 0;
+#pragma unroll
+            for (int i = 0; i < BN / BS; ++i) {
+                ids[i] = resolve(raw[i]);
+                if (ids[i] >= 0) {
+                    m |= 1u << i;
+                    ++n;
+                }
+            }
+            const int x = ti % NSG;
+            const uint32_t bar = stg_full(isk, x);
+            dev::mbar_arrive_expect_tx(bar, (uint32_t)(n * BS * D));
+#pragma unroll
+            for (int i = 0; i < BN / BS; ++i)
+                if (ids[i] >= 0)
+                    tc::tma_load_3d(stg_base + x * L::STG + i * BS * D, map, 0, 0, ids[i] * p.Hkv + un.h, bar);
+            masks = (masks & ~(0xFu << (4 * (ti % 8)))) | (m << (4 * (ti % 8)));
+            ++ti;
+            if (++jc == un.nkv) {
+                jc = 0;
+                if (++uc < u1) un = units[uc];
+            }
+            if (ti < nt) fetch_ids(un, jc, raw);
+        };
+        if (lane == 0)
+            while (ti < nt && ti < NSG) issue_next();
+        // lane: 8-byte piece cc of the tile row (bytes 8cc .. 8cc + 7, the output's atom column
+        // cc / 8 and 16-byte chunk cc % 8), rows rr, rr + RP, ...: each pass reads RP whole
+        // contiguous rows
+        constexpr int LPR = D / 8, RP = 32 / LPR;    // lanes per row, rows per pass
+        const int cc = lane % LPR, rr = lane / LPR, hf = cc / 8, c = cc % 8;
+        bool ok = true;
+        int J = 0;                                   // tiles converted
+        for (; J < nt; ++J) {
+            // tile J: its staging copy, then its ring stage free (S of the stage's previous
+            // tile done for K, its P.V for V)
+            const int st = J % NSTAGE;
+            bool okw = dev::mbar_wait_bounded(stg_full(isk, J % NSG), (uint32_t)((J / NSG) & 1));
+            if (okw && J >= NSTAGE) {
+                const uint32_t par = ((J - NSTAGE) / NSTAGE) & 1;
+                okw = isk ? dev::mbar_wait_bounded(k_free(st), par) : dev::mbar_wait_bounded(o_done(st), par);
+            }
+            if (!__all_sync(dev::FULL, okw)) {
+                ok = false;
+                break;
+            }
+            const unsigned mask = (__shfl_sync(dev::FULL, masks, 0) >> (4 * (J % 8))) & 0xFu;
+            const uint8_t *src = stg + (J % NSG) * L::STG;
+            uint8_t *dst = ring + st * L::KSTAGE + hf * L::KHALF;
+            for (int i = 0; i < BN / BS; ++i) {
+                if (!((mask >> i) & 1u)) continue;           // not loaded (uniform over the warp)
+#pragma unroll
+                for (int p0 = 0; p0 < BS / RP; p0 += 4) {
+                    uint2 e[4];                              // four passes' loads in flight
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        e[k] = *reinterpret_cast<const uint2 *>(src + (i * BS + (p0 + k) * RP + rr) * D + cc * 8);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int r = i * BS + (p0 + k) * RP + rr;
+                        *reinterpret_cast<uint4 *>(dst + r * 128 + ((c ^ (r & 7)) << 4)) =
+                            make_uint4(dev::e4m3x2_to_f16x2((uint16_t)e[k].x),
+                                       dev::e4m3x2_to_f16x2((uint16_t)(e[k].x >> 16)),
+                                       dev::e4m3x2_to_f16x2((uint16_t)e[k].y),
+                                       dev::e4m3x2_to_f16x2((uint16_t)(e[k].y >> 16)));
+                    }
+                }
+            }
+            dev::fence_proxy_async_smem();           // converted rows -> tensor core (and the
+            __syncwarp();                            // staging tile's reads before its refill)
+            if (lane == 0) {
+                dev::mbar_arrive(isk ? k_full(st) : v_full(st));
+                if (ti < nt) issue_next();           // into the staging tile just converted
+            }
+        }
+        if (lane == 0) {
+            if (!ok) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+            // no copy may land after the CTA has left: wait (bounded) for the staging copies
+            // issued but not converted
+            for (int t = J; t < ti; ++t)
+                (void)dev::mbar_wait_bounded(stg_full(isk, t % NSG), (uint32_t)((t / NSG) & 1));
+        }
+    };
+
+    if (FP8 && warp == 11) {
+        // ============ Q for E4M3 pools: every lane.  Lane 0 loads a unit's rows as below; every
+        // lane then takes them to f16 in place, as q * 2^-8 (so that queries up to 2^24 in
+        // magnitude fit, saturating beyond), and lane 0 marks them ready for the S issuers.
+        int uq = 0;
+        bool pending = false;                        // lane 0: a Q copy not yet waited for
+        int okl = !p.test_stall || lane != 0 || dev::mbar_wait_bounded_ns(never, 0, dev::TEST_EXPIRE_NS);
+        bool ok = __shfl_sync(dev::FULL, okl, 0);
+        for (int u = u0; u < u1 && ok; ++u, ++uq) {
+            const Unit un = units[u];
+            okl = 1;
+            if (lane == 0) {
+                if (uq > 0 && !dev::mbar_wait_bounded(q_free, (uq - 1) & 1)) {
+                    okl = 0;
+                } else {
+                    dev::mbar_arrive_expect_tx(q_full, (uint32_t)(H * 64 * p.group * p.TP * 2));
+                    for (int hf = 0; hf < H; ++hf)
+                        tc::tma_load_3d(base + L::Q + hf * L::QHALF, &qmap, hf * 64, un.h * p.group, un.row0, q_full);
+                    pending = true;
+                }
+            }
+            if (!__shfl_sync(dev::FULL, okl, 0) ||
+                !__all_sync(dev::FULL, dev::mbar_wait_bounded(q_full, (uint32_t)(uq & 1)))) {
+                ok = false;
+                break;
+            }
+            pending = false;
+            uint4 *qs = reinterpret_cast<uint4 *>(sm + L::Q);
+            for (int e = lane; e < H * L::QHALF / 16; e += 32) {
+                uint4 v = qs[e];
+                uint32_t *w4 = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    w4[t] = dev::pack_f16x2_satfinite(dev::bf16_lo(w4[t]) * FP8_Q_SCALE, dev::bf16_hi(w4[t]) * FP8_Q_SCALE);
+                qs[e] = v;
+            }
+            dev::fence_proxy_async_smem();           // converted rows -> tensor core
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(q_ready);
+        }
+        if (lane == 0) {
+            if (!ok) dev::flag_error(p.err, PKV_DEVERR_TIMEOUT);
+            // no copy may land after the CTA has left
+            if (pending) (void)dev::mbar_wait_bounded(q_full, (uint32_t)((uq) & 1));
+        }
+    } else if (warp == 11) {
         // ============ TMA producer of Q: a unit's rows once the previous unit's last S is done
         if (lane == 0) {
             int uq = 0;
@@ -235,7 +409,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // is needed until P.V: a K stage is held for about a load plus S, not for a whole
         // tile's pipeline.  Q has a producer of its own so that the K ring runs ahead into
         // the next unit while the current one finishes.
-        if (lane == 0 && u0 < u1) {
+        if (FP8 && u0 < u1) {
+            load_fp8(warp == 0);
+        } else if (!FP8 && lane == 0 && u0 < u1) {
             const bool isk = warp == 0;
             const CUtensorMap *map = isk ? &kmap : &vmap;
             int J = 0, arms[NSTAGE] = {};
@@ -310,13 +486,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 return ok;
             };
             if (is_s) {
-                constexpr uint32_t IDS = tc::idesc_bf16(BM, BN, 0);   // S = Q K^T: M 128, N 64 keys
+                // S = Q K^T: M 128, N 64 keys (f16 operands for E4M3 pools)
+                constexpr uint32_t IDS = FP8 ? tc::idesc_f16(BM, BN, 0) : tc::idesc_bf16(BM, BN, 0);
                 // The operand descriptors are built once; each MMA adds its offset.
                 const uint64_t dQ = tc::desc_add(tc::smem_desc_sw128(base + L::Q, 16, 1024), (uint32_t)w * 16384);
                 const uint64_t dK = tc::smem_desc_sw128(base + L::K, 16, 1024);
                 for (int u = u0; u < u1 && ok; ++u, ++uq) {
                     const Unit un = units[u];
-                    if (!wait(q_full, uq & 1)) break;
+                    if (!wait(FP8 ? q_ready : q_full, uq & 1)) break;
                     for (int j = 0; j < un.nkv; ++j, ++J) {
                         const int st = J % NSTAGE;
                         if (!wait(k_full(st), (J / NSTAGE) & 1)) break;
@@ -337,7 +514,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     }
                 }
             } else {
-                constexpr uint32_t IDO = tc::idesc_bf16(BM, D, 1);    // O += P V: M 128, N D, V MN-major
+                // O += P V: M 128, N D, V MN-major
+                constexpr uint32_t IDO = FP8 ? tc::idesc_f16(BM, D, 1) : tc::idesc_bf16(BM, D, 1);
                 const uint64_t dV = tc::smem_desc_sw128(base + L::V, L::KHALF, 1024);
                 const uint32_t to = tO(w);
                 for (int u = u0; u < u1 && ok; ++u, ++uq) {
@@ -420,7 +598,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     const float2 t = tc::ffma2(make_float2(x[2 * e], x[2 * e + 1]), sc2, nm2);
                     const float2 pe = make_float2(dev::fast_exp2(t.x), dev::fast_exp2(t.y));
                     ps[e & 1] = tc::fadd2(ps[e & 1], pe);
-                    pw[e] = dev::pack_bf16x2(pe.x, pe.y);
+                    pw[e] = FP8 ? dev::pack_f16x2(pe.x, pe.y) : dev::pack_bf16x2(pe.x, pe.y);
                 }
                 const float2 ps2 = tc::fadd2(ps[0], ps[1]);
                 l = l * f + (ps2.x + ps2.y);
@@ -468,7 +646,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             ok = __all_sync(dev::FULL, dev::mbar_wait_bounded(o_done((J - 1) % NSTAGE), ((J - 1) / NSTAGE) & 1));
             if (!ok) break;
             tc::fence_after_sync();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? p.out_scale / l : 0.f;
             uint16_t *dst = p.out + ((size_t)(un.row0 + pl) * p.Hq + (size_t)un.h * p.group + hh) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
@@ -519,17 +697,18 @@ int sm_count()
     return n;
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch(const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm, const Params &p,
                    cudaStream_t s)
 {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::ALLOC);
+        attr = cudaFuncSetAttribute(prefill_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Smem<D, FP8>::ALLOC);
     });
     if (attr != cudaSuccess) return attr;
-    prefill_kernel<D><<<p.grid, NTHREADS, Smem<D>::ALLOC, s>>>(qm, km, vm, p);
+    prefill_kernel<D, FP8><<<p.grid, NTHREADS, Smem<D, FP8>::ALLOC, s>>>(qm, km, vm, p);
     return cudaGetLastError();
 }
 
@@ -697,7 +876,6 @@ extern "C" int pkv_paged_prefill(pkv_pool *pool, const void *q, const void *key_
     int st = pkv::check_attached(pool);
     if (st != PKV_OK) return st;
     const pkv_pool_desc &d = pool->desc;
-    if (d.kv_dtype != PKV_KV_BF16) return PKV_ERR_INVALID;       // bf16 pools only
     if (batch < 1 || num_q_heads < 1 || max_blocks < 1 || total_q < 0 || grid < 1 || !std::isfinite(scale))
         return PKV_ERR_INVALID;
     if (total_q == 0) return PKV_OK;
@@ -711,12 +889,24 @@ extern "C" int pkv_paged_prefill(pkv_pool *pool, const void *q, const void *key_
     if (g > 16) return PKV_ERR_INVALID;
     const int tp = tile_positions(g);
     const int D = d.head_dim;
+    const bool fp8 = d.kv_dtype == PKV_KV_FP8E4M3;
     CUtensorMap qm, km, vm;
     const uint64_t rows = (uint64_t)d.num_blocks * d.num_kv_heads;
-    if (!encode_3d(&qm, q, D, num_q_heads, total_q, (uint64_t)D * 2, (uint64_t)num_q_heads * D * 2, 64, g, tp) ||
-        !encode_3d(&km, key_cache, D, BS, rows, (uint64_t)D * 2, (uint64_t)BS * D * 2, 64, BS, 1) ||
-        !encode_3d(&vm, value_cache, D, BS, rows, (uint64_t)D * 2, (uint64_t)BS * D * 2, 64, BS, 1))
+    if (!encode_3d(&qm, q, D, num_q_heads, total_q, (uint64_t)D * 2, (uint64_t)num_q_heads * D * 2, 64, g, tp))
         return PKV_ERR_CUDA;
+    if (fp8) {
+        // E4M3 blocks as stored: [16 keys][D bytes] each, copied whole into the staging tiles
+        const uint64_t dims[3] = {(uint64_t)D, BS, rows}, strides[2] = {(uint64_t)D, (uint64_t)BS * D};
+        const uint32_t box[3] = {(uint32_t)D, BS, 1};
+        if (!pkv::encode_tiled_3d(&km, key_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !pkv::encode_tiled_3d(&vm, value_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+            return PKV_ERR_CUDA;
+    } else if (!encode_3d(&km, key_cache, D, BS, rows, (uint64_t)D * 2, (uint64_t)BS * D * 2, 64, BS, 1) ||
+               !encode_3d(&vm, value_cache, D, BS, rows, (uint64_t)D * 2, (uint64_t)BS * D * 2, 64, BS, 1)) {
+        return PKV_ERR_CUDA;
+    }
     Params p;
     p.tables = block_tables;
     p.plan = static_cast<const uint8_t *>(plan);
@@ -729,9 +919,12 @@ extern "C" int pkv_paged_prefill(pkv_pool *pool, const void *q, const void *key_
     p.TP = tp;
     p.num_blocks = d.num_blocks;
     p.grid = grid;
-    p.score_scale = scale * LOG2E;
+    // (E4M3 pools: q enters the products as q * 2^-8)
+    p.score_scale = scale * d.k_scale * LOG2E * (fp8 ? 1.0f / FP8_Q_SCALE : 1.0f);
+    p.out_scale = d.v_scale;
     p.test_stall = pkv::test_expire() == PKV_TEST_EXPIRE_PREFILL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = D == 128 ? launch<128>(qm, km, vm, p, s) : launch<64>(qm, km, vm, p, s);
+    const cudaError_t e = D == 128 ? (fp8 ? launch<128, true>(qm, km, vm, p, s) : launch<128, false>(qm, km, vm, p, s))
+                                   : (fp8 ? launch<64, true>(qm, km, vm, p, s) : launch<64, false>(qm, km, vm, p, s));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -40,6 +40,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn)
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with f16 A and B (format fields 0).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int b_mn)
+{
+    return (1u << 4) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] . B[smem]^T, issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate)

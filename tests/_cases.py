@@ -304,9 +304,16 @@ class PrefillCase:
     value_cache: torch.Tensor
     key_host: np.ndarray
     value_host: np.ndarray
+    kv_dtype: int = 0            # pkv.KV_BF16, or pkv.KV_FP8E4M3
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    @property
+    def fp8(self) -> bool:
+        return self.kv_dtype == pkv.KV_FP8E4M3
 
 
-def build_prefill(name: str, device="cuda", overrides=None) -> PrefillCase:
+def build_prefill(name: str, device="cuda", overrides=None, fp8=False) -> PrefillCase:
     w = workloads.PREFILL_WORKLOADS[name]
     if overrides:
         w = dataclasses.replace(w, **overrides)
@@ -326,9 +333,33 @@ def build_prefill(name: str, device="cuda", overrides=None) -> PrefillCase:
     sd = torch.from_numpy(slots).to(device)                    # the chunk's slots start as NaN
     kc[sd // 16, :, sd % 16, :] = nan
     vc[sd // 16, :, sd % 16, :] = nan
-    pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim, free_order=d.free_order)
+    if not fp8:
+        pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim, free_order=d.free_order)
+        pool.attach_device(torch.cuda.current_device())
+        return PrefillCase(w, d, tables, slots, pool, kc, vc, workloads.bf16_bits(kc), workloads.bf16_bits(vc))
+    # An E4M3 pool: the history positions (every position but the chunks') written through
+    # kv_append from their bf16 rows, the oracle encoding its own host copy; per-tensor scales
+    # amax / 448 over the history and the chunks, in fp32.  Every other byte starts as NaN.
+    hist = np.setdiff1d(oracle.all_slots(tables, d.seq_lens), slots)
+    hs = torch.from_numpy(hist).to(device)
+    k_src = kc[hs // 16, :, hs % 16, :].contiguous()
+    v_src = vc[hs // 16, :, hs % 16, :].contiguous()
+    kmax = max(k_src.float().abs().max().item() if len(hist) else 0.0, d.k_chunk.float().abs().max().item())
+    vmax = max(v_src.float().abs().max().item() if len(hist) else 0.0, d.v_chunk.float().abs().max().item())
+    k_scale = float(np.float32(kmax) / np.float32(448.0))
+    v_scale = float(np.float32(vmax) / np.float32(448.0))
+    pool = pkv.Pool(d.num_blocks, w.num_kv_heads, w.head_dim, pkv.KV_FP8E4M3, k_scale, v_scale, d.free_order)
     pool.attach_device(torch.cuda.current_device())
-    return PrefillCase(w, d, tables, slots, pool, kc, vc, workloads.bf16_bits(kc), workloads.bf16_bits(vc))
+    k8 = torch.full(kc.shape, FP8_NAN, dtype=torch.uint8, device=device)
+    v8 = torch.full(vc.shape, FP8_NAN, dtype=torch.uint8, device=device)
+    key_host = np.full(kc.shape, FP8_NAN, dtype=np.uint8)
+    value_host = np.full(vc.shape, FP8_NAN, dtype=np.uint8)
+    if len(hist):
+        assert oracle.kv_append(workloads.bf16_bits(k_src), workloads.bf16_bits(v_src), hist, key_host, value_host,
+                                16, oracle.FP8E4M3, k_scale, v_scale) == 0
+        pkv.kv_append(pool, k_src, v_src, hs, k8, v8)
+        torch.cuda.synchronize()
+    return PrefillCase(w, d, tables, slots, pool, k8, v8, key_host, value_host, pkv.KV_FP8E4M3, k_scale, v_scale)
 
 
 def prefill_append(c: PrefillCase):
@@ -337,7 +368,13 @@ def prefill_append(c: PrefillCase):
     np.testing.assert_array_equal(slots, c.slots)
     pkv.kv_append(c.pool, c.d.k_chunk, c.d.v_chunk, torch.from_numpy(slots).cuda(), c.key_cache, c.value_cache)
     assert oracle.kv_append(workloads.bf16_bits(c.d.k_chunk), workloads.bf16_bits(c.d.v_chunk), c.slots,
-                            c.key_host, c.value_host) == 0
+                            c.key_host, c.value_host, 16, oracle.FP8E4M3 if c.fp8 else oracle.BF16,
+                            c.k_scale, c.v_scale) == 0
+
+
+def prefill_pool_bits(c: PrefillCase, t: torch.Tensor) -> np.ndarray:
+    """A pool tensor as the host copies hold it (bf16 bit patterns, or E4M3 bytes)."""
+    return t.cpu().numpy() if c.fp8 else workloads.bf16_bits(t)
 
 
 def gpu_prefill(c: PrefillCase):
@@ -355,7 +392,8 @@ def oracle_prefill_rows(c: PrefillCase, rows=None, threads=None):
     is position L_b - P_b + i, i.e. a decode query of length position + 1."""
     if rows is None:
         st, out = oracle.paged_prefill(workloads.bf16_bits(c.d.q), c.key_host, c.value_host, c.tables,
-                                       c.d.seq_lens, c.d.cu_q, c.w.scale, c.w.num_kv_heads,
+                                       c.d.seq_lens, c.d.cu_q, c.w.scale, c.w.num_kv_heads, 16,
+                                       oracle.FP8E4M3 if c.fp8 else oracle.BF16, c.k_scale, c.v_scale,
                                        num_threads=threads or oracle.max_threads())
         assert st == 0
         return out
@@ -363,7 +401,8 @@ def oracle_prefill_rows(c: PrefillCase, rows=None, threads=None):
     seq = np.searchsorted(c.d.cu_q, rows, side="right") - 1
     lens = (c.d.seq_lens[seq] - c.d.chunk_lens[seq] + (rows - c.d.cu_q[seq]) + 1).astype(np.int32)
     st, out = oracle.paged_decode(workloads.bf16_bits(c.d.q)[rows], c.key_host, c.value_host,
-                                  np.ascontiguousarray(c.tables[seq]), lens, c.w.scale, c.w.num_kv_heads,
+                                  np.ascontiguousarray(c.tables[seq]), lens, c.w.scale, c.w.num_kv_heads, 16,
+                                  oracle.FP8E4M3 if c.fp8 else oracle.BF16, c.k_scale, c.v_scale,
                                   num_threads=threads or oracle.max_threads())
     assert st == 0
     return out

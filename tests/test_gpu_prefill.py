@@ -24,11 +24,12 @@ def _gpu():
     torch.cuda.set_device(0)
 
 
-def _run(name, overrides=None, rows=None):
-    c = C.build_prefill(name, overrides=overrides)
+def _run(name, overrides=None, rows=None, fp8=False):
+    c = C.build_prefill(name, overrides=overrides, fp8=fp8)
     C.prefill_append(c)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(workloads.bf16_bits(c.key_cache), c.key_host)
+    np.testing.assert_array_equal(C.prefill_pool_bits(c, c.key_cache), c.key_host)
+    np.testing.assert_array_equal(C.prefill_pool_bits(c, c.value_cache), c.value_host)
     out = C.gpu_prefill(c)
     ref = C.oracle_prefill_rows(c, rows)
     got = C.bf16_to_f64(out if rows is None else out[torch.as_tensor(rows)])
@@ -46,6 +47,21 @@ def test_prefill_heads_and_head_dims(Hq, Hkv, D):
     contexts long enough for several query tiles and several KV tiles per unit."""
     _run("prefill_tiny", {"num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "batch": 5,
                           "chunk": 300, "context": 420, "seed": 159110 + Hq + D})
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 2, 128), (4, 4, 64), (28, 4, 128), (16, 2, 64), (32, 2, 128)])
+def test_prefill_fp8_pool(Hq, Hkv, D):
+    """An E4M3 pool ("KV Cache 与推理优化", KV 量化: the cache stored in FP8, the arithmetic in
+    higher precision): the tiles are converted to bf16 on the chip, the scales applied to the
+    scores and the output.  The oracle decodes its own E4M3 copy of the pool."""
+    _run("prefill_tiny", {"num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "batch": 5,
+                          "chunk": 300, "context": 420, "seed": 159130 + Hq + D}, fp8=True)
+
+
+@pytest.mark.parametrize("chunk,context", [(1, 0), (129, 0), (16, 16), (257, 1), (64, 700)])
+def test_prefill_fp8_edge_lengths(chunk, context):
+    _run("prefill_tiny", {"ragged": False, "chunk": chunk, "context": context, "batch": 4,
+                          "head_dim": 128, "seed": 159140 + chunk + context}, fp8=True)
 
 
 @pytest.mark.parametrize("chunk,context", [(1, 0), (1, 700), (16, 16), (129, 0), (128, 128), (257, 1)])
@@ -77,6 +93,22 @@ def test_chunked_prefill_llama3_8b_full_size_sampled():
     pos = np.array([0, 1, 31, 32, 255, 256, 510, 511])
     rows = np.concatenate([b * 512 + pos for b in range(w.batch)])
     _run("chunked_prefill_llama3_8b", rows=rows)
+
+
+def test_chunked_prefill_llama3_8b_fp8_full_size_sampled():
+    """The chunked workload over an E4M3 pool: contexts up to 8192 cached positions, so every
+    unit streams many converted tiles."""
+    w = workloads.PREFILL_WORKLOADS["chunked_prefill_llama3_8b"]
+    pos = np.array([0, 1, 255, 256, 511])
+    rows = np.concatenate([b * 512 + pos for b in range(w.batch)])
+    _run("chunked_prefill_llama3_8b", rows=rows, fp8=True)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_fp8_sequences_without_new_rows(D):
+    _run("prefill_tiny", {"batch": 5, "head_dim": D, "num_q_heads": 8, "num_kv_heads": 2,
+                          "chunk_list": (40, 0, 129, 0, 1), "context_list": (37, 50, 0, 300, 16),
+                          "seed": 159150 + D}, fp8=True)
 
 
 def _plan_units(buf, grid):

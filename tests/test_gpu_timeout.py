@@ -94,11 +94,12 @@ def test_decode_step_wait_runs_out_then_the_step_reruns():
     C.tol_check(C.bf16_to_f64(out), C.oracle_decode(c))
 
 
-def test_prefill_wait_runs_out_then_the_context_is_usable():
-    c = C.build_prefill("prefill_tiny", overrides={"head_dim": 128, "num_q_heads": 8, "num_kv_heads": 2})
+@pytest.mark.parametrize("fp8", [False, True], ids=["bf16", "fp8"])
+def test_prefill_wait_runs_out_then_the_context_is_usable(fp8):
+    c = C.build_prefill("prefill_tiny", overrides={"head_dim": 128, "num_q_heads": 8, "num_kv_heads": 2}, fp8=fp8)
     C.prefill_append(c)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(workloads.bf16_bits(c.key_cache), c.key_host)
+    np.testing.assert_array_equal(C.prefill_pool_bits(c, c.key_cache), c.key_host)
     plan, grid = pkv.prefill_plan(c.pool, c.d.cu_q, c.d.seq_lens, c.w.num_q_heads, c.tables.shape[1])
     plan_d = torch.from_numpy(plan).cuda()
     bt = torch.from_numpy(c.tables).cuda()

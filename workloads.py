@@ -208,6 +208,7 @@ class PrefillWorkload:
     seed: int = 159100
     chunk_list: tuple = ()       # explicit P_b per sequence (with context_list), overriding the above
     context_list: tuple = ()
+    kv_dtype: str = "bf16"       # the pool: "bf16", or "fp8" (E4M3, per-tensor scales amax / 448)
 
     @property
     def scale(self) -> float:
@@ -222,6 +223,10 @@ PREFILL_WORKLOADS = {
     "chunked_prefill_llama3_8b": PrefillWorkload("chunked_prefill_llama3_8b", 16, 32, 8, 128,
                                                  chunk=512, context=8192, ragged=False,
                                                  seed=159102),
+    # the same chunked batch over an FP8 E4M3 pool
+    "chunked_prefill_llama3_8b_fp8": PrefillWorkload("chunked_prefill_llama3_8b_fp8", 16, 32, 8, 128,
+                                                     chunk=512, context=8192, ragged=False,
+                                                     seed=159102, kv_dtype="fp8"),
 }
 
 
